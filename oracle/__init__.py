@@ -1,0 +1,163 @@
+"""float64 CPU oracle for the selective state-space scan (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may load it.  It shares no code with the CUDA library in
+``selective_state_space_113_b300``; the two meet only in the seeded input
+generators of ``selective_state_space_113_b300.workloads``, which hold none of
+the method's arithmetic.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain C, float64, sequential in t);
+this module compiles it with gcc and calls it through ctypes.  ctypes releases
+the GIL during the call, so independent channel ranges run on a thread pool.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "ssm_oracle.c")
+LIB = os.path.join(HERE, "libssmoracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+def build(src: str = SRC, out: str = LIB, extra_flags=()) -> str:
+    """Compile the oracle with gcc into a shared library and return its path."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           *extra_flags, "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.oracle_scan_fwd.restype = ctypes.c_int
+    lib.oracle_scan_fwd.argtypes = [vp] * 10 + [i64] * 4 + [ctypes.c_int, i64, i64]
+    lib.oracle_step.restype = ctypes.c_int
+    lib.oracle_step.argtypes = [vp] * 10 + [i64] * 3 + [ctypes.c_int]
+    lib.oracle_abi_version.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) an oracle library.
+
+    With ``path`` given, loads that build (the planted-mistake tests use
+    this); otherwise the cached default build next to this file.
+    """
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if (not os.path.exists(LIB)
+                    or os.path.getmtime(LIB) < os.path.getmtime(SRC)):
+                build()
+            lib = _bind(ctypes.CDLL(LIB))
+            if lib.oracle_abi_version() != 1:
+                raise RuntimeError("stale oracle build: " + LIB)
+            _lib = lib
+        return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _as_input(a, dtype: int):
+    """Return a C-contiguous numpy view of an input tensor in the oracle's dtype.
+
+    float32 inputs stay float32; bfloat16 inputs must arrive as uint16 bit
+    patterns (see ``bits_of``).
+    """
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    want = np.float32 if dtype == F32 else np.uint16
+    if a.dtype != want:
+        raise TypeError(f"expected {want.__name__} input, got {a.dtype}")
+    return a
+
+
+def _as_f32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def bits_of(t) -> np.ndarray:
+    """Host numpy array of a torch tensor: float32 as is, bf16 as uint16 bits."""
+    import torch
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.numpy()
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def scan_fwd(u, delta, dt_bias, A, B, C, Dskip, z, dtype: int = F32,
+             threads: int = 1, lib: ctypes.CDLL | None = None):
+    """Selective scan, float64.  Shapes: u/delta/z [Bt,L,D], B/C [Bt,L,N], A [D,N].
+
+    Returns ``(y [Bt,L,D] float64, h_last [Bt,D,N] float64)``.
+    """
+    lib = lib or load()
+    u, delta, z = (_as_input(x, dtype) for x in (u, delta, z))
+    B, C = _as_input(B, dtype), _as_input(C, dtype)
+    A, dt_bias, Dskip = _as_f32(A), _as_f32(dt_bias), _as_f32(Dskip)
+    batch, L, D = u.shape
+    N = A.shape[1]
+    if A.shape != (D, N) or B.shape != (batch, L, N) or C.shape != (batch, L, N):
+        raise ValueError("inconsistent shapes")
+    y = np.zeros((batch, L, D), np.float64)
+    h = np.zeros((batch, D, N), np.float64)
+    threads = max(1, min(int(threads), D)) if D else 1
+
+    def run(lo, hi):
+        rc = lib.oracle_scan_fwd(_ptr(u), _ptr(delta), _ptr(dt_bias), _ptr(A),
+                                 _ptr(B), _ptr(C), _ptr(Dskip), _ptr(z),
+                                 _ptr(y), _ptr(h), batch, L, D, N, dtype, lo, hi)
+        if rc != 0:
+            raise RuntimeError(f"oracle_scan_fwd returned {rc}")
+
+    if threads == 1:
+        run(0, D)
+    else:
+        bounds = np.linspace(0, D, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])),
+                        range(threads)))
+    return y, h
+
+
+def step(state, u, delta, dt_bias, A, B, C, Dskip, z, dtype: int = F32,
+         lib: ctypes.CDLL | None = None):
+    """One decode step, float64.  state [Bt,D,N] (copied), u/delta/z [Bt,D], B/C [Bt,N].
+
+    Returns ``(new_state, y [Bt,D])``.
+    """
+    lib = lib or load()
+    u, delta, z = (_as_input(x, dtype) for x in (u, delta, z))
+    B, C = _as_input(B, dtype), _as_input(C, dtype)
+    A, dt_bias, Dskip = _as_f32(A), _as_f32(dt_bias), _as_f32(Dskip)
+    st = np.array(state, dtype=np.float64, order="C", copy=True)
+    batch, D = u.shape
+    N = A.shape[1]
+    if st.shape != (batch, D, N) or B.shape != (batch, N):
+        raise ValueError("inconsistent shapes")
+    y = np.zeros((batch, D), np.float64)
+    rc = lib.oracle_step(_ptr(st), _ptr(u), _ptr(delta), _ptr(dt_bias), _ptr(A),
+                         _ptr(B), _ptr(C), _ptr(Dskip), _ptr(z), _ptr(y),
+                         batch, D, N, dtype)
+    if rc != 0:
+        raise RuntimeError(f"oracle_step returned {rc}")
+    return st, y

@@ -1,0 +1,191 @@
+/*
+ * ssm_oracle.c -- float64 CPU oracle for the selective state-space scan and
+ * its single-token decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * definition that the CUDA library is checked against.  Only the test suite,
+ * the package smoke check and the benchmark's CPU-baseline leg may load it.
+ * It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (sources are the pages on Mamba / selective SSMs):
+ *   - "Mamba と状態空間モデル(SSM)" (ta-paperlens), section "Mamba: 状態を
+ *     「選択的」にする", pseudocode: dt = softplus(x W_d + bias), A stays a
+ *     learned parameter, the state update and y_t = C_t h.
+ *   - "State Space Models (SSM)" (ultralytics glossary), section "SSMの仕組み",
+ *     code listing: zero-order hold  A_bar = exp(delta*A),
+ *     B_bar = (A_bar - 1)/A * B,  h = A_bar*h + B_bar*x_t,  y_t = C h,
+ *     starting from h = 0.
+ *   - news.han.ihouse.idv.tw article 1304, output equation y = C h + D x
+ *     (the skip term D).
+ *   - agenticai-flow Mamba guide, block diagram: the S6 output is multiplied
+ *     element-wise by SiLU(z).
+ *
+ * Per batch b, channel d, step t, state n (sequential in t, h starts at 0):
+ *   dt      = softplus(delta[b,t,d] + dt_bias[d])
+ *   Abar    = exp(dt * A[d,n])
+ *   Bbar    = (exp(dt*A[d,n]) - 1) / A[d,n] * B[b,t,n]     (expm1 form; the
+ *             limit dt*B[b,t,n] when A[d,n] == 0)
+ *   h[n]    = Abar * h[n] + Bbar * u[b,t,d]
+ *   y[b,t,d]= (sum_n C[b,t,n] * h[n] + Dskip[d] * u[b,t,d]) * silu(z[b,t,d])
+ *   h_last[b,d,n] = h[n] after the last step.
+ *
+ * Layouts (row-major): u, delta, z, y: [B, L, D];  B, C: [B, L, N];
+ * A: [D, N];  dt_bias, Dskip: [D];  h_last / state: [B, D, N].
+ * dtype 0: u, delta, z, B, C are float32; dtype 1: they are bfloat16, decoded
+ * exactly (bf16 is the top half of a float32).  dt_bias, A, Dskip are float32.
+ * Optional inputs: dt_bias == NULL means 0, Dskip == NULL means 0,
+ * z == NULL means no gate.  h_last == NULL means it is not written.
+ *
+ * Every function here is pinned by tests/test_oracle_pins.py against values
+ * fixed by the pages and by mathematics (the convolution form, brute-force
+ * unrolling, a continuous-time ODE solve, closed forms, library routines).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Read element i of an input tensor of the given dtype, as a double. */
+static double load_elem(const void *p, int64_t i, int dtype)
+{
+    if (dtype == 0)
+        return (double)((const float *)p)[i];
+    /* bfloat16: the 16 stored bits are the high half of a float32. */
+    uint16_t bits16 = ((const uint16_t *)p)[i];
+    uint32_t bits32 = (uint32_t)bits16 << 16;
+    float f;
+    memcpy(&f, &bits32, sizeof f);
+    return (double)f;
+}
+
+/* softplus(x) = log(1 + exp(x)), written in the overflow-free form. */
+static double softplus(double x)
+{
+    return fmax(x, 0.0) + log1p(exp(-fabs(x)));
+}
+
+/* SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)). */
+static double silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/*
+ * Zero-order-hold pair for one (dt, a):  *abar = exp(dt a) and
+ * *bcoef = Bbar / B = (exp(dt a) - 1) / a, whose limit at a == 0 is dt.
+ */
+static void zoh(double dt, double a, double *abar, double *bcoef)
+{
+    *abar = exp(dt * a);
+    *bcoef = (a == 0.0) ? dt : expm1(dt * a) / a;
+}
+
+/*
+ * One selective-scan channel (b, d): runs the recurrence over all L steps.
+ * Writes y for that channel into y[(b*L + t)*D + d] and, if h_last is not
+ * NULL, the final state into h_last[(b*D + d)*N + n].  h is N doubles of
+ * scratch.
+ */
+static void scan_channel(const void *u, const void *delta, const float *dt_bias,
+                         const float *A, const void *B, const void *C,
+                         const float *Dskip, const void *z, double *y,
+                         double *h_last, int64_t b, int64_t d, int64_t L,
+                         int64_t D, int64_t N, int dtype, double *h)
+{
+    for (int64_t n = 0; n < N; n++)
+        h[n] = 0.0;
+    double bias = dt_bias ? (double)dt_bias[d] : 0.0;
+    double dsk = Dskip ? (double)Dskip[d] : 0.0;
+    for (int64_t t = 0; t < L; t++) {
+        int64_t i_btd = (b * L + t) * D + d;
+        double ut = load_elem(u, i_btd, dtype);
+        double dt = softplus(load_elem(delta, i_btd, dtype) + bias);
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; n++) {
+            double abar, bcoef;
+            zoh(dt, (double)A[d * N + n], &abar, &bcoef);
+            double bt = load_elem(B, (b * L + t) * N + n, dtype);
+            double ct = load_elem(C, (b * L + t) * N + n, dtype);
+            h[n] = abar * h[n] + bcoef * bt * ut;
+            acc += ct * h[n];
+        }
+        acc += dsk * ut;
+        if (z)
+            acc *= silu(load_elem(z, i_btd, dtype));
+        y[i_btd] = acc;
+    }
+    if (h_last)
+        for (int64_t n = 0; n < N; n++)
+            h_last[(b * D + d) * N + n] = h[n];
+}
+
+/*
+ * Selective scan over channels d in [d_begin, d_end) of every batch entry.
+ * Returns 0, or -1 for a bad argument, -2 when scratch cannot be allocated.
+ * Callers may split the channel range across threads; channels are
+ * independent and each is computed exactly as above.
+ */
+int oracle_scan_fwd(const void *u, const void *delta, const float *dt_bias,
+                    const float *A, const void *B, const void *C,
+                    const float *Dskip, const void *z, double *y,
+                    double *h_last, int64_t batch, int64_t L, int64_t D,
+                    int64_t N, int dtype, int64_t d_begin, int64_t d_end)
+{
+    if (!u || !delta || !A || !B || !C || !y)
+        return -1;
+    if (batch < 0 || L < 0 || D < 0 || N < 1 || (dtype != 0 && dtype != 1))
+        return -1;
+    if (d_begin < 0 || d_end > D || d_begin > d_end)
+        return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!h)
+        return -2;
+    for (int64_t b = 0; b < batch; b++)
+        for (int64_t d = d_begin; d < d_end; d++)
+            scan_channel(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, b, d,
+                         L, D, N, dtype, h);
+    free(h);
+    return 0;
+}
+
+/*
+ * Single-token decode step: the same per-token update as one step of the
+ * scan, applied to a stored state.  state: [B, D, N] float64, updated in
+ * place; u, delta, z, y: [B, D]; B, C: [B, N].
+ */
+int oracle_step(double *state, const void *u, const void *delta,
+                const float *dt_bias, const float *A, const void *B,
+                const void *C, const float *Dskip, const void *z, double *y,
+                int64_t batch, int64_t D, int64_t N, int dtype)
+{
+    if (!state || !u || !delta || !A || !B || !C || !y)
+        return -1;
+    if (batch < 0 || D < 0 || N < 1 || (dtype != 0 && dtype != 1))
+        return -1;
+    for (int64_t b = 0; b < batch; b++) {
+        for (int64_t d = 0; d < D; d++) {
+            int64_t i_bd = b * D + d;
+            double ut = load_elem(u, i_bd, dtype);
+            double bias = dt_bias ? (double)dt_bias[d] : 0.0;
+            double dt = softplus(load_elem(delta, i_bd, dtype) + bias);
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; n++) {
+                double abar, bcoef;
+                zoh(dt, (double)A[d * N + n], &abar, &bcoef);
+                double bt = load_elem(B, b * N + n, dtype);
+                double ct = load_elem(C, b * N + n, dtype);
+                double *hp = &state[i_bd * N + n];
+                *hp = abar * *hp + bcoef * bt * ut;
+                acc += ct * *hp;
+            }
+            acc += (Dskip ? (double)Dskip[d] : 0.0) * ut;
+            if (z)
+                acc *= silu(load_elem(z, i_bd, dtype));
+            y[i_bd] = acc;
+        }
+    }
+    return 0;
+}
+
+/* ABI probe used by the Python wrapper to refuse a stale build. */
+int oracle_abi_version(void) { return 1; }

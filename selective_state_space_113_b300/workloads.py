@@ -1,0 +1,154 @@
+"""Seeded synthetic inputs for the selective scan and the decode step.
+
+This module only draws random inputs; it holds none of the scan's arithmetic.
+Both the CUDA library's tests/benchmarks and the float64 oracle consume what it
+produces, so the two sides always see bit-identical inputs.
+
+Recipe (the shapes are Mamba layers; the distributions are the ones the
+workload definitions fix):
+  u, delta, z ~ N(0, 1)   [batch, L, D]      (cast to the workload dtype)
+  B, C        ~ N(0, 1)   [batch, L, N]      (cast to the workload dtype)
+  dt0         = exp(U(log 1e-3, log 1e-1))   per channel, float32
+  dt_bias     = log(expm1(dt0))              per channel, float32
+                (so softplus(dt_bias) = dt0: the usual Mamba dt initialisation)
+  Dskip       ~ N(0, 1)   [D]                float32
+  A[d, n]     = -(n + 1)                     float32 (S4D-real / Mamba init)
+  decode state ~ N(0, 1)  [batch, D, N]      float32
+Draws happen in float32 from one torch.Generator seeded with the workload's
+seed, in the order listed, then are rounded to bf16 where the workload is bf16.
+The time-invariant variant repeats the t = 0 draws of delta, B and C along t.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class ScanWorkload:
+    name: str
+    batch: int
+    L: int
+    D: int
+    N: int
+    dtype: torch.dtype
+    seed: int
+    time_invariant: bool = False
+
+    @property
+    def elements(self) -> int:
+        return self.batch * self.L * self.D
+
+
+@dataclasses.dataclass(frozen=True)
+class StepWorkload:
+    name: str
+    batch: int
+    D: int
+    N: int
+    steps: int
+    dtype: torch.dtype
+    seed: int
+
+    @property
+    def elements_per_step(self) -> int:
+        return self.batch * self.D
+
+
+# The five workloads: a tiny fp32 scan (plus its time-invariant variant), the
+# Mamba-130M and Mamba-2.8B shaped layer scans, a 2^20-step scan and a
+# 64-token decode of 256 sequences.
+TINY_F32 = ScanWorkload("tiny_f32_2x256x64_n16", 2, 256, 64, 16, torch.float32, 0)
+TINY_F32_LTI = ScanWorkload("tiny_f32_lti_2x256x64_n16", 2, 256, 64, 16,
+                            torch.float32, 0, time_invariant=True)
+MAMBA_130M = ScanWorkload("mamba130m_8x2048x1536_n16_bf16", 8, 2048, 1536, 16,
+                          torch.bfloat16, 1)
+MAMBA_2P8B = ScanWorkload("mamba2.8b_4x4096x5120_n16_bf16", 4, 4096, 5120, 16,
+                          torch.bfloat16, 2)
+LONG_SEQ = ScanWorkload("longseq_1x1048576x1536_n16_bf16", 1, 1 << 20, 1536, 16,
+                        torch.bfloat16, 3)
+DECODE = StepWorkload("decode_256x5120_n16_bf16_64steps", 256, 5120, 16, 64,
+                      torch.bfloat16, 4)
+
+SCAN_WORKLOADS = {w.name: w for w in (TINY_F32, TINY_F32_LTI, MAMBA_130M,
+                                      MAMBA_2P8B, LONG_SEQ)}
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _randn(shape, g, device, dtype):
+    return torch.randn(shape, generator=g, device=device,
+                       dtype=torch.float32).to(dtype)
+
+
+def channel_params(D: int, N: int, g: torch.Generator, device):
+    """dt_bias, Dskip and A for D channels (all float32)."""
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt0 = torch.exp(torch.rand(D, generator=g, device=device) * (hi - lo) + lo)
+    dt_bias = torch.log(torch.expm1(dt0)).to(torch.float32)
+    Dskip = torch.randn(D, generator=g, device=device, dtype=torch.float32)
+    A = -(torch.arange(N, device=device, dtype=torch.float32) + 1.0)
+    A = A.unsqueeze(0).repeat(D, 1).contiguous()
+    return dt_bias, Dskip, A
+
+
+def make_scan_inputs(w: ScanWorkload, device="cpu", seed: int | None = None,
+                     batch: int | None = None, L: int | None = None,
+                     D: int | None = None, N: int | None = None):
+    """All inputs of one scan workload as a dict of tensors on ``device``.
+
+    ``batch``/``L``/``D``/``N``/``seed`` override the workload's values (used
+    for smaller parity cases with the same distributions).
+    """
+    batch = w.batch if batch is None else batch
+    L = w.L if L is None else L
+    D = w.D if D is None else D
+    N = w.N if N is None else N
+    g = _gen(w.seed if seed is None else seed, device)
+    dt = w.dtype
+    if w.time_invariant:
+        u = _randn((batch, L, D), g, device, dt)
+        delta = _randn((batch, 1, D), g, device, dt).expand(batch, L, D).contiguous()
+        z = _randn((batch, L, D), g, device, dt)
+        B = _randn((batch, 1, N), g, device, dt).expand(batch, L, N).contiguous()
+        C = _randn((batch, 1, N), g, device, dt).expand(batch, L, N).contiguous()
+    else:
+        u = _randn((batch, L, D), g, device, dt)
+        delta = _randn((batch, L, D), g, device, dt)
+        z = _randn((batch, L, D), g, device, dt)
+        B = _randn((batch, L, N), g, device, dt)
+        C = _randn((batch, L, N), g, device, dt)
+    dt_bias, Dskip, A = channel_params(D, N, g, device)
+    return dict(u=u, delta=delta, dt_bias=dt_bias, A=A, B=B, C=C, Dskip=Dskip, z=z)
+
+
+def make_step_inputs(w: StepWorkload, device="cpu", seed: int | None = None,
+                     batch: int | None = None, D: int | None = None,
+                     N: int | None = None, steps: int | None = None):
+    """Decode inputs: per-step tensors stacked on a leading ``steps`` axis.
+
+    Returns dict with state [batch,D,N] f32, u/delta/z [steps,batch,D],
+    B/C [steps,batch,N] (workload dtype) and dt_bias/Dskip/A.
+    """
+    batch = w.batch if batch is None else batch
+    D = w.D if D is None else D
+    N = w.N if N is None else N
+    steps = w.steps if steps is None else steps
+    g = _gen(w.seed if seed is None else seed, device)
+    dt = w.dtype
+    state = torch.randn((batch, D, N), generator=g, device=device,
+                        dtype=torch.float32)
+    u = _randn((steps, batch, D), g, device, dt)
+    delta = _randn((steps, batch, D), g, device, dt)
+    z = _randn((steps, batch, D), g, device, dt)
+    B = _randn((steps, batch, N), g, device, dt)
+    C = _randn((steps, batch, N), g, device, dt)
+    dt_bias, Dskip, A = channel_params(D, N, g, device)
+    return dict(state=state, u=u, delta=delta, dt_bias=dt_bias, A=A, B=B, C=C,
+                Dskip=Dskip, z=z)

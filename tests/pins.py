@@ -1,0 +1,441 @@
+"""Pins for the float64 oracle: checks against values fixed by the pages and by
+mathematics, each independent of the oracle's own code.
+
+Every pin takes an oracle library handle (``oracle.load()`` or a build with a
+planted mistake) and raises AssertionError when the oracle disagrees.  The
+references here use library routines (scipy's zero-order-hold discretisation,
+scipy's IIR filter, an adaptive ODE solver, numpy/torch softplus and SiLU) or
+closed forms, never a retyped copy of the oracle's recurrence.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import scipy.integrate
+import scipy.signal
+import scipy.special
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ----------------------------------------------------------------- helpers
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def softplus_ref(x):
+    """softplus via numpy's log-add-exp: log(exp(0) + exp(x))."""
+    return np.logaddexp(0.0, np.asarray(x, np.float64))
+
+
+def silu_ref(z):
+    """SiLU via scipy's logistic function."""
+    z = np.asarray(z, np.float64)
+    return z * scipy.special.expit(z)
+
+
+def zoh_ref(a: float, dt: float):
+    """(Abar, Bbar/B) of the scalar system h' = a h + 1*x, by scipy's ZOH."""
+    Ad, Bd, _, _, _ = scipy.signal.cont2discrete(
+        (np.array([[a]]), np.array([[1.0]]), np.array([[1.0]]), np.array([[0.0]])),
+        dt, method="zoh")
+    return float(Ad[0, 0]), float(Bd[0, 0])
+
+
+def random_problem(rng, batch, L, D, N, gate=True, skip=True, bias=True):
+    """Small random float32 selective-scan problem (time-varying everything)."""
+    u = _f32(rng.standard_normal((batch, L, D)))
+    delta = _f32(rng.standard_normal((batch, L, D)))
+    z = _f32(rng.standard_normal((batch, L, D))) if gate else None
+    B = _f32(rng.standard_normal((batch, L, N)))
+    C = _f32(rng.standard_normal((batch, L, N)))
+    # distinct, negative A entries (a generic diagonal A, not the -(n+1) init)
+    A = _f32(-(0.2 + 2.0 * rng.random((D, N))))
+    dt_bias = _f32(np.log(np.expm1(np.exp(rng.uniform(np.log(1e-2), np.log(0.5), D)))))
+    Dskip = _f32(rng.standard_normal(D)) if skip else None
+    return dict(u=u, delta=delta, dt_bias=dt_bias if bias else None, A=A, B=B,
+                C=C, Dskip=Dskip, z=z)
+
+
+def scan(lib, p, dtype=oracle.F32):
+    return oracle.scan_fwd(p["u"], p["delta"], p["dt_bias"], p["A"], p["B"],
+                           p["C"], p["Dskip"], p["z"], dtype=dtype, lib=lib)
+
+
+def _close(got, want, rtol, atol, what):
+    got, want = np.asarray(got), np.asarray(want)
+    assert got.shape == want.shape, f"{what}: shape {got.shape} != {want.shape}"
+    err = np.abs(got - want)
+    bound = atol + rtol * np.abs(want)
+    bad = ~(err <= bound)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} mismatches, max err "
+                           f"{float(np.nanmax(err)):.3e}")
+
+
+# ------------------------------------------------------------------- pins
+def pin_p2_worked_example(lib):
+    """Ultralytics page, 'SSMの仕組み' listing: recurrent form == convolution form.
+
+    Same inputs as the listing (torch seed 0, L=64, N=16, A = -(U+0.5),
+    delta = 0.1); the page prints only 'Same outputs: True' at atol 1e-5.
+    The convolution kernel K_k = C . (Abar^k * Bbar) is evaluated directly.
+    """
+    with open(os.path.join(GOLDEN, "p2_worked_example.json")) as f:
+        gold = json.load(f)
+    L, N = gold["L"], gold["N"]
+    torch.manual_seed(gold["seed"])
+    x = torch.randn(L)
+    A = -(torch.rand(N) + 0.5)
+    Bv, Cv = torch.randn(N), torch.randn(N)
+    dt_target = gold["delta"]
+    dt_bias = _f32([math.log(math.expm1(dt_target))])
+    dt = float(softplus_ref(dt_bias.astype(np.float64))[0])  # what the oracle sees
+    p = dict(u=_f32(x.numpy().reshape(1, L, 1)),
+             delta=_f32(np.zeros((1, L, 1))), dt_bias=dt_bias,
+             A=_f32(A.numpy().reshape(1, N)),
+             B=_f32(np.tile(Bv.numpy(), (1, L, 1))),
+             C=_f32(np.tile(Cv.numpy(), (1, L, 1))), Dskip=None, z=None)
+    y, _ = scan(lib, p)
+    a = A.numpy().astype(np.float64)
+    abar = np.exp(dt * a)
+    bbar = (abar - 1.0) / a * Bv.numpy().astype(np.float64)
+    K = np.array([Cv.numpy().astype(np.float64) @ (abar ** k * bbar) for k in range(L)])
+    xs = x.numpy().astype(np.float64)
+    y_conv = np.array([K[: t + 1][::-1] @ xs[: t + 1] for t in range(L)])
+    same = bool(np.allclose(y[0, :, 0], y_conv, atol=gold["atol"]))
+    assert same == gold["expected_same_outputs"], "page's identity does not hold"
+    _close(y[0, :, 0], y_conv, 1e-11, 1e-12, "recurrent vs convolution")
+
+
+def pin_lti_convolution_with_skip_and_gate(lib):
+    """Time-invariant variant (dt, B, C constant in t): y_t = silu(z_t) *
+    (sum_k K_k[d] u_{t-k} + D u_t), K_k[d] = sum_n C_n Abar^k Bbar B_n, with
+    Abar/Bbar from scipy's ZOH (several channels, batch 2)."""
+    rng = np.random.default_rng(11)
+    batch, L, D, N = 2, 40, 3, 5
+    p = random_problem(rng, batch, L, D, N)
+    for key in ("delta", "B", "C"):
+        p[key] = _f32(np.repeat(p[key][:, :1, :], L, axis=1))
+    y, h = scan(lib, p)
+    for b in range(batch):
+        for d in range(D):
+            dt = float(softplus_ref(p["delta"][b, 0, d] + np.float64(p["dt_bias"][d])))
+            K = np.zeros(L)
+            for n in range(N):
+                ad, bd = zoh_ref(float(p["A"][d, n]), dt)
+                K += float(p["C"][b, 0, n]) * ad ** np.arange(L) * bd * float(p["B"][b, 0, n])
+            us = p["u"][b, :, d].astype(np.float64)
+            conv = np.array([K[: t + 1][::-1] @ us[: t + 1] for t in range(L)])
+            want = (conv + float(p["Dskip"][d]) * us) * silu_ref(p["z"][b, :, d])
+            _close(y[b, :, d], want, 1e-10, 1e-12, f"LTI conv b={b} d={d}")
+
+
+def pin_bruteforce_unrolled(lib):
+    """Selective (time-varying) case by brute force: h_t = sum_{s<=t}
+    (prod_{r=s+1..t} Abar_r) Bbar_s B_s u_s, no recurrence; ZOH from scipy,
+    softplus from numpy, SiLU from scipy."""
+    rng = np.random.default_rng(5)
+    batch, L, D, N = 2, 12, 3, 4
+    p = random_problem(rng, batch, L, D, N)
+    y, h = scan(lib, p)
+    for b in range(batch):
+        for d in range(D):
+            dts = softplus_ref(p["delta"][b, :, d].astype(np.float64)
+                               + np.float64(p["dt_bias"][d]))
+            hs = np.zeros((L, N))
+            for n in range(N):
+                pairs = [zoh_ref(float(p["A"][d, n]), float(dt)) for dt in dts]
+                for t in range(L):
+                    tot = 0.0
+                    for s in range(t + 1):
+                        prod = 1.0
+                        for r in range(s + 1, t + 1):
+                            prod *= pairs[r][0]
+                        tot += prod * pairs[s][1] * float(p["B"][b, s, n]) * float(p["u"][b, s, d])
+                    hs[t, n] = tot
+            Ct = p["C"][b].astype(np.float64)
+            want = ((Ct * hs).sum(1) + float(p["Dskip"][d]) * p["u"][b, :, d].astype(np.float64)) \
+                * silu_ref(p["z"][b, :, d])
+            _close(y[b, :, d], want, 1e-10, 1e-12, f"unrolled y b={b} d={d}")
+            _close(h[b, d], hs[-1], 1e-10, 1e-12, f"unrolled h_last b={b} d={d}")
+
+
+def pin_continuous_time_ode(lib):
+    """Zero-order hold is exact for input held constant over each step
+    (ta-paperlens page, 仕組み: 'その区間では入力が一定だとみなす'): integrate
+    h' = A h + B_t u_t over consecutive intervals of length dt_t with an
+    adaptive ODE solver and compare the state and the readout."""
+    rng = np.random.default_rng(7)
+    batch, L, D, N = 1, 10, 2, 3
+    p = random_problem(rng, batch, L, D, N, gate=False)
+    y, h = scan(lib, p)
+    for d in range(D):
+        a = p["A"][d].astype(np.float64)
+        dts = softplus_ref(p["delta"][0, :, d].astype(np.float64) + np.float64(p["dt_bias"][d]))
+        state = np.zeros(N)
+        for t in range(L):
+            drive = p["B"][0, t].astype(np.float64) * float(p["u"][0, t, d])
+            sol = scipy.integrate.solve_ivp(lambda _s, x: a * x + drive, (0.0, dts[t]),
+                                            state, method="DOP853", rtol=1e-12, atol=1e-15)
+            state = sol.y[:, -1]
+            want_y = float(p["C"][0, t].astype(np.float64) @ state) \
+                + float(p["Dskip"][d]) * float(p["u"][0, t, d])
+            _close(y[0, t, d], want_y, 1e-8, 1e-10, f"ODE y t={t} d={d}")
+        _close(h[0, d], state, 1e-8, 1e-10, f"ODE h_last d={d}")
+
+
+def pin_constant_input_closed_form(lib):
+    """dt, B, u constant: h_t = (B u / -A) (1 - Abar^(t+1)) -> -B u / A."""
+    rng = np.random.default_rng(3)
+    batch, L, D, N = 1, 60, 2, 4
+    p = random_problem(rng, batch, L, D, N, gate=False, skip=False)
+    for key in ("delta", "B", "C", "u"):
+        p[key] = _f32(np.repeat(p[key][:, :1, :], L, axis=1))
+    y, h = scan(lib, p)
+    t = np.arange(L, dtype=np.float64)
+    for d in range(D):
+        dt = float(softplus_ref(p["delta"][0, 0, d] + np.float64(p["dt_bias"][d])))
+        uu = float(p["u"][0, 0, d])
+        hs = np.zeros((L, N))
+        for n in range(N):
+            a = float(p["A"][d, n])
+            hs[:, n] = (float(p["B"][0, 0, n]) * uu / -a) * (1.0 - np.exp(dt * a * (t + 1)))
+        _close(h[0, d], hs[-1], 1e-11, 1e-13, f"closed-form h d={d}")
+        _close(y[0, :, d], hs @ p["C"][0, 0].astype(np.float64), 1e-10, 1e-12,
+               f"closed-form y d={d}")
+
+
+def pin_small_dt_keeps_state(lib):
+    """dt -> 0 (delta + dt_bias = -40): the state keeps its value (ta-paperlens
+    page: a small Delta ignores the input) so h stays 0 and y = D u silu(z);
+    the decode step leaves a stored state unchanged."""
+    rng = np.random.default_rng(9)
+    batch, L, D, N = 2, 20, 3, 4
+    p = random_problem(rng, batch, L, D, N, bias=False)
+    p["delta"] = _f32(np.full((batch, L, D), -40.0))
+    y, h = scan(lib, p)
+    assert np.abs(h).max() < 1e-15, "state moved although dt ~ 4e-18"
+    want = p["Dskip"][None, None, :].astype(np.float64) * p["u"] \
+        * torch.nn.functional.silu(torch.from_numpy(p["z"].astype(np.float64))).numpy()
+    _close(y, want, 1e-12, 1e-14, "dt->0 readout")
+    st0 = rng.standard_normal((batch, D, N))
+    st1, _ = oracle.step(st0, p["u"][:, 0], p["delta"][:, 0], None, p["A"], p["B"][:, 0],
+                         p["C"][:, 0], p["Dskip"], p["z"][:, 0], lib=lib)
+    _close(st1, st0, 1e-15, 1e-15, "dt->0 step state")
+
+
+def pin_pure_decay(lib):
+    """B = 0 (eigenvalue argument of the ta-paperlens page): the step does
+    state <- exp(dt A) * state; the scan's impulse at t = 0 decays as
+    Bbar_0 u_0 exp(A sum_{s=1..t} dt_s)."""
+    rng = np.random.default_rng(4)
+    batch, D, N = 2, 3, 5
+    A = _f32(-(0.1 + 3 * rng.random((D, N))))
+    dt_bias = _f32(rng.standard_normal(D) - 2)
+    u = _f32(rng.standard_normal((batch, D)))
+    delta = _f32(rng.standard_normal((batch, D)))
+    z = _f32(rng.standard_normal((batch, D)))
+    C = _f32(rng.standard_normal((batch, N)))
+    Dskip = _f32(rng.standard_normal(D))
+    st0 = rng.standard_normal((batch, D, N))
+    st1, y1 = oracle.step(st0, u, delta, dt_bias, A, _f32(np.zeros((batch, N))), C,
+                          Dskip, z, lib=lib)
+    dt = softplus_ref(delta.astype(np.float64) + dt_bias[None, :])
+    decay = np.exp(dt[:, :, None] * A[None].astype(np.float64))
+    _close(st1, decay * st0, 1e-13, 1e-15, "step decay")
+    want_y = ((st1 * C[:, None, :]).sum(-1) + Dskip.astype(np.float64) * u) * silu_ref(z)
+    _close(y1, want_y, 1e-12, 1e-14, "step readout")
+    # scan impulse
+    L = 30
+    p = random_problem(rng, 1, L, D, N, gate=False, skip=False)
+    p["B"][:, 1:, :] = 0.0
+    y, h = scan(lib, p)
+    for d in range(D):
+        dts = softplus_ref(p["delta"][0, :, d].astype(np.float64) + np.float64(p["dt_bias"][d]))
+        for n in range(N):
+            a = float(p["A"][d, n])
+            _, bd0 = zoh_ref(a, float(dts[0]))
+            want = bd0 * float(p["B"][0, 0, n]) * float(p["u"][0, 0, d]) * math.exp(a * dts[1:].sum())
+            _close(h[0, d, n], want, 1e-11, 1e-15, f"impulse decay d={d} n={n}")
+
+
+def pin_ema_special_case(lib):
+    """N=1, A=-1, B=C=1, constant dt: h_t = e^-dt h + (1 - e^-dt) u_t, i.e. the
+    first-order IIR filter y = lfilter([alpha], [1, alpha-1], u)."""
+    rng = np.random.default_rng(2)
+    L = 200
+    dtb = 0.3
+    p = dict(u=_f32(rng.standard_normal((1, L, 1))), delta=_f32(np.zeros((1, L, 1))),
+             dt_bias=_f32([dtb]), A=_f32([[-1.0]]), B=_f32(np.ones((1, L, 1))),
+             C=_f32(np.ones((1, L, 1))), Dskip=None, z=None)
+    y, h = scan(lib, p)
+    dt = float(softplus_ref(np.float64(np.float32(dtb))))
+    alpha = -math.expm1(-dt)
+    want = scipy.signal.lfilter([alpha], [1.0, alpha - 1.0], p["u"][0, :, 0].astype(np.float64))
+    _close(y[0, :, 0], want, 1e-12, 1e-14, "EMA")
+
+
+def pin_zero_A_integrator(lib):
+    """A = 0: the ZOH input matrix tends to dt*B and the state integrates,
+    h_t = sum_{s<=t} dt_s B_s u_s (cumulative sum)."""
+    rng = np.random.default_rng(8)
+    L, N = 25, 3
+    p = random_problem(rng, 1, L, 1, N, gate=False, skip=False)
+    p["A"] = _f32(np.zeros((1, N)))
+    y, h = scan(lib, p)
+    dts = softplus_ref(p["delta"][0, :, 0].astype(np.float64) + np.float64(p["dt_bias"][0]))
+    hs = np.cumsum(dts[:, None] * p["B"][0].astype(np.float64) * p["u"][0, :, :1], axis=0)
+    _close(h[0, 0], hs[-1], 1e-12, 1e-14, "integrator h")
+    _close(y[0, :, 0], (hs * p["C"][0]).sum(1), 1e-11, 1e-13, "integrator y")
+
+
+def pin_scan_step_consistency(lib):
+    """Training form == inference form: L decode steps from a zero state give
+    the scan's y and h_last; scan(L1) + K steps == scan(L1 + K)."""
+    rng = np.random.default_rng(6)
+    batch, L, D, N = 2, 16, 3, 4
+    p = random_problem(rng, batch, L, D, N)
+    y, h = scan(lib, p)
+    st = np.zeros((batch, D, N))
+    ys = []
+    for t in range(L):
+        st, yt = oracle.step(st, p["u"][:, t], p["delta"][:, t], p["dt_bias"], p["A"],
+                             p["B"][:, t], p["C"][:, t], p["Dskip"], p["z"][:, t], lib=lib)
+        ys.append(yt)
+    _close(np.stack(ys, 1), y, 1e-13, 1e-15, "steps vs scan y")
+    _close(st, h, 1e-13, 1e-15, "steps vs scan h_last")
+    L1 = 9
+    q = {k: (v[:, :L1] if k in ("u", "delta", "z", "B", "C") else v) for k, v in p.items()}
+    _, h1 = scan(lib, q)
+    st = h1
+    for t in range(L1, L):
+        st, yt = oracle.step(st, p["u"][:, t], p["delta"][:, t], p["dt_bias"], p["A"],
+                             p["B"][:, t], p["C"][:, t], p["Dskip"], p["z"][:, t], lib=lib)
+        _close(yt, y[:, t], 1e-13, 1e-15, f"scan+step y t={t}")
+    _close(st, h, 1e-13, 1e-15, "scan+step h_last")
+
+
+def pin_channels_independent(lib):
+    """Each (b, d) channel is its own scan: running a channel alone (batch 1,
+    D 1, its own A row and parameters) reproduces the full run, and permuting
+    channels permutes outputs."""
+    rng = np.random.default_rng(12)
+    batch, L, D, N = 3, 10, 4, 3
+    p = random_problem(rng, batch, L, D, N)
+    y, h = scan(lib, p)
+    for b in range(batch):
+        for d in range(D):
+            q = dict(u=p["u"][b:b + 1, :, d:d + 1], delta=p["delta"][b:b + 1, :, d:d + 1],
+                     dt_bias=p["dt_bias"][d:d + 1], A=p["A"][d:d + 1],
+                     B=p["B"][b:b + 1], C=p["C"][b:b + 1], Dskip=p["Dskip"][d:d + 1],
+                     z=p["z"][b:b + 1, :, d:d + 1])
+            y1, h1 = scan(lib, q)
+            _close(y1[0, :, 0], y[b, :, d], 0, 0, f"channel alone b={b} d={d}")
+            _close(h1[0, 0], h[b, d], 0, 0, f"channel alone h b={b} d={d}")
+    perm = rng.permutation(D)
+    q = dict(p)
+    for k in ("u", "delta", "z"):
+        q[k] = _f32(p[k][:, :, perm])
+    for k in ("dt_bias", "Dskip"):
+        q[k] = _f32(p[k][perm])
+    q["A"] = _f32(p["A"][perm])
+    yp, hp = scan(lib, q)
+    _close(yp, y[:, :, perm], 0, 0, "permuted channels y")
+    _close(hp, h[:, perm], 0, 0, "permuted channels h")
+
+
+def pin_optional_inputs(lib):
+    """dt_bias = NULL is 0, Dskip = NULL is 0, z = NULL disables the gate
+    (then y * silu(z) equals the gated output)."""
+    rng = np.random.default_rng(13)
+    batch, L, D, N = 2, 8, 3, 4
+    p = random_problem(rng, batch, L, D, N)
+    y, h = scan(lib, p)
+    r = dict(p, dt_bias=_f32(np.zeros(D)))
+    _close(scan(lib, dict(p, dt_bias=None))[0], scan(lib, r)[0], 0, 0, "dt_bias NULL")
+    r = dict(p, Dskip=_f32(np.zeros(D)))
+    _close(scan(lib, dict(p, Dskip=None))[0], scan(lib, r)[0], 0, 0, "Dskip NULL")
+    yg, hg = scan(lib, dict(p, z=None))
+    _close(yg * silu_ref(p["z"]), y, 1e-13, 1e-15, "z NULL then gate")
+    _close(hg, h, 0, 0, "gate does not touch the state")
+
+
+def pin_bf16_decode(lib):
+    """bf16 inputs decode exactly: the bf16 run equals the float32 run on
+    torch's own bf16 -> float32 conversion of the same tensors."""
+    g = torch.Generator().manual_seed(21)
+    batch, L, D, N = 2, 12, 5, 4
+    bf = {k: torch.randn(s, generator=g).to(torch.bfloat16)
+          for k, s in (("u", (batch, L, D)), ("delta", (batch, L, D)),
+                       ("z", (batch, L, D)), ("B", (batch, L, N)), ("C", (batch, L, N)))}
+    rng = np.random.default_rng(21)
+    A = _f32(-(0.5 + rng.random((D, N))))
+    dt_bias = _f32(rng.standard_normal(D) - 2)
+    Dskip = _f32(rng.standard_normal(D))
+    pb = dict({k: oracle.bits_of(v) for k, v in bf.items()}, A=A, dt_bias=dt_bias, Dskip=Dskip)
+    pf = dict({k: v.to(torch.float32).numpy() for k, v in bf.items()}, A=A,
+              dt_bias=dt_bias, Dskip=Dskip)
+    yb, hb = scan(lib, pb, dtype=oracle.BF16)
+    yf, hf = scan(lib, pf, dtype=oracle.F32)
+    _close(yb, yf, 0, 0, "bf16 vs f32 decode y")
+    _close(hb, hf, 0, 0, "bf16 vs f32 decode h")
+    sb, ysb = oracle.step(np.ones((batch, D, N)), pb["u"][:, 0], pb["delta"][:, 0], dt_bias,
+                          A, pb["B"][:, 0], pb["C"][:, 0], Dskip, pb["z"][:, 0],
+                          dtype=oracle.BF16, lib=lib)
+    sf, ysf = oracle.step(np.ones((batch, D, N)), pf["u"][:, 0], pf["delta"][:, 0], dt_bias,
+                          A, pf["B"][:, 0], pf["C"][:, 0], Dskip, pf["z"][:, 0],
+                          dtype=oracle.F32, lib=lib)
+    _close(sb, sf, 0, 0, "bf16 step state")
+    _close(ysb, ysf, 0, 0, "bf16 step y")
+
+
+def pin_step_matches_library_pipeline(lib):
+    """One decode step from a random state, every stage from a library
+    routine: softplus (torch), ZOH (scipy), SiLU (torch)."""
+    rng = np.random.default_rng(17)
+    batch, D, N = 2, 3, 4
+    A = _f32(-(0.2 + 2 * rng.random((D, N))))
+    dt_bias = _f32(rng.standard_normal(D) - 1)
+    u, delta, z = (_f32(rng.standard_normal((batch, D))) for _ in range(3))
+    B, C = (_f32(rng.standard_normal((batch, N))) for _ in range(2))
+    Dskip = _f32(rng.standard_normal(D))
+    st0 = rng.standard_normal((batch, D, N))
+    st1, y1 = oracle.step(st0, u, delta, dt_bias, A, B, C, Dskip, z, lib=lib)
+    v = torch.from_numpy(delta.astype(np.float64) + dt_bias.astype(np.float64)[None])
+    dt = torch.nn.functional.softplus(v, beta=1.0, threshold=1e9).numpy()
+    silu = torch.nn.functional.silu(torch.from_numpy(z.astype(np.float64))).numpy()
+    want_s = np.zeros_like(st0)
+    want_y = np.zeros((batch, D))
+    for b in range(batch):
+        for d in range(D):
+            for n in range(N):
+                ad, bd = zoh_ref(float(A[d, n]), float(dt[b, d]))
+                want_s[b, d, n] = ad * st0[b, d, n] + bd * float(B[b, n]) * float(u[b, d])
+            want_y[b, d] = (want_s[b, d] @ C[b].astype(np.float64)
+                            + float(Dskip[d]) * float(u[b, d])) * silu[b, d]
+    _close(st1, want_s, 1e-12, 1e-14, "library step state")
+    _close(y1, want_y, 1e-12, 1e-14, "library step y")
+
+
+ALL_PINS = [
+    pin_p2_worked_example,
+    pin_lti_convolution_with_skip_and_gate,
+    pin_bruteforce_unrolled,
+    pin_continuous_time_ode,
+    pin_constant_input_closed_form,
+    pin_small_dt_keeps_state,
+    pin_pure_decay,
+    pin_ema_special_case,
+    pin_zero_A_integrator,
+    pin_scan_step_consistency,
+    pin_channels_independent,
+    pin_optional_inputs,
+    pin_bf16_decode,
+    pin_step_matches_library_pipeline,
+]
