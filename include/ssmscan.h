@@ -1,0 +1,137 @@
+/*
+ * ssmscan.h -- C ABI of libssmscan, the B300 (sm_103a) selective state-space
+ * scan (the S6 core of Mamba) and its single-token decode step.
+ *
+ * The operation, from the pages on Mamba / selective SSMs:
+ *   - "Mamba と状態空間モデル(SSM)" (ta-paperlens), section "Mamba: 状態を
+ *     「選択的」にする", pseudocode: Delta, B and C are per-token, A is a
+ *     learned parameter, dt = softplus(x W_d + bias), the state update and
+ *     the readout y_t = C_t h;
+ *   - "State Space Models (SSM)" (ultralytics glossary), section "SSMの仕組み":
+ *     zero-order hold A_bar = exp(Delta A), B_bar = (A_bar - 1)/A * B, the
+ *     recurrence h_t = A_bar h_{t-1} + B_bar x_t from h = 0, y_t = C h_t;
+ *   - news.han.ihouse.idv.tw article 1304: the output equation y = C h + D x;
+ *   - agenticai-flow Mamba guide, block diagram: the S6 output is multiplied
+ *     element-wise by SiLU(z).
+ *
+ * For every batch entry b, channel d, step t and state n:
+ *   dt         = softplus(delta[b,t,d] + dt_bias[d])
+ *   A_bar      = exp(dt * A[d,n])
+ *   B_bar      = (A_bar - 1) / A[d,n] * B[b,t,n]   (dt * B[b,t,n] if A[d,n] == 0)
+ *   h[b,d,n]   = A_bar * h[b,d,n] + B_bar * u[b,t,d]          (h starts at 0)
+ *   y[b,t,d]   = (sum_n C[b,t,n] * h[b,d,n] + Dskip[d] * u[b,t,d]) * silu(z[b,t,d])
+ * with silu(z) = z / (1 + exp(-z)).  All arithmetic is float32 with the
+ * state kept in float32; bf16 inputs are widened exactly and y is rounded to
+ * bf16 (round-to-nearest-even) only when stored.
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is DEVICE memory on the current CUDA device,
+ *     allocated, owned and freed by the caller; the library never frees or
+ *     retains a caller pointer after the call returns.  Tensors are dense and
+ *     row-major with the shapes given below.
+ *   - `dtype` (ssm_dtype_t) is the element type of u, delta, z, B, C and y.
+ *     dt_bias, A, Dskip, h_last and state are always float32.
+ *   - `stream` is a cudaStream_t (NULL: the legacy default stream).  Work is
+ *     enqueued on it and the call returns without synchronising; results are
+ *     valid once the stream has reached that point.
+ *   - Argument errors are returned synchronously, before anything is
+ *     enqueued.  A failed launch returns SSM_ERR_CUDA.  A device-side bounded
+ *     wait that gives up is recorded on the device and reported by
+ *     ssm_device_status().
+ *   - Any element-aligned pointer is accepted.  16-byte-aligned tensors with
+ *     D * sizeof(dtype) a multiple of 16 and N == 16 take the fast kernels;
+ *     everything else runs a generic GPU kernel (never the CPU).
+ */
+#ifndef SSMSCAN_H
+#define SSMSCAN_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = -1,        /* a required pointer is NULL */
+    SSM_ERR_SIZE = -2,        /* negative size, N < 1, or a size that overflows */
+    SSM_ERR_DTYPE = -3,       /* dtype is not an ssm_dtype_t value */
+    SSM_ERR_ALIGN = -4,       /* a pointer is not aligned to its element size */
+    SSM_ERR_UNSUPPORTED = -5, /* N > SSM_MAX_N */
+    SSM_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
+    SSM_ERR_NOMEM = -7,       /* the stream-ordered workspace could not be allocated */
+    SSM_ERR_TIMEOUT = -8      /* a device-side bounded wait gave up (see ssm_device_status) */
+} ssm_status_t;
+
+/* Largest supported state size N. */
+#define SSM_MAX_N 256
+
+/*
+ * ssm_scan_fwd -- selective scan over a whole sequence, from h = 0.
+ *
+ *   u, delta, z : [batch, L, D]  dtype      (z may be NULL: no gate)
+ *   B, C        : [batch, L, N]  dtype
+ *   dt_bias     : [D] float32               (NULL means 0)
+ *   A           : [D, N] float32
+ *   Dskip       : [D] float32               (NULL means 0)
+ *   y           : [batch, L, D] dtype, written
+ *   h_last      : [batch, D, N] float32, written with the state after the
+ *                 last step (h_last == NULL: not written).  It has the layout
+ *                 of ssm_step's `state`, so a prefill continues into decode.
+ * Sizes: batch, L, D >= 0; 1 <= N <= SSM_MAX_N.  L == 0 writes h_last = 0.
+ * The fast path may take a small stream-ordered workspace
+ * (cudaMallocAsync/cudaFreeAsync on `stream`); SSM_ERR_NOMEM if that fails.
+ * Returns an ssm_status_t.
+ */
+SSM_API int ssm_scan_fwd(const void *u, const void *delta, const float *dt_bias,
+                 const float *A, const void *B, const void *C,
+                 const float *Dskip, const void *z, void *y, float *h_last,
+                 int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                 void *stream);
+
+/*
+ * ssm_step -- one decode token: the same per-token update as one step of
+ * ssm_scan_fwd, applied in place to a stored state (the recurrent,
+ * constant-cost inference form; ta-paperlens page, S4 section).
+ *
+ *   state       : [batch, D, N] float32, read and overwritten in place
+ *   u, delta, z : [batch, D] dtype           (z may be NULL: no gate)
+ *   B, C        : [batch, N] dtype
+ *   dt_bias     : [D] float32 (NULL means 0);  A : [D, N] float32
+ *   Dskip       : [D] float32 (NULL means 0)
+ *   y           : [batch, D] dtype, written
+ * Sizes: batch, D >= 0; 1 <= N <= SSM_MAX_N.  Allocates nothing.
+ * Returns an ssm_status_t.
+ */
+SSM_API int ssm_step(float *state, const void *u, const void *delta,
+             const float *dt_bias, const float *A, const void *B,
+             const void *C, const float *Dskip, const void *z, void *y,
+             int64_t batch, int64_t D, int64_t N, int dtype, void *stream);
+
+/*
+ * ssm_device_status -- synchronises `stream`, then reads and clears this
+ * device's error word, which the kernels set when a bounded device-side
+ * wait gives up.  Returns SSM_OK, SSM_ERR_TIMEOUT, or SSM_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+SSM_API int ssm_device_status(void *stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+SSM_API const char *ssm_status_string(int status);
+
+/* Library ABI version (this header describes version 1). */
+SSM_API int ssm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSMSCAN_H */

@@ -1,0 +1,117 @@
+"""ctypes binding of libssmscan (include/ssmscan.h), argument marshalling only.
+
+Each function has the C entry point's name and argument order.  Tensor
+arguments are torch CUDA tensors (or None for an optional NULL); sizes and the
+dtype code are taken from the tensors' shapes and dtypes; ``stream`` defaults
+to torch's current CUDA stream.  A non-zero status raises ``SsmError``.  There
+is no fallback: if the shared library is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssmscan.so")
+
+SSM_F32, SSM_BF16 = 0, 1
+STATUS = {0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_SIZE", -3: "SSM_ERR_DTYPE",
+          -4: "SSM_ERR_ALIGN", -5: "SSM_ERR_UNSUPPORTED", -6: "SSM_ERR_CUDA",
+          -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT"}
+EXPORTS = ("ssm_scan_fwd", "ssm_step", "ssm_device_status", "ssm_status_string",
+           "ssm_abi_version")
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status_text(status)})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libssmscan.so is not built ({LIB_PATH}); run "
+                          "`python -m selective_state_space_113_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.ssm_scan_fwd.restype = ci
+    lib.ssm_scan_fwd.argtypes = [vp] * 10 + [i64] * 4 + [ci, vp]
+    lib.ssm_step.restype = ci
+    lib.ssm_step.argtypes = [vp] * 10 + [i64] * 3 + [ci, vp]
+    lib.ssm_device_status.restype = ci
+    lib.ssm_device_status.argtypes = [vp]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_status_string.argtypes = [ci]
+    lib.ssm_abi_version.restype = ci
+    if lib.ssm_abi_version() != 1:
+        raise ImportError("libssmscan ABI version mismatch")
+    return lib
+
+
+lib = _load()
+
+
+def status_text(status: int) -> str:
+    return lib.ssm_status_string(int(status)).decode()
+
+
+def ssm_status_string(status: int) -> str:
+    return status_text(status)
+
+
+def _p(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSM_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise SsmError(status, where)
+
+
+def ssm_scan_fwd(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, stream=None) -> None:
+    """y, h_last <- selective scan of (u, delta, dt_bias, A, B, C, Dskip, z)."""
+    batch, L, D = u.shape
+    N = A.shape[-1]
+    _check(lib.ssm_scan_fwd(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip),
+                            _p(z), _p(y), _p(h_last), batch, L, D, N, _dtype_code(u),
+                            _stream(stream)), "ssm_scan_fwd")
+
+
+def ssm_step(state, u, delta, dt_bias, A, B, C, Dskip, z, y, stream=None) -> None:
+    """state, y <- one decode step of (u, delta, dt_bias, A, B, C, Dskip, z)."""
+    batch, D = u.shape
+    N = A.shape[-1]
+    _check(lib.ssm_step(_p(state), _p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C),
+                        _p(Dskip), _p(z), _p(y), batch, D, N, _dtype_code(u),
+                        _stream(stream)), "ssm_step")
+
+
+def ssm_device_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device error status."""
+    return lib.ssm_device_status(_stream(stream))
+
+
+def ssm_abi_version() -> int:
+    return lib.ssm_abi_version()

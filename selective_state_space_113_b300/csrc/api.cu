@@ -1,0 +1,144 @@
+// api.cu -- the extern "C" boundary of libssmscan (declared in
+// include/ssmscan.h): argument validation, plan choice and kernel launch.
+//
+// The whole library is this one translation unit; every kernel file is
+// included here.
+#include "../../include/ssmscan.h"
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+#include "scan_generic.cuh"
+#include "step_generic.cuh"
+
+namespace {
+
+using ssm::bf16;
+
+bool aligned_to(const void* p, size_t a) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// a*b without signed overflow for non-negative a, b; false if it would overflow.
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a == 0 || b == 0) { *out = 0; return true; }
+    if (a > INT64_MAX / b) return false;
+    *out = a * b;
+    return true;
+}
+
+size_t elem_size(int dtype) { return dtype == SSM_BF16 ? 2 : 4; }
+
+// Element-alignment check of every tensor argument.
+bool elems_aligned(int dtype, std::initializer_list<const void*> typed,
+                   std::initializer_list<const void*> f32) {
+    for (const void* p : typed)
+        if (!aligned_to(p, elem_size(dtype))) return false;
+    for (const void* p : f32)
+        if (!aligned_to(p, 4)) return false;
+    return true;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bias,
+                            const float* A, const void* B, const void* C,
+                            const float* Dskip, const void* z, void* y, float* h_last,
+                            int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                            void* stream_) {
+    if (!u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
+    if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
+    if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    int64_t bl, bld, bln, bd, bdn;
+    if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) ||
+        !mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || bld > (INT64_MAX >> 4) ||
+        bln > (INT64_MAX >> 4) || bdn > (INT64_MAX >> 4))
+        return SSM_ERR_SIZE;
+    if (!elems_aligned(dtype, {u, delta, B, C, z, y}, {dt_bias, A, Dskip, h_last}))
+        return SSM_ERR_ALIGN;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (bd == 0) return SSM_OK;
+    if (L == 0) {
+        // The state after zero steps is the initial state, 0.
+        if (h_last) return from_cuda(cudaMemsetAsync(h_last, 0, sizeof(float) * bdn, stream));
+        return SSM_OK;
+    }
+    cudaError_t e;
+    if (dtype == SSM_F32)
+        e = ssm::launch_scan_generic<float>(
+            static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+            static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+            static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D, (int)N,
+            stream);
+    else
+        e = ssm::launch_scan_generic<bf16>(
+            static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+            static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, (int)N,
+            stream);
+    return from_cuda(e);
+}
+
+extern "C" int ssm_step(float* state, const void* u, const void* delta, const float* dt_bias,
+                        const float* A, const void* B, const void* C, const float* Dskip,
+                        const void* z, void* y, int64_t batch, int64_t D, int64_t N, int dtype,
+                        void* stream_) {
+    if (!state || !u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
+    if (batch < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
+    if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    int64_t bd, bdn;
+    if (!mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || bdn > (INT64_MAX >> 4))
+        return SSM_ERR_SIZE;
+    if (!elems_aligned(dtype, {u, delta, B, C, z, y}, {state, dt_bias, A, Dskip}))
+        return SSM_ERR_ALIGN;
+    if (bd == 0) return SSM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    cudaError_t e;
+    if (dtype == SSM_F32)
+        e = ssm::launch_step_generic<float>(
+            state, static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+            static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+            static_cast<const float*>(z), static_cast<float*>(y), batch, D, (int)N, stream);
+    else
+        e = ssm::launch_step_generic<bf16>(
+            state, static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+            static_cast<const bf16*>(z), static_cast<bf16*>(y), batch, D, (int)N, stream);
+    return from_cuda(e);
+}
+
+extern "C" int ssm_device_status(void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SSM_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, ssm::g_error_word, sizeof word) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(ssm::g_error_word, &zero, sizeof zero) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (word & ssm::kErrTimeout) return SSM_ERR_TIMEOUT;
+    }
+    return SSM_OK;
+}
+
+extern "C" const char* ssm_status_string(int status) {
+    switch (status) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_NULL: return "a required pointer is NULL";
+        case SSM_ERR_SIZE: return "invalid or overflowing size";
+        case SSM_ERR_DTYPE: return "unknown dtype";
+        case SSM_ERR_ALIGN: return "pointer not aligned to its element size";
+        case SSM_ERR_UNSUPPORTED: return "unsupported state size N";
+        case SSM_ERR_CUDA: return "CUDA runtime error";
+        case SSM_ERR_NOMEM: return "workspace allocation failed";
+        case SSM_ERR_TIMEOUT: return "device-side bounded wait gave up";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int ssm_abi_version(void) { return 1; }

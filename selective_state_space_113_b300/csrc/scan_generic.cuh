@@ -1,0 +1,99 @@
+// scan_generic.cuh -- the generic selective-scan kernel: any N <= 256, any
+// element alignment, any D.  One thread owns one (b, d) channel and walks the
+// sequence; the state stays in registers (N <= 32) or thread-local memory.
+//
+// Arithmetic is the definition written out in float32 (ultralytics page,
+// "SSMの仕組み": A_bar = exp(dt A), B_bar = (A_bar - 1)/A * B with expm1 for
+// accuracy; ta-paperlens page, Mamba pseudocode: dt = softplus(delta + bias),
+// h = A_bar h + B_bar u, y = C h; D skip from the output equation y = C h + D x;
+// SiLU(z) gate from the Mamba block diagram).
+#pragma once
+
+#include "common.cuh"
+
+namespace ssm {
+
+template <typename T, int NMAX>
+__global__ void __launch_bounds__(128)
+scan_generic_kernel(const T* __restrict__ u, const T* __restrict__ delta,
+                    const float* __restrict__ dt_bias, const float* __restrict__ A,
+                    const T* __restrict__ Bm, const T* __restrict__ Cm,
+                    const float* __restrict__ Dskip, const T* __restrict__ z,
+                    T* __restrict__ y, float* __restrict__ h_last,
+                    int64_t batch, int64_t L, int64_t D, int N) {
+    const int64_t ch = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (ch >= batch * D) return;
+    const int64_t b = ch / D, d = ch - b * D;
+
+    float h[NMAX];
+    float a[NMAX];
+#pragma unroll
+    for (int n = 0; n < NMAX; ++n) {
+        h[n] = 0.0f;
+        a[n] = (n < N) ? A[d * N + n] : 0.0f;
+    }
+    const float bias = dt_bias ? dt_bias[d] : 0.0f;
+    const float dsk = Dskip ? Dskip[d] : 0.0f;
+
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t i = (b * L + t) * D + d;
+        const float ut = to_f32(u[i]);
+        const float dt = softplus_ref(to_f32(delta[i]) + bias);
+        const T* Bt = Bm + (b * L + t) * N;
+        const T* Ct = Cm + (b * L + t) * N;
+        float acc = 0.0f;
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n) {
+            if (n < N) {
+                const float x = dt * a[n];
+                const float abar = expf(x);
+                const float bcoef = (a[n] != 0.0f) ? expm1f(x) / a[n] : dt;
+                h[n] = fmaf(abar, h[n], bcoef * to_f32(Bt[n]) * ut);
+                acc = fmaf(to_f32(Ct[n]), h[n], acc);
+            }
+        }
+        acc = fmaf(dsk, ut, acc);
+        if (z) acc *= silu_ref(to_f32(z[i]));
+        y[i] = from_f32<T>(acc);
+    }
+    if (h_last) {
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n)
+            if (n < N) h_last[ch * N + n] = h[n];
+    }
+}
+
+template <typename T, int NMAX>
+static cudaError_t launch_scan_generic_n(const T* u, const T* delta, const float* dt_bias,
+                                         const float* A, const T* Bm, const T* Cm,
+                                         const float* Dskip, const T* z, T* y, float* h_last,
+                                         int64_t batch, int64_t L, int64_t D, int N,
+                                         cudaStream_t stream) {
+    const int64_t channels = batch * D;
+    const int threads = 128;
+    const int64_t blocks = (channels + threads - 1) / threads;
+    scan_generic_kernel<T, NMAX><<<(unsigned)blocks, threads, 0, stream>>>(
+        u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D, N);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_scan_generic(const T* u, const T* delta, const float* dt_bias,
+                                       const float* A, const T* Bm, const T* Cm,
+                                       const float* Dskip, const T* z, T* y, float* h_last,
+                                       int64_t batch, int64_t L, int64_t D, int N,
+                                       cudaStream_t stream) {
+    if (N <= 16)
+        return launch_scan_generic_n<T, 16>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
+                                            batch, L, D, N, stream);
+    if (N <= 32)
+        return launch_scan_generic_n<T, 32>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
+                                            batch, L, D, N, stream);
+    if (N <= 64)
+        return launch_scan_generic_n<T, 64>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
+                                            batch, L, D, N, stream);
+    return launch_scan_generic_n<T, 256>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
+                                         batch, L, D, N, stream);
+}
+
+}  // namespace ssm

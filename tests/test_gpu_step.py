@@ -1,0 +1,102 @@
+"""GPU parity of ssm_step (decode) against the float64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_113_b300 as ssm
+from selective_state_space_113_b300 import workloads as wl
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def gpu_steps(inp, steps):
+    state = inp["state"].clone()
+    ys = []
+    for s in range(steps):
+        ys.append(ssm.step(state, inp["u"][s], inp["delta"][s], inp["dt_bias"], inp["A"],
+                           inp["B"][s], inp["C"][s], inp["Dskip"],
+                           None if inp["z"] is None else inp["z"][s]))
+    torch.cuda.synchronize()
+    return state, torch.stack(ys)
+
+
+def oracle_steps(inp, steps, chans):
+    """Oracle decode on sampled (b, d) channels; returns {(b,d): (state [N], y [steps])}."""
+    dt = parity.dtype_code(inp["u"].dtype)
+    by_b = {}
+    for b, d in chans:
+        by_b.setdefault(b, []).append(d)
+    out = {}
+    for b, ds in by_b.items():
+        ds = sorted(set(ds))
+        idx = torch.tensor(ds, device=DEV)
+        st = parity.to_f64(inp["state"][b:b + 1].index_select(1, idx))
+        A = parity.host(inp["A"].index_select(0, idx))
+        bias = parity.host(None if inp["dt_bias"] is None else inp["dt_bias"].index_select(0, idx))
+        dsk = parity.host(None if inp["Dskip"] is None else inp["Dskip"].index_select(0, idx))
+        ys = []
+        for s in range(steps):
+            sub = lambda t: None if t is None else parity.host(t[s, b:b + 1].index_select(1, idx))  # noqa: E731
+            st, y = oracle.step(st, sub(inp["u"]), sub(inp["delta"]), bias, A,
+                                parity.host(inp["B"][s, b:b + 1]), parity.host(inp["C"][s, b:b + 1]),
+                                dsk, sub(inp["z"]), dtype=dt)
+            ys.append(y[0])
+        ys = np.stack(ys)  # [steps, len(ds)]
+        for j, d in enumerate(ds):
+            out[(b, d)] = (st[0, j], ys[:, j])
+    return out
+
+
+def check_steps(inp, steps, chans, what):
+    state, ys = gpu_steps(inp, steps)
+    ref = oracle_steps(inp, steps, chans)
+    tol = parity.TOL[inp["u"].dtype]
+    for (b, d) in chans:
+        parity.check(parity.to_f64(state[b, d]), ref[(b, d)][0], tol, f"{what} state b={b} d={d}")
+        parity.check(parity.to_f64(ys[:, b, d]), ref[(b, d)][1], tol, f"{what} y b={b} d={d}")
+
+
+def test_decode_full_size_64_steps_sampled():
+    inp = wl.make_step_inputs(wl.DECODE, device=DEV)
+    chans = parity.sample_channels(wl.DECODE.batch, wl.DECODE.D, 40)
+    check_steps(inp, wl.DECODE.steps, chans, "decode")
+
+
+@pytest.mark.parametrize("N", [1, 5, 16, 32, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_step_small_full(N, dtype):
+    w = wl.StepWorkload("small", 3, 70, N, 5, dtype, 100 + N)
+    inp = wl.make_step_inputs(w, device=DEV)
+    chans = [(b, d) for b in range(3) for d in range(70)]
+    check_steps(inp, 5, chans, f"step N={N} {dtype}")
+
+
+def test_step_optional_null_and_empty():
+    w = wl.StepWorkload("small", 2, 40, 16, 3, torch.bfloat16, 7)
+    for drop in ("z", "Dskip", "dt_bias"):
+        inp = wl.make_step_inputs(w, device=DEV)
+        inp[drop] = None
+        check_steps(inp, 3, [(b, d) for b in range(2) for d in range(40)], f"{drop}=NULL")
+    inp = wl.make_step_inputs(w, device=DEV, batch=0)
+    gpu_steps(inp, 1)
+
+
+def test_step_small_dt_and_pure_decay():
+    """dt -> 0 leaves the state unchanged; B = 0 gives state * exp(dt A)."""
+    w = wl.StepWorkload("small", 2, 64, 16, 1, torch.float32, 8)
+    inp = wl.make_step_inputs(w, device=DEV)
+    inp["delta"][:] = -60.0
+    inp["dt_bias"] = None
+    st0 = inp["state"].clone()
+    state, _ = gpu_steps(inp, 1)
+    assert torch.equal(state, st0)
+    inp = wl.make_step_inputs(w, device=DEV)
+    inp["B"][:] = 0.0
+    st0 = inp["state"].clone()
+    state, _ = gpu_steps(inp, 1)
+    dt = torch.nn.functional.softplus(inp["delta"][0].double() + inp["dt_bias"].double())
+    want = st0.double() * torch.exp(dt[:, :, None] * inp["A"].double()[None])
+    parity.check(parity.to_f64(state), want.cpu().numpy(), 1e-5, "pure decay")
