@@ -312,9 +312,8 @@ def cpu_baseline(inp, w):
     """The float64 oracle, as it stands, on this host's cores: a channel sample
     of the same workload sized to ~10-30 s of CPU work."""
     n = cores()
-    channels = min(w.D, max(n * 32, 256))
-    # ~10-30 core-seconds: the oracle runs ~3-4e6 elements/s per core
-    channels = min(channels, max(64, int(20 * 3.5e6 / (w.batch * w.L))))
+    # ~20 core-seconds of work: the oracle runs ~3-4e6 elements/s per core
+    channels = min(w.D, max(64, int(20 * 3.5e6 / (w.batch * w.L))))
     channels = max(n, channels - channels % n)
     elems, secs = _oracle_sample(inp, w, channels, n)
     return {"value": elems / secs, "unit": "elements/s", "cores": n, "kind": "oracle",

@@ -38,6 +38,8 @@
  *     enqueued.  A failed launch returns SSM_ERR_CUDA.  A device-side bounded
  *     wait that gives up is recorded on the device and reported by
  *     ssm_device_status().
+ *   - A tensor pointer may be NULL only when that tensor has no elements
+ *     (or when the entry point documents it as optional).
  *   - Any element-aligned pointer is accepted.  16-byte-aligned tensors with
  *     D * sizeof(dtype) a multiple of 16 and N == 16 take the fast kernels;
  *     everything else runs a generic GPU kernel (never the CPU).

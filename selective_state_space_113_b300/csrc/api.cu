@@ -48,15 +48,17 @@ extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bi
                             const float* Dskip, const void* z, void* y, float* h_last,
                             int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
                             void* stream_) {
-    if (!u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
     if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
-    int64_t bl, bld, bln, bd, bdn;
+    int64_t bl, bld, bln, bd, bdn, dn;
     if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) ||
-        !mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || bld > (INT64_MAX >> 4) ||
-        bln > (INT64_MAX >> 4) || bdn > (INT64_MAX >> 4))
+        !mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || !mul_ok(D, N, &dn) ||
+        bld > (INT64_MAX >> 4) || bln > (INT64_MAX >> 4) || bdn > (INT64_MAX >> 4))
         return SSM_ERR_SIZE;
+    // A pointer may be NULL only when its tensor has no elements.
+    if ((bld && (!u || !delta || !y)) || (bln && (!B || !C)) || (dn && !A))
+        return SSM_ERR_NULL;
     if (!elems_aligned(dtype, {u, delta, B, C, z, y}, {dt_bias, A, Dskip, h_last}))
         return SSM_ERR_ALIGN;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -86,13 +88,15 @@ extern "C" int ssm_step(float* state, const void* u, const void* delta, const fl
                         const float* A, const void* B, const void* C, const float* Dskip,
                         const void* z, void* y, int64_t batch, int64_t D, int64_t N, int dtype,
                         void* stream_) {
-    if (!state || !u || !delta || !A || !B || !C || !y) return SSM_ERR_NULL;
     if (batch < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
-    int64_t bd, bdn;
-    if (!mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || bdn > (INT64_MAX >> 4))
+    int64_t bd, bdn, bn, dn;
+    if (!mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || !mul_ok(batch, N, &bn) ||
+        !mul_ok(D, N, &dn) || bdn > (INT64_MAX >> 4))
         return SSM_ERR_SIZE;
+    if ((bd && (!state || !u || !delta || !y)) || (bn && (!B || !C)) || (dn && !A))
+        return SSM_ERR_NULL;
     if (!elems_aligned(dtype, {u, delta, B, C, z, y}, {state, dt_bias, A, Dskip}))
         return SSM_ERR_ALIGN;
     if (bd == 0) return SSM_OK;

@@ -62,8 +62,11 @@ def step(lib, state=FAKE, u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, y=FAKE, ba
 
 def test_scan_argument_validation(lib):
     assert scan(lib) == 0                      # batch == 0: nothing to do
-    for k in ("u", "delta", "A", "B", "C", "y"):
-        assert scan(lib, **{k: None}) == -1
+    for k in ("A",):
+        assert scan(lib, **{k: None}) == -1    # A has D*N elements even when batch == 0
+    for k in ("u", "delta", "B", "C", "y"):
+        assert scan(lib, **{k: None}) == 0     # empty tensors may be NULL
+        assert scan(lib, batch=1, **{k: None}) == -1
     assert scan(lib, batch=-1) == -2
     assert scan(lib, L=-1) == -2
     assert scan(lib, D=-1) == -2
@@ -80,8 +83,10 @@ def test_scan_argument_validation(lib):
 
 def test_step_argument_validation(lib):
     assert step(lib) == 0
-    for k in ("state", "u", "delta", "A", "B", "C", "y"):
-        assert step(lib, **{k: None}) == -1
+    assert step(lib, A=None) == -1
+    for k in ("state", "u", "delta", "B", "C", "y"):
+        assert step(lib, **{k: None}) == 0
+        assert step(lib, batch=1, **{k: None}) == -1
     assert step(lib, batch=-1) == -2
     assert step(lib, N=0) == -2
     assert step(lib, N=300) == -5
