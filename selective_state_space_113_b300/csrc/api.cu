@@ -10,6 +10,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "scan_fast_host.cuh"
 #include "scan_generic.cuh"
 #include "step_generic.cuh"
 
@@ -18,6 +19,12 @@ namespace {
 using ssm::bf16;
 
 bool aligned_to(const void* p, size_t a) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool all_aligned16(std::initializer_list<const void*> ps) {
+    for (const void* p : ps)
+        if (!aligned_to(p, 16)) return false;
+    return true;
+}
 
 // a*b without signed overflow for non-negative a, b; false if it would overflow.
 bool mul_ok(int64_t a, int64_t b, int64_t* out) {
@@ -67,6 +74,21 @@ extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bi
         // The state after zero steps is the initial state, 0.
         if (h_last) return from_cuda(cudaMemsetAsync(h_last, 0, sizeof(float) * bdn, stream));
         return SSM_OK;
+    }
+    // Fast path: N == 16, 16-byte-aligned tensors and rows (TMA tiles).
+    const int plan = ssm::fast::forced_plan();
+    if (N == ssm::fast::NS && plan != ssm::fast::kPlanGeneric &&
+        all_aligned16({u, delta, z, B, C, y, h_last}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
+        if (dtype == SSM_F32)
+            return ssm::fast::launch_scan_fast<float>(
+                static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+                static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+                static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D, plan,
+                stream);
+        return ssm::fast::launch_scan_fast<bf16>(
+            static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+            static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, plan, stream);
     }
     cudaError_t e;
     if (dtype == SSM_F32)

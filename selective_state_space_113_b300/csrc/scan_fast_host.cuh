@@ -1,0 +1,222 @@
+// scan_fast_host.cuh -- plan choice, TMA descriptors, stream-ordered workspace
+// and launches for the N == 16 selective-scan kernel (scan_fast.cuh).
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/ssmscan.h"
+#include "scan_fast.cuh"
+
+namespace ssm {
+namespace fast {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, found once through the runtime (no
+// link-time dependency on libcuda).
+inline EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Rank-3 map over a row-major [batch, L, inner] tensor, box {box_inner, TC, 1}.
+template <typename T>
+inline bool make_map(CUtensorMap* m, const void* base, long long inner, long long L,
+                     long long batch, unsigned box_inner) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t es = sizeof(T);
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)L, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)inner * es, (cuuint64_t)inner * (cuuint64_t)L * es};
+    const cuuint32_t box[3] = {box_inner, (cuuint32_t)TC, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+inline long long env_ll(const char* name, long long dflt) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    return std::strtoll(v, nullptr, 10);
+}
+
+// Plan names accepted by SSM_FORCE_PLAN (development and tests).
+enum Plan { kPlanAuto = 0, kPlanGeneric = 1, kPlanChained = 2, kPlanNarrow = 3 };
+
+inline int forced_plan() {
+    const char* v = std::getenv("SSM_FORCE_PLAN");
+    if (!v) return kPlanAuto;
+    if (!std::strcmp(v, "generic")) return kPlanGeneric;
+    if (!std::strcmp(v, "chained")) return kPlanChained;
+    if (!std::strcmp(v, "narrow")) return kPlanNarrow;
+    return kPlanAuto;
+}
+
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+template <typename T, int MODE>
+inline cudaError_t prepare(int* occ) {
+    auto kern = scan_fast_kernel<T, MODE>;
+    const int smem = Layout<T>::kBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, THREADS, smem);
+}
+
+template <typename T, int MODE>
+inline cudaError_t launch_mode(int grid, const CUtensorMap* maps, const Params& p,
+                               cudaStream_t s) {
+    const int smem = Layout<T>::kBytes + 1024;
+    scan_fast_kernel<T, MODE><<<grid, THREADS, smem, s>>>(maps[0], maps[1], maps[2], maps[3],
+                                                          maps[4], p);
+    return cudaGetLastError();
+}
+
+// Returns an ssm_status_t.  Preconditions (checked by the caller): N == 16,
+// all typed tensors and h_last 16-byte aligned, D * sizeof(T) % 16 == 0,
+// batch*D > 0, L > 0.
+template <typename T>
+int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const float* A,
+                     const T* Bm, const T* Cm, const float* Dskip, const T* z, T* y,
+                     float* h_last, long long batch, long long L, long long D, int plan,
+                     cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    int occ_c = 0, occ_a = 0, occ_f = 0;
+    if (prepare<T, (int)kChained>(&occ_c) != cudaSuccess ||
+        prepare<T, (int)kAggregate>(&occ_a) != cudaSuccess ||
+        prepare<T, (int)kFromState>(&occ_f) != cudaSuccess || occ_c < 1 || occ_a < 1 || occ_f < 1)
+        return SSM_ERR_CUDA;
+
+    CUtensorMap maps[5];
+    if (!make_map<T>(&maps[0], u, D, L, batch, CH) || !make_map<T>(&maps[1], delta, D, L, batch, CH) ||
+        !make_map<T>(&maps[2], z ? z : u, D, L, batch, CH) ||
+        !make_map<T>(&maps[3], Bm, NS, L, batch, NS) || !make_map<T>(&maps[4], Cm, NS, L, batch, NS))
+        return SSM_ERR_CUDA;
+
+    Params p{};
+    p.y = y;
+    p.h_last = h_last;
+    p.dt_bias = dt_bias;
+    p.A = A;
+    p.Dskip = Dskip;
+    p.has_z = z != nullptr;
+    p.test_stall = env_ll("SSM_TEST_STALL_CHAIN", 0) != 0;
+    p.batch = batch;
+    p.L = L;
+    p.D = D;
+    p.nCB = cdiv(D, CH);
+    p.nchains = batch * p.nCB;
+    p.wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
+
+    const long long workers = (long long)sms * occ_c;
+    bool narrow = false;
+    if (plan == kPlanNarrow) narrow = true;
+    else if (plan == kPlanAuto) narrow = p.nchains * 100 < workers * 55;
+    long long steps;
+    const long long forced_steps = env_ll("SSM_CHUNK_T", 0);
+    if (!narrow) {
+        const long long P0 = cdiv(8 * workers, p.nchains);
+        steps = cdiv(cdiv(L, P0 > 0 ? P0 : 1), TC) * TC;
+    } else {
+        const long long P0 = cdiv(4 * (long long)sms * occ_a, p.nchains);
+        steps = cdiv(cdiv(L, P0 < 2 ? 2 : P0), TC) * TC;
+    }
+    if (forced_steps > 0) steps = cdiv(forced_steps, TC) * TC;
+    if (steps < TC) steps = TC;
+    p.T = steps;
+    p.P = cdiv(L, steps);
+    if (p.P < 2) narrow = false;
+
+    // Workspace: [0,8) phase-A ticket, [16,24) phase-B ticket, [32,36) abort,
+    // [256, 256+4*nchains) chain flags, then the state buffers.
+    const long long nch = batch * D;
+    const size_t head = 256 + (size_t)p.nchains * 4;
+    const size_t head_al = (head + 255) & ~(size_t)255;
+    size_t bytes = head_al;
+    size_t off_carry = 0, off_agg = 0, off_hin = 0;
+    if (!narrow) {
+        if (!h_last) {
+            off_carry = bytes;
+            bytes += (size_t)nch * NS * 4;
+        }
+    } else {
+        off_agg = bytes;
+        bytes += (size_t)(p.P - 1) * nch * (NS + 1) * 4;
+        bytes = (bytes + 255) & ~(size_t)255;
+        off_hin = bytes;
+        bytes += (size_t)p.P * nch * NS * 4;
+    }
+    unsigned char* ws = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_NOMEM;
+    }
+    int status = SSM_OK;
+    do {
+        if (cudaMemsetAsync(ws, 0, head_al, stream) != cudaSuccess) {
+            status = SSM_ERR_CUDA;
+            break;
+        }
+        p.abort = reinterpret_cast<unsigned*>(ws + 32);
+        p.flags = reinterpret_cast<unsigned*>(ws + 256);
+        if (!narrow) {
+            p.ticket = reinterpret_cast<unsigned long long*>(ws);
+            p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + off_carry);
+            p.total_units = p.nchains * p.P;
+            const int grid = (int)(p.total_units < workers ? p.total_units : workers);
+            if (launch_mode<T, (int)kChained>(grid, maps, p, stream) != cudaSuccess)
+                status = SSM_ERR_CUDA;
+        } else {
+            p.agg = reinterpret_cast<float*>(ws + off_agg);
+            p.hin = reinterpret_cast<float*>(ws + off_hin);
+            p.ticket = reinterpret_cast<unsigned long long*>(ws);
+            p.total_units = p.nchains * (p.P - 1);
+            const long long wa = (long long)sms * occ_a, wf = (long long)sms * occ_f;
+            const int grid_a = (int)(p.total_units < wa ? p.total_units : wa);
+            if (launch_mode<T, (int)kAggregate>(grid_a, maps, p, stream) != cudaSuccess) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
+            const long long threads = nch * NS;
+            carry_kernel<<<(unsigned)cdiv(threads, 256), 256, 0, stream>>>(
+                p.agg, A, reinterpret_cast<float*>(ws + off_hin), batch, D, p.P);
+            if (cudaGetLastError() != cudaSuccess) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
+            p.ticket = reinterpret_cast<unsigned long long*>(ws + 16);
+            p.total_units = p.nchains * p.P;
+            const int grid_f = (int)(p.total_units < wf ? p.total_units : wf);
+            if (launch_mode<T, (int)kFromState>(grid_f, maps, p, stream) != cudaSuccess)
+                status = SSM_ERR_CUDA;
+        }
+    } while (0);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && status == SSM_OK) status = SSM_ERR_CUDA;
+    return status;
+}
+
+}  // namespace fast
+}  // namespace ssm
