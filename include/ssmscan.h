@@ -70,7 +70,8 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = -5, /* N > SSM_MAX_N */
     SSM_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
     SSM_ERR_NOMEM = -7,       /* the stream-ordered workspace could not be allocated */
-    SSM_ERR_TIMEOUT = -8      /* a device-side bounded wait gave up (see ssm_device_status) */
+    SSM_ERR_TIMEOUT = -8,     /* a device-side bounded wait gave up (see ssm_device_status) */
+    SSM_ERR_SCRATCH = -9      /* ssm_scan_fwd_noalloc: problem exceeds its fixed scratch */
 } ssm_status_t;
 
 /* Largest supported state size N. */
@@ -117,6 +118,43 @@ SSM_API int ssm_step(float *state, const void *u, const void *delta,
              const float *dt_bias, const float *A, const void *B,
              const void *C, const float *Dskip, const void *z, void *y,
              int64_t batch, int64_t D, int64_t N, int dtype, void *stream);
+
+/*
+ * ssm_scan_fwd_noalloc -- ssm_scan_fwd for callers that cannot allocate.
+ *
+ * The pages describe no such call; it exists for library users whose code
+ * must not allocate device memory while it runs: a server that reserves all
+ * of its memory up front in its own pool, or code running where a
+ * cudaMalloc/cudaMallocAsync would synchronise the device, fail, or is not
+ * allowed.  Arguments, layouts, results and errors are those of ssm_scan_fwd.
+ * The difference is where the N == 16 fast kernel keeps its scratch (its unit
+ * counter, per-chain progress flags and, when h_last is NULL, the state
+ * carried between chunks): in one fixed device array of
+ * SSM_NOALLOC_SCRATCH_BYTES inside this library, which every GPU that loads
+ * the library holds until the process exits.  It always runs the chained
+ * plan of that kernel; inputs that kernel does not take (N != 16, tensors not
+ * 16-byte aligned, D * sizeof(dtype) not a multiple of 16) run the generic
+ * kernel, which needs no scratch.  Nothing here calls cudaMalloc, cudaFree
+ * or any allocating routine.
+ *
+ *   - Limit: 256 + 4 * batch * ceil(D/32) bytes (rounded up to 256), plus
+ *     64 * batch * D bytes when h_last is NULL, must fit in
+ *     SSM_NOALLOC_SCRATCH_BYTES; otherwise SSM_ERR_SCRATCH is returned before
+ *     anything is enqueued.  (batch 4, D 5120 needs 2.8 KB with h_last and
+ *     1.3 MB without.)
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array, and it keeps the last call's contents
+ *     (each call clears the parts that must start at zero).  Calls whose
+ *     work overlaps on the GPU -- on different streams, or from different
+ *     host threads -- race on it and must be serialised by the caller.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES (4u << 20)
+SSM_API int ssm_scan_fwd_noalloc(const void *u, const void *delta, const float *dt_bias,
+                                 const float *A, const void *B, const void *C,
+                                 const float *Dskip, const void *z, void *y, float *h_last,
+                                 int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                                 void *stream);
 
 /*
  * ssm_device_status -- synchronises `stream`, then reads and clears this

@@ -19,8 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libssmscan.so")
 SSM_F32, SSM_BF16 = 0, 1
 STATUS = {0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_SIZE", -3: "SSM_ERR_DTYPE",
           -4: "SSM_ERR_ALIGN", -5: "SSM_ERR_UNSUPPORTED", -6: "SSM_ERR_CUDA",
-          -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT"}
-EXPORTS = ("ssm_scan_fwd", "ssm_step", "ssm_device_status", "ssm_status_string",
+          -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT", -9: "SSM_ERR_SCRATCH"}
+EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_step", "ssm_device_status", "ssm_status_string",
            "ssm_abi_version")
 
 
@@ -38,6 +38,8 @@ def _load() -> ctypes.CDLL:
     vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.ssm_scan_fwd.restype = ci
     lib.ssm_scan_fwd.argtypes = [vp] * 10 + [i64] * 4 + [ci, vp]
+    lib.ssm_scan_fwd_noalloc.restype = ci
+    lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [i64] * 4 + [ci, vp]
     lib.ssm_step.restype = ci
     lib.ssm_step.argtypes = [vp] * 10 + [i64] * 3 + [ci, vp]
     lib.ssm_device_status.restype = ci
@@ -97,6 +99,17 @@ def ssm_scan_fwd(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, stream=None) -
     _check(lib.ssm_scan_fwd(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip),
                             _p(z), _p(y), _p(h_last), batch, L, D, N, _dtype_code(u),
                             _stream(stream)), "ssm_scan_fwd")
+
+
+def ssm_scan_fwd_noalloc(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, stream=None) -> None:
+    """As ssm_scan_fwd, with the kernel scratch in the library's fixed device
+    array instead of a stream-ordered allocation (for callers that cannot
+    allocate device memory)."""
+    batch, L, D = u.shape
+    N = A.shape[-1]
+    _check(lib.ssm_scan_fwd_noalloc(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C),
+                                    _p(Dskip), _p(z), _p(y), _p(h_last), batch, L, D, N,
+                                    _dtype_code(u), _stream(stream)), "ssm_scan_fwd_noalloc")
 
 
 def ssm_step(state, u, delta, dt_bias, A, B, C, Dskip, z, y, stream=None) -> None:

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "scan_fast_host.cuh"
@@ -163,8 +164,166 @@ extern "C" const char* ssm_status_string(int status) {
         case SSM_ERR_CUDA: return "CUDA runtime error";
         case SSM_ERR_NOMEM: return "workspace allocation failed";
         case SSM_ERR_TIMEOUT: return "device-side bounded wait gave up";
+        case SSM_ERR_SCRATCH: return "problem needs more scratch than the fixed no-allocation buffer";
         default: return "unknown status";
     }
 }
 
 extern "C" int ssm_abi_version(void) { return 1; }
+
+// ---------------------------------------------------------------------------
+// ssm_scan_fwd_noalloc: the selective scan for callers that must not allocate
+// device memory while they run (for example a serving loop whose memory is
+// all reserved up front by its own pool, or code in a context where a
+// cudaMalloc/cudaMallocAsync would synchronise, fail or be forbidden).  It is
+// the chained variant of the N == 16 fast kernel, whose scratch (unit ticket,
+// abort word, per-chain progress flags and, when h_last is NULL, the carried
+// chunk state) lives in the fixed device array below instead of a
+// stream-ordered workspace.  Inputs the fast kernel does not take (other N,
+// unaligned tensors) run the generic kernel, which needs no scratch at all.
+namespace {
+
+// Scratch of the allocation-free entry point.  Every device that loads this
+// library holds these bytes until the process exits.  In host code the name
+// is only a host-side stand-in: kernels get the device address looked up by
+// noalloc_scratch_ptr().
+constexpr size_t kNoallocScratchBytes = SSM_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 128;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the first call on a device does it, with that device current).
+int noalloc_scratch_ptr(unsigned char** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return SSM_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_ptr[dev]);
+    return SSM_OK;
+}
+
+// Scratch bytes the chained plan needs: header (ticket, abort), one flag per
+// 32-channel chain, and the carried state when h_last cannot hold it.
+size_t noalloc_scratch_need(int64_t batch, int64_t D, bool have_h_last) {
+    const int64_t nchains = batch * ((D + ssm::fast::CH - 1) / ssm::fast::CH);
+    size_t bytes = ((256 + (size_t)nchains * 4) + 255) & ~(size_t)255;
+    if (!have_h_last) bytes += (size_t)(batch * D) * ssm::fast::NS * 4;
+    return bytes;
+}
+
+template <typename T>
+int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float* A,
+                   const T* Bm, const T* Cm, const float* Dskip, const T* z, T* y,
+                   float* h_last, long long batch, long long L, long long D,
+                   unsigned char* ws, cudaStream_t stream) {
+    using namespace ssm::fast;
+    int dev = 0, sms = 0, occ = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        prepare<T, (int)kChained>(&occ) != cudaSuccess || occ < 1)
+        return SSM_ERR_CUDA;
+    CUtensorMap maps[5];
+    if (!make_map<T>(&maps[0], u, D, L, batch, CH) || !make_map<T>(&maps[1], delta, D, L, batch, CH) ||
+        !make_map<T>(&maps[2], z ? z : u, D, L, batch, CH) ||
+        !make_map<T>(&maps[3], Bm, NS, L, batch, NS) || !make_map<T>(&maps[4], Cm, NS, L, batch, NS))
+        return SSM_ERR_CUDA;
+    Params p{};
+    p.y = y;
+    p.h_last = h_last;
+    p.dt_bias = dt_bias;
+    p.A = A;
+    p.Dskip = Dskip;
+    p.has_z = z != nullptr;
+    p.batch = batch;
+    p.L = L;
+    p.D = D;
+    p.nCB = cdiv(D, CH);
+    p.nchains = batch * p.nCB;
+    p.wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
+    const long long workers = (long long)sms * occ;
+    const long long P0 = cdiv(8 * workers, p.nchains);
+    long long steps = cdiv(cdiv(L, P0 > 0 ? P0 : 1), TC) * TC;
+    if (steps < TC) steps = TC;
+    p.T = steps;
+    p.P = cdiv(L, steps);
+    const size_t head = ((256 + (size_t)p.nchains * 4) + 255) & ~(size_t)255;
+    // The array keeps the previous call's contents: reset the ticket, the
+    // abort word and the chain flags, which must start at zero.
+    if (cudaMemsetAsync(ws, 0, head, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    p.ticket = reinterpret_cast<unsigned long long*>(ws);
+    p.abort = reinterpret_cast<unsigned*>(ws + 32);
+    p.flags = reinterpret_cast<unsigned*>(ws + 256);
+    p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + head);
+    p.total_units = p.nchains * p.P;
+    const int grid = (int)(p.total_units < workers ? p.total_units : workers);
+    return launch_mode<T, (int)kChained>(grid, maps, p, stream) == cudaSuccess ? SSM_OK
+                                                                               : SSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* dt_bias,
+                                    const float* A, const void* B, const void* C,
+                                    const float* Dskip, const void* z, void* y, float* h_last,
+                                    int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                                    void* stream_) {
+    if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
+    if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    int64_t bl, bld, bln, bd, bdn, dn;
+    if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) ||
+        !mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || !mul_ok(D, N, &dn) ||
+        bld > (INT64_MAX >> 4) || bln > (INT64_MAX >> 4) || bdn > (INT64_MAX >> 4))
+        return SSM_ERR_SIZE;
+    if ((bld && (!u || !delta || !y)) || (bln && (!B || !C)) || (dn && !A)) return SSM_ERR_NULL;
+    if (!elems_aligned(dtype, {u, delta, B, C, z, y}, {dt_bias, A, Dskip, h_last}))
+        return SSM_ERR_ALIGN;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (bd == 0) return SSM_OK;
+    if (L == 0) {
+        if (h_last) return from_cuda(cudaMemsetAsync(h_last, 0, sizeof(float) * bdn, stream));
+        return SSM_OK;
+    }
+    const bool fast = N == ssm::fast::NS && all_aligned16({u, delta, z, B, C, y, h_last}) &&
+                      (D * (int64_t)elem_size(dtype)) % 16 == 0;
+    if (!fast) {
+        cudaError_t e;
+        if (dtype == SSM_F32)
+            e = ssm::launch_scan_generic<float>(
+                static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+                static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+                static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D,
+                (int)N, stream);
+        else
+            e = ssm::launch_scan_generic<bf16>(
+                static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+                static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+                static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D,
+                (int)N, stream);
+        return from_cuda(e);
+    }
+    if (noalloc_scratch_need(batch, D, h_last != nullptr) > kNoallocScratchBytes)
+        return SSM_ERR_SCRATCH;
+    unsigned char* ws = nullptr;
+    const int st = noalloc_scratch_ptr(&ws);
+    if (st != SSM_OK) return st;
+    if (dtype == SSM_F32)
+        return launch_noalloc<float>(
+            static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+            static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+            static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D, ws, stream);
+    return launch_noalloc<bf16>(
+        static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+        static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+        static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, ws, stream);
+}
