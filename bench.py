@@ -43,7 +43,18 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="mamba2.8b", choices=sorted(WORKLOADS),
+                    help="scan shape (default: the Mamba-2.8B layer; the others are the "
+                         "smaller cases used for ncu captures)")
     return ap.parse_args()
+
+
+def _workloads():
+    from selective_state_space_113_b300 import workloads as wl
+    return {"mamba2.8b": wl.MAMBA_2P8B, "mamba130m": wl.MAMBA_130M, "longseq": wl.LONG_SEQ}
+
+
+WORKLOADS = ("mamba2.8b", "mamba130m", "longseq")
 
 
 def dist_env():
@@ -157,7 +168,7 @@ def bench_ours(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = wl.MAMBA_2P8B
+    w = _workloads()[args.workload]
     inp = wl.make_scan_inputs(w, device=dev, seed=w.seed + rank)
     y = torch.empty_like(inp["u"])
     h = torch.empty((w.batch, w.D, w.N), device=dev, dtype=torch.float32)
@@ -227,7 +238,7 @@ def bench_ours(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) u/delta/z/B/C, Mamba dt_bias init, A=-(n+1))",
         "config": {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.D, "N": w.N,
                    "state": "fp32", "arith": "fp32",
-                   "l2": "inputs 674 MB per step > 126 MB L2; no flush",
+                   "l2": f"inputs {alg / 1e6:.0f} MB per step > 126 MB L2; no flush",
                    "parallelism": f"replicas x{world} (independent workloads per GPU)"},
         "hbm_gbs": achieved_gbs,
         "hbm_frac_measured": achieved_gbs / peak,
@@ -240,13 +251,18 @@ def bench_ours(args, rank, world, local):
                      "traffic": traffic, "traffic_source": traffic_src},
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "gpu_launches": args.steps * LAUNCHES_PER_CALL,
+        "gpu_launches": args.steps * launches_per_call(w),
         "cpu_baseline": cpu,
     }
 
 
-# Kernels of this library launched per ssm_scan_fwd call on this workload.
-LAUNCHES_PER_CALL = 1
+def launches_per_call(w) -> int:
+    """Kernels of this library one ssm_scan_fwd call launches on ``w``: one for
+    the chained plan, three (chunk summaries, carry, output pass) for the plan
+    of narrow problems, which the library picks when batch * ceil(D/32) is
+    below 0.55 x the resident CTAs (148 SMs x 4)."""
+    chains = w.batch * -(-w.D // 32)
+    return 3 if chains * 100 < 148 * 4 * 55 else 1
 
 
 def bench_e2e(args, ssm, inp, w, dev, stream, world):
@@ -327,7 +343,7 @@ def bench_reference(args, rank, world):
         return None
     import torch
     from selective_state_space_113_b300 import workloads as wl
-    w = wl.MAMBA_2P8B
+    w = _workloads()[args.workload]
     inp = wl.make_scan_inputs(w, device="cpu", seed=w.seed)
     n = cores()
     channels = max(n, min(w.D, 128 * n))

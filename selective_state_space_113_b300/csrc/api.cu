@@ -227,10 +227,11 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
                    float* h_last, long long batch, long long L, long long D,
                    unsigned char* ws, cudaStream_t stream) {
     using namespace ssm::fast;
-    int dev = 0, sms = 0, occ = 0;
+    int dev = 0, sms = 0;
+    long long workers = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        prepare<T, (int)kChained>(&occ) != cudaSuccess || occ < 1)
+        prepare<T, (int)kChained>(sms, &workers) != cudaSuccess || workers < 1)
         return SSM_ERR_CUDA;
     CUtensorMap maps[5];
     if (!make_map<T>(&maps[0], u, D, L, batch, CH) || !make_map<T>(&maps[1], delta, D, L, batch, CH) ||
@@ -250,7 +251,6 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
     p.nCB = cdiv(D, CH);
     p.nchains = batch * p.nCB;
     p.wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
-    const long long workers = (long long)sms * occ;
     const long long P0 = cdiv(8 * workers, p.nchains);
     long long steps = cdiv(cdiv(L, P0 > 0 ? P0 : 1), TC) * TC;
     if (steps < TC) steps = TC;
@@ -265,9 +265,9 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
     p.flags = reinterpret_cast<unsigned*>(ws + 256);
     p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + head);
     p.total_units = p.nchains * p.P;
-    const int grid = (int)(p.total_units < workers ? p.total_units : workers);
-    return launch_mode<T, (int)kChained>(grid, maps, p, stream) == cudaSuccess ? SSM_OK
-                                                                               : SSM_ERR_CUDA;
+    return launch_mode<T, (int)kChained>(p.total_units, workers, maps, p, stream) == cudaSuccess
+               ? SSM_OK
+               : SSM_ERR_CUDA;
 }
 
 }  // namespace

@@ -49,7 +49,6 @@ constexpr int S = 4;     // stages in the shared-memory ring
 constexpr int LA = 2;    // stages the TMA issue runs ahead of the B/C widening
 constexpr int CH = 32;   // channels per unit (one per consumer lane)
 constexpr int NS = 16;   // state size handled here
-constexpr int THREADS = 64;
 constexpr unsigned kProducerSleepNs = 128;  // producer back-off between mbarrier polls
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -108,6 +107,16 @@ struct Layout {
     static constexpr int offBar = offMeta + S * (int)sizeof(Meta);
     static constexpr int kBytes = offBar + 3 * S * 8;
     static_assert(kTile % 128 == 0 && kRaw % 128 == 0 && kConv % 128 == 0, "TMA alignment");
+    // One pair's carve-out, rounded to 1 KiB so every pair's tiles stay aligned.
+    static constexpr int kPairBytes = (kBytes + 1023) & ~1023;
+    // Worker pairs (consumer + producer warp) per CTA: four for 2-byte
+    // elements (one consumer per SM sub-partition), two for float32, whose
+    // stages are twice as large.
+    static constexpr int kPairs = es == 2 ? 4 : 2;
+    static constexpr int kThreads = 64 * kPairs;
+    // Dynamic shared memory a CTA requests (+1 KiB for aligning the base).
+    static constexpr int kSmemBytes = kPairs * kPairBytes + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "CTA shared memory");
 };
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
@@ -290,7 +299,7 @@ __device__ __forceinline__ void run_stage_general(const unsigned char* st, int n
 template <typename T, int MODE>
 __device__ __forceinline__ void widen_rows(unsigned char* st, int lane) {
     using Lt = Layout<T>;
-    constexpr int kPairs = TC * NS / 2;
+    constexpr int kElemPairs = TC * NS / 2;
     const int n0 = 2 * (lane % (NS / 2));
     const float s0 = 1.0f / (float)(n0 + 1), s1 = 1.0f / (float)(n0 + 2);
     const T* Br = reinterpret_cast<const T*>(st + Lt::offBr);
@@ -298,7 +307,7 @@ __device__ __forceinline__ void widen_rows(unsigned char* st, int lane) {
     float2* Bc = reinterpret_cast<float2*>(st + Lt::offBc);
     float2* Cc = reinterpret_cast<float2*>(st + Lt::offCc);
 #pragma unroll
-    for (int i = 0; i < kPairs / 32; ++i) {
+    for (int i = 0; i < kElemPairs / 32; ++i) {
         const int w = lane + 32 * i;
         Bc[w] = make_float2(ld_elem(Br + 2 * w) * s0, ld_elem(Br + 2 * w + 1) * s1);
         if (MODE != kAggregate) Cc[w] = make_float2(ld_elem(Cr + 2 * w), ld_elem(Cr + 2 * w + 1));
@@ -306,23 +315,30 @@ __device__ __forceinline__ void widen_rows(unsigned char* st, int lane) {
 }
 
 template <typename T, int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Layout<T>::kThreads, 1)
 scan_fast_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmD,
                  const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmC, const Params p) {
     using Lt = Layout<T>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // A CTA is kPairs independent workers; worker i is consumer warp i and
+    // producer warp kPairs + i.  When the CTA is alone on its SM, warp w runs
+    // on SM sub-partition w % 4, so with four pairs every sub-partition gets
+    // one consumer (the recurrence) and one mostly sleeping producer.
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = warp % Lt::kPairs;
+    const bool producer = warp >= Lt::kPairs;
     // Stage tiles are TMA destinations: align the carve-out base to 1 KiB
-    // (the launch requests kBytes + 1024).
-    unsigned char* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+    // (the launch requests kSmemBytes, which includes that slack).
+    unsigned char* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u) +
+                          pair * Lt::kPairBytes;
     Meta* meta = reinterpret_cast<Meta*>(smem + Lt::offMeta);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lt::offBar);
     uint64_t* convd = full + S;
     uint64_t* empty = convd + S;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const volatile unsigned* vabort = p.abort;
 
-    if (threadIdx.x == 0) {
+    if (!producer && lane == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&convd[s], 32);
@@ -332,7 +348,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
     }
     __syncthreads();
 
-    if (warp == 1) {
+    if (producer) {
         // ---------------- producer warp: TMA issue (lane 0) + B/C widening
         if (lane == 0) {
             ptx::prefetch_tensormap(&tmU);

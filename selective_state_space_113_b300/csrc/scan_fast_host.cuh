@@ -74,21 +74,28 @@ inline int forced_plan() {
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
+// Sets the kernel's shared-memory limit and returns in *workers the number
+// of worker pairs that can be resident at once (resident CTAs x kPairs).
 template <typename T, int MODE>
-inline cudaError_t prepare(int* occ) {
+inline cudaError_t prepare(int sms, long long* workers) {
     auto kern = scan_fast_kernel<T, MODE>;
-    const int smem = Layout<T>::kBytes + 1024;
+    const int smem = Layout<T>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, THREADS, smem);
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Layout<T>::kThreads, smem);
+    *workers = (long long)sms * occ * Layout<T>::kPairs;
+    return e;
 }
 
+// Launches enough CTAs for min(units, workers) worker pairs.
 template <typename T, int MODE>
-inline cudaError_t launch_mode(int grid, const CUtensorMap* maps, const Params& p,
-                               cudaStream_t s) {
-    const int smem = Layout<T>::kBytes + 1024;
-    scan_fast_kernel<T, MODE><<<grid, THREADS, smem, s>>>(maps[0], maps[1], maps[2], maps[3],
-                                                          maps[4], p);
+inline cudaError_t launch_mode(long long units, long long workers, const CUtensorMap* maps,
+                               const Params& p, cudaStream_t s) {
+    const long long w = units < workers ? units : workers;
+    const int grid = (int)((w + Layout<T>::kPairs - 1) / Layout<T>::kPairs);
+    scan_fast_kernel<T, MODE><<<grid, Layout<T>::kThreads, Layout<T>::kSmemBytes, s>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], p);
     return cudaGetLastError();
 }
 
@@ -104,10 +111,10 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SSM_ERR_CUDA;
-    int occ_c = 0, occ_a = 0, occ_f = 0;
-    if (prepare<T, (int)kChained>(&occ_c) != cudaSuccess ||
-        prepare<T, (int)kAggregate>(&occ_a) != cudaSuccess ||
-        prepare<T, (int)kFromState>(&occ_f) != cudaSuccess || occ_c < 1 || occ_a < 1 || occ_f < 1)
+    long long wc = 0, wa = 0, wf = 0;
+    if (prepare<T, (int)kChained>(sms, &wc) != cudaSuccess ||
+        prepare<T, (int)kAggregate>(sms, &wa) != cudaSuccess ||
+        prepare<T, (int)kFromState>(sms, &wf) != cudaSuccess || wc < 1 || wa < 1 || wf < 1)
         return SSM_ERR_CUDA;
 
     CUtensorMap maps[5];
@@ -131,7 +138,7 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
     p.nchains = batch * p.nCB;
     p.wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
 
-    const long long workers = (long long)sms * occ_c;
+    const long long workers = wc;
     bool narrow = false;
     if (plan == kPlanNarrow) narrow = true;
     else if (plan == kPlanAuto) narrow = p.nchains * 100 < workers * 55;
@@ -141,7 +148,7 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
         const long long P0 = cdiv(8 * workers, p.nchains);
         steps = cdiv(cdiv(L, P0 > 0 ? P0 : 1), TC) * TC;
     } else {
-        const long long P0 = cdiv(4 * (long long)sms * occ_a, p.nchains);
+        const long long P0 = cdiv(4 * wa, p.nchains);
         steps = cdiv(cdiv(L, P0 < 2 ? 2 : P0), TC) * TC;
     }
     if (forced_steps > 0) steps = cdiv(forced_steps, TC) * TC;
@@ -186,17 +193,16 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + off_carry);
             p.total_units = p.nchains * p.P;
-            const int grid = (int)(p.total_units < workers ? p.total_units : workers);
-            if (launch_mode<T, (int)kChained>(grid, maps, p, stream) != cudaSuccess)
+            if (launch_mode<T, (int)kChained>(p.total_units, workers, maps, p, stream) !=
+                cudaSuccess)
                 status = SSM_ERR_CUDA;
         } else {
             p.agg = reinterpret_cast<float*>(ws + off_agg);
             p.hin = reinterpret_cast<float*>(ws + off_hin);
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.total_units = p.nchains * (p.P - 1);
-            const long long wa = (long long)sms * occ_a, wf = (long long)sms * occ_f;
-            const int grid_a = (int)(p.total_units < wa ? p.total_units : wa);
-            if (launch_mode<T, (int)kAggregate>(grid_a, maps, p, stream) != cudaSuccess) {
+            if (launch_mode<T, (int)kAggregate>(p.total_units, wa, maps, p, stream) !=
+                cudaSuccess) {
                 status = SSM_ERR_CUDA;
                 break;
             }
@@ -209,8 +215,8 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
             }
             p.ticket = reinterpret_cast<unsigned long long*>(ws + 16);
             p.total_units = p.nchains * p.P;
-            const int grid_f = (int)(p.total_units < wf ? p.total_units : wf);
-            if (launch_mode<T, (int)kFromState>(grid_f, maps, p, stream) != cudaSuccess)
+            if (launch_mode<T, (int)kFromState>(p.total_units, wf, maps, p, stream) !=
+                cudaSuccess)
                 status = SSM_ERR_CUDA;
         }
     } while (0);
