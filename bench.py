@@ -46,12 +46,22 @@ def parse():
     ap.add_argument("--workload", default="mamba2.8b", choices=sorted(WORKLOADS),
                     help="scan shape (default: the Mamba-2.8B layer; the others are the "
                          "smaller cases used for ncu captures)")
+    ap.add_argument("--L", type=int, default=None,
+                    help="override the workload's sequence length (shorter ncu captures)")
     return ap.parse_args()
 
 
 def _workloads():
     from selective_state_space_113_b300 import workloads as wl
     return {"mamba2.8b": wl.MAMBA_2P8B, "mamba130m": wl.MAMBA_130M, "longseq": wl.LONG_SEQ}
+
+
+def workload(args):
+    import dataclasses
+    w = _workloads()[args.workload]
+    if args.L is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_L{args.L}", L=args.L)
+    return w
 
 
 WORKLOADS = ("mamba2.8b", "mamba130m", "longseq")
@@ -168,7 +178,7 @@ def bench_ours(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = _workloads()[args.workload]
+    w = workload(args)
     inp = wl.make_scan_inputs(w, device=dev, seed=w.seed + rank)
     y = torch.empty_like(inp["u"])
     h = torch.empty((w.batch, w.D, w.N), device=dev, dtype=torch.float32)
@@ -343,7 +353,7 @@ def bench_reference(args, rank, world):
         return None
     import torch
     from selective_state_space_113_b300 import workloads as wl
-    w = _workloads()[args.workload]
+    w = workload(args)
     inp = wl.make_scan_inputs(w, device="cpu", seed=w.seed)
     n = cores()
     channels = max(n, min(w.D, 128 * n))

@@ -11,7 +11,7 @@
 #include <mutex>
 
 #include "common.cuh"
-#include "scan_fast_host.cuh"
+#include "scan_tile_host.cuh"
 #include "scan_generic.cuh"
 #include "step_generic.cuh"
 
@@ -77,16 +77,16 @@ extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bi
         return SSM_OK;
     }
     // Fast path: N == 16, 16-byte-aligned tensors and rows (TMA tiles).
-    const int plan = ssm::fast::forced_plan();
-    if (N == ssm::fast::NS && plan != ssm::fast::kPlanGeneric &&
-        all_aligned16({u, delta, z, B, C, y, h_last}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
+    const int plan = ssm::tile::forced_plan();
+    if (N == ssm::tile::NS && plan != ssm::tile::kPlanGeneric &&
+        all_aligned16({u, delta, z, B, C, y, h_last, A}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
         if (dtype == SSM_F32)
-            return ssm::fast::launch_scan_fast<float>(
+            return ssm::tile::launch_scan_tile<float>(
                 static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
                 static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
                 static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D, plan,
                 stream);
-        return ssm::fast::launch_scan_fast<bf16>(
+        return ssm::tile::launch_scan_tile<bf16>(
             static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
             static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
             static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, plan, stream);
@@ -177,8 +177,8 @@ extern "C" int ssm_abi_version(void) { return 1; }
 // all reserved up front by its own pool, or code in a context where a
 // cudaMalloc/cudaMallocAsync would synchronise, fail or be forbidden).  It is
 // the chained variant of the N == 16 fast kernel, whose scratch (unit ticket,
-// abort word, per-chain progress flags and, when h_last is NULL, the carried
-// chunk state) lives in the fixed device array below instead of a
+// abort word, per-sub-block progress flags and, when h_last is NULL, the
+// carried chunk state) lives in the fixed device array below instead of a
 // stream-ordered workspace.  Inputs the fast kernel does not take (other N,
 // unaligned tensors) run the generic kernel, which needs no scratch at all.
 namespace {
@@ -212,12 +212,11 @@ int noalloc_scratch_ptr(unsigned char** out) {
     return SSM_OK;
 }
 
-// Scratch bytes the chained plan needs: header (ticket, abort), one flag per
-// 32-channel chain, and the carried state when h_last cannot hold it.
+// Scratch bytes the chained plan needs: header (tickets, abort), one flag per
+// 32-channel sub-block, and the carried state when h_last cannot hold it.
 size_t noalloc_scratch_need(int64_t batch, int64_t D, bool have_h_last) {
-    const int64_t nchains = batch * ((D + ssm::fast::CH - 1) / ssm::fast::CH);
-    size_t bytes = ((256 + (size_t)nchains * 4) + 255) & ~(size_t)255;
-    if (!have_h_last) bytes += (size_t)(batch * D) * ssm::fast::NS * 4;
+    size_t bytes = ssm::tile::header_bytes(batch, D);
+    if (!have_h_last) bytes += (size_t)(batch * D) * ssm::tile::NS * 4;
     return bytes;
 }
 
@@ -226,39 +225,22 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
                    const T* Bm, const T* Cm, const float* Dskip, const T* z, T* y,
                    float* h_last, long long batch, long long L, long long D,
                    unsigned char* ws, cudaStream_t stream) {
-    using namespace ssm::fast;
+    using namespace ssm::tile;
     int dev = 0, sms = 0;
     long long workers = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         prepare<T, (int)kChained>(sms, &workers) != cudaSuccess || workers < 1)
         return SSM_ERR_CUDA;
-    CUtensorMap maps[5];
-    if (!make_map<T>(&maps[0], u, D, L, batch, CH) || !make_map<T>(&maps[1], delta, D, L, batch, CH) ||
-        !make_map<T>(&maps[2], z ? z : u, D, L, batch, CH) ||
-        !make_map<T>(&maps[3], Bm, NS, L, batch, NS) || !make_map<T>(&maps[4], Cm, NS, L, batch, NS))
+    CUtensorMap maps[6];
+    Params p;
+    if (!setup<T>(maps, &p, u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D))
         return SSM_ERR_CUDA;
-    Params p{};
-    p.y = y;
-    p.h_last = h_last;
-    p.dt_bias = dt_bias;
-    p.A = A;
-    p.Dskip = Dskip;
-    p.has_z = z != nullptr;
-    p.batch = batch;
-    p.L = L;
-    p.D = D;
-    p.nCB = cdiv(D, CH);
-    p.nchains = batch * p.nCB;
-    p.wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
-    const long long P0 = cdiv(8 * workers, p.nchains);
-    long long steps = cdiv(cdiv(L, P0 > 0 ? P0 : 1), TC) * TC;
-    if (steps < TC) steps = TC;
-    p.T = steps;
-    p.P = cdiv(L, steps);
-    const size_t head = ((256 + (size_t)p.nchains * 4) + 255) & ~(size_t)255;
-    // The array keeps the previous call's contents: reset the ticket, the
-    // abort word and the chain flags, which must start at zero.
+    p.T = chained_steps<T>(p.nchains, workers, L);
+    p.P = cdiv(L, p.T);
+    const size_t head = header_bytes(batch, D);
+    // The array keeps the previous call's contents: reset the tickets, the
+    // abort word and the sub-block flags, which must start at zero.
     if (cudaMemsetAsync(ws, 0, head, stream) != cudaSuccess) return SSM_ERR_CUDA;
     p.ticket = reinterpret_cast<unsigned long long*>(ws);
     p.abort = reinterpret_cast<unsigned*>(ws + 32);
@@ -294,7 +276,7 @@ extern "C" int ssm_scan_fwd_noalloc(const void* u, const void* delta, const floa
         if (h_last) return from_cuda(cudaMemsetAsync(h_last, 0, sizeof(float) * bdn, stream));
         return SSM_OK;
     }
-    const bool fast = N == ssm::fast::NS && all_aligned16({u, delta, z, B, C, y, h_last}) &&
+    const bool fast = N == ssm::tile::NS && all_aligned16({u, delta, z, B, C, y, h_last, A}) &&
                       (D * (int64_t)elem_size(dtype)) % 16 == 0;
     if (!fast) {
         cudaError_t e;

@@ -59,19 +59,26 @@ __device__ __forceinline__ void nanosleep(unsigned ns) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete, giving up
-// after `limit_ns` nanoseconds (false) or when *abort becomes non-zero.  A
-// non-zero `sleep_ns` puts the warp to sleep between polls, which leaves the
-// issue slots of its SM sub-partition to the warps that share it.
+// after about `limit_ns` nanoseconds (false) or, once the wait has lasted
+// ~100 us, when *abort is non-zero.  The time is taken from the SM cycle
+// counter (counted at an assumed clock of at most 2.1 GHz, so the limit is
+// never shorter than asked), and the abort word -- a global-memory load --
+// is only read in waits that are already long: the common short wait costs
+// no memory round trip.  A non-zero `sleep_ns` puts the warp to sleep
+// between polls, which leaves the issue slots of its SM sub-partition to the
+// warps that share it.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                           const volatile unsigned* abort, uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    const long long limit = (long long)(limit_ns * 21 / 10);
+    const long long t0 = clock64();
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if (sleep_ns) nanosleep(sleep_ns);
-        if ((spin & 31u) == 0) {
-            if (globaltimer() - t0 > limit_ns) return false;
-            if (abort && *abort) return false;
+        if ((spin & 63u) == 0) {
+            const long long dt = clock64() - t0;
+            if (dt > limit) return false;
+            if (dt > 200000 && abort && *abort) return false;
         }
     }
 }
@@ -84,6 +91,40 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 3-D tiled TMA store shared -> global (bulk async-group completion).
+// Coordinates past the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until at most N bulk async-groups of this thread still read their
+// shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until at most N bulk async-groups of this thread are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

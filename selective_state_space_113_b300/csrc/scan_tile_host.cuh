@@ -1,5 +1,5 @@
-// scan_fast_host.cuh -- plan choice, TMA descriptors, stream-ordered workspace
-// and launches for the N == 16 selective-scan kernel (scan_fast.cuh).
+// scan_tile_host.cuh -- plan choice, TMA descriptors, stream-ordered workspace
+// and launches for the N == 16 selective-scan kernel (scan_tile.cuh).
 #pragma once
 
 #include <cuda.h>
@@ -9,10 +9,10 @@
 #include <mutex>
 
 #include "../../include/ssmscan.h"
-#include "scan_fast.cuh"
+#include "scan_tile.cuh"
 
 namespace ssm {
-namespace fast {
+namespace tile {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -35,16 +35,16 @@ inline EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// Rank-3 map over a row-major [batch, L, inner] tensor, box {box_inner, TC, 1}.
+// Rank-3 map over a row-major [batch, L, inner] tensor, box {box_inner, box_t, 1}.
 template <typename T>
 inline bool make_map(CUtensorMap* m, const void* base, long long inner, long long L,
-                     long long batch, unsigned box_inner) {
+                     long long batch, unsigned box_inner, unsigned box_t) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
     const cuuint64_t es = sizeof(T);
     const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)L, (cuuint64_t)batch};
     const cuuint64_t strides[2] = {(cuuint64_t)inner * es, (cuuint64_t)inner * (cuuint64_t)L * es};
-    const cuuint32_t box[3] = {box_inner, (cuuint32_t)TC, 1u};
+    const cuuint32_t box[3] = {box_inner, box_t, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -74,39 +74,121 @@ inline int forced_plan() {
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// Sets the kernel's shared-memory limit and returns in *workers the number
-// of worker pairs that can be resident at once (resident CTAs x kPairs).
+// Sets the kernel's shared-memory limit and returns in *workers the number of
+// CTAs that can be resident at once.  Done once per device and kernel; later
+// calls read the cached count.
 template <typename T, int MODE>
 inline cudaError_t prepare(int sms, long long* workers) {
-    auto kern = scan_fast_kernel<T, MODE>;
-    const int smem = Layout<T>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static long long cached[kMaxDev] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDev) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cached[dev] > 0) {
+            *workers = cached[dev];
+            return cudaSuccess;
+        }
+    }
+    auto kern = scan_tile_kernel<T, MODE>;
+    const int smem = Cfg<T>::kSmemBytes;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Layout<T>::kThreads, smem);
-    *workers = (long long)sms * occ * Layout<T>::kPairs;
-    return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS, smem);
+    if (e != cudaSuccess) return e;
+    *workers = (long long)sms * occ;
+    if (dev >= 0 && dev < kMaxDev && *workers > 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        cached[dev] = *workers;
+    }
+    return cudaSuccess;
 }
 
-// Launches enough CTAs for min(units, workers) worker pairs.
+// Steps per unit for the chained plan.  With no more chains than workers
+// every worker takes a whole chain (splitting a chain only adds hand-offs,
+// since its pieces run one after another).  Otherwise a chain is cut into P
+// units so that the units, handed out chain-interleaved, fill their last
+// wave nearly completely; longer units are preferred because each unit
+// start costs about as much as ~24 steps.
+template <typename T>
+inline long long chained_steps(long long nchains, long long workers, long long L) {
+    constexpr long long TC = Cfg<T>::TC;
+    auto round_up = [](long long v) { return cdiv(v, TC) * TC; };
+    if (nchains <= workers) return round_up(L);
+    long long best = round_up(L);
+    double best_score = -1.0;
+    for (long long P = 1; P <= 64; ++P) {
+        const long long steps = round_up(cdiv(L, P));
+        const long long units = nchains * cdiv(L, steps);
+        const double waves = (double)units / (double)workers;
+        const double fill = waves / (double)cdiv(units, workers);
+        const double score = fill * (double)steps / (double)(steps + 24);
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = steps;
+        }
+    }
+    return best;
+}
+
+// Bytes of the workspace header: two tickets, the abort word, then one flag
+// per 32-channel sub-block, rounded to 256.
+inline size_t header_bytes(long long batch, long long D) {
+    return ((256 + (size_t)(batch * cdiv(D, CW)) * 4) + 255) & ~(size_t)255;
+}
+
 template <typename T, int MODE>
 inline cudaError_t launch_mode(long long units, long long workers, const CUtensorMap* maps,
                                const Params& p, cudaStream_t s) {
-    const long long w = units < workers ? units : workers;
-    const int grid = (int)((w + Layout<T>::kPairs - 1) / Layout<T>::kPairs);
-    scan_fast_kernel<T, MODE><<<grid, Layout<T>::kThreads, Layout<T>::kSmemBytes, s>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    const long long grid = units < workers ? units : workers;
+    scan_tile_kernel<T, MODE><<<(unsigned)grid, THREADS, Cfg<T>::kSmemBytes, s>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
     return cudaGetLastError();
 }
 
+// Fills the tensor maps and the fields of Params shared by every plan.
+template <typename T>
+inline bool setup(CUtensorMap* maps, Params* p, const T* u, const T* delta, const float* dt_bias,
+                  const float* A, const T* Bm, const T* Cm, const float* Dskip, const T* z,
+                  T* y, float* h_last, long long batch, long long L, long long D) {
+    constexpr unsigned TC = Cfg<T>::TC;
+    if (!make_map<T>(&maps[0], u, D, L, batch, CB, TC) ||
+        !make_map<T>(&maps[1], delta, D, L, batch, CB, TC) ||
+        !make_map<T>(&maps[2], z ? z : u, D, L, batch, CB, TC) ||
+        !make_map<T>(&maps[3], Bm, NS, L, batch, NS, TC) ||
+        !make_map<T>(&maps[4], Cm, NS, L, batch, NS, TC) ||
+        !make_map<T>(&maps[5], y, D, L, batch, CW, TC))
+        return false;
+    *p = Params{};
+    p->y = y;
+    p->h_last = h_last;
+    p->dt_bias = dt_bias;
+    p->A = A;
+    p->Dskip = Dskip;
+    p->has_z = z != nullptr;
+    p->test_stall = env_ll("SSM_TEST_STALL_CHAIN", 0) != 0;
+    p->batch = batch;
+    p->L = L;
+    p->D = D;
+    p->nCB = cdiv(D, CB);
+    p->nSB = cdiv(D, CW);
+    p->nchains = batch * p->nCB;
+    p->wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
+    return true;
+}
+
 // Returns an ssm_status_t.  Preconditions (checked by the caller): N == 16,
-// all typed tensors and h_last 16-byte aligned, D * sizeof(T) % 16 == 0,
+// u, delta, z, B, C, y, A and h_last 16-byte aligned, D * sizeof(T) % 16 == 0,
 // batch*D > 0, L > 0.
 template <typename T>
-int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const float* A,
+int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const float* A,
                      const T* Bm, const T* Cm, const float* Dskip, const T* z, T* y,
                      float* h_last, long long batch, long long L, long long D, int plan,
                      cudaStream_t stream) {
+    constexpr long long TC = Cfg<T>::TC;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -117,36 +199,18 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
         prepare<T, (int)kFromState>(sms, &wf) != cudaSuccess || wc < 1 || wa < 1 || wf < 1)
         return SSM_ERR_CUDA;
 
-    CUtensorMap maps[5];
-    if (!make_map<T>(&maps[0], u, D, L, batch, CH) || !make_map<T>(&maps[1], delta, D, L, batch, CH) ||
-        !make_map<T>(&maps[2], z ? z : u, D, L, batch, CH) ||
-        !make_map<T>(&maps[3], Bm, NS, L, batch, NS) || !make_map<T>(&maps[4], Cm, NS, L, batch, NS))
+    CUtensorMap maps[6];
+    Params p;
+    if (!setup<T>(maps, &p, u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D))
         return SSM_ERR_CUDA;
 
-    Params p{};
-    p.y = y;
-    p.h_last = h_last;
-    p.dt_bias = dt_bias;
-    p.A = A;
-    p.Dskip = Dskip;
-    p.has_z = z != nullptr;
-    p.test_stall = env_ll("SSM_TEST_STALL_CHAIN", 0) != 0;
-    p.batch = batch;
-    p.L = L;
-    p.D = D;
-    p.nCB = cdiv(D, CH);
-    p.nchains = batch * p.nCB;
-    p.wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
-
-    const long long workers = wc;
     bool narrow = false;
     if (plan == kPlanNarrow) narrow = true;
-    else if (plan == kPlanAuto) narrow = p.nchains * 100 < workers * 55;
+    else if (plan == kPlanAuto) narrow = p.nchains * 100 < wc * 55;
     long long steps;
     const long long forced_steps = env_ll("SSM_CHUNK_T", 0);
     if (!narrow) {
-        const long long P0 = cdiv(8 * workers, p.nchains);
-        steps = cdiv(cdiv(L, P0 > 0 ? P0 : 1), TC) * TC;
+        steps = chained_steps<T>(p.nchains, wc, L);
     } else {
         const long long P0 = cdiv(4 * wa, p.nchains);
         steps = cdiv(cdiv(L, P0 < 2 ? 2 : P0), TC) * TC;
@@ -158,11 +222,10 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
     if (p.P < 2) narrow = false;
 
     // Workspace: [0,8) phase-A ticket, [16,24) phase-B ticket, [32,36) abort,
-    // [256, 256+4*nchains) chain flags, then the state buffers.
+    // [256, 256 + 4*batch*nSB) sub-block flags, then the state buffers.
     const long long nch = batch * D;
-    const size_t head = 256 + (size_t)p.nchains * 4;
-    const size_t head_al = (head + 255) & ~(size_t)255;
-    size_t bytes = head_al;
+    const size_t head = header_bytes(batch, D);
+    size_t bytes = head;
     size_t off_carry = 0, off_agg = 0, off_hin = 0;
     if (!narrow) {
         if (!h_last) {
@@ -183,7 +246,7 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
     }
     int status = SSM_OK;
     do {
-        if (cudaMemsetAsync(ws, 0, head_al, stream) != cudaSuccess) {
+        if (cudaMemsetAsync(ws, 0, head, stream) != cudaSuccess) {
             status = SSM_ERR_CUDA;
             break;
         }
@@ -193,16 +256,14 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + off_carry);
             p.total_units = p.nchains * p.P;
-            if (launch_mode<T, (int)kChained>(p.total_units, workers, maps, p, stream) !=
-                cudaSuccess)
+            if (launch_mode<T, (int)kChained>(p.total_units, wc, maps, p, stream) != cudaSuccess)
                 status = SSM_ERR_CUDA;
         } else {
             p.agg = reinterpret_cast<float*>(ws + off_agg);
             p.hin = reinterpret_cast<float*>(ws + off_hin);
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.total_units = p.nchains * (p.P - 1);
-            if (launch_mode<T, (int)kAggregate>(p.total_units, wa, maps, p, stream) !=
-                cudaSuccess) {
+            if (launch_mode<T, (int)kAggregate>(p.total_units, wa, maps, p, stream) != cudaSuccess) {
                 status = SSM_ERR_CUDA;
                 break;
             }
@@ -215,8 +276,7 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
             }
             p.ticket = reinterpret_cast<unsigned long long*>(ws + 16);
             p.total_units = p.nchains * p.P;
-            if (launch_mode<T, (int)kFromState>(p.total_units, wf, maps, p, stream) !=
-                cudaSuccess)
+            if (launch_mode<T, (int)kFromState>(p.total_units, wf, maps, p, stream) != cudaSuccess)
                 status = SSM_ERR_CUDA;
         }
     } while (0);
@@ -224,5 +284,5 @@ int launch_scan_fast(const T* u, const T* delta, const float* dt_bias, const flo
     return status;
 }
 
-}  // namespace fast
+}  // namespace tile
 }  // namespace ssm
