@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--workload", default="mamba2.8b", choices=sorted(WORKLOADS),
                     help="scan shape (default: the Mamba-2.8B layer; the others are the "
                          "smaller cases used for ncu captures)")
@@ -228,6 +229,9 @@ def bench_ours(args, rank, world, local):
     achieved_gbs = alg / avg_launch_s / 1e9
     traffic, traffic_src = recorded_traffic()
 
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(ssm, dev, stream)
     e2e = None
     if not args.no_e2e:
         e2e = bench_e2e(args, ssm, inp, w, dev, stream, world)
@@ -260,10 +264,84 @@ def bench_ours(args, rank, world, local):
                      "median_launch_ms": launch_ms[len(launch_ms) // 2],
                      "traffic": traffic, "traffic_source": traffic_src},
         "clocks": clocks.summary(),
+        "decode": decode,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_call(w),
         "cpu_baseline": cpu,
     }
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic bytes of one decode step: state read and written (float32),
+    u, delta, z read and y written (dtype), B and C rows, A, dt_bias, Dskip."""
+    es = 2 if w.dtype == torch_bf16() else 4
+    return (2 * w.batch * w.D * w.N * 4 + 4 * w.batch * w.D * es + 2 * w.batch * w.N * es
+            + w.D * w.N * 4 + 2 * w.D * 4)
+
+
+def torch_bf16():
+    import torch
+    return torch.bfloat16
+
+
+def bench_decode(ssm, dev, stream, reps: int = 5):
+    """The 64-token decode of 256 sequences x D 5120 x N 16 (ssm_step on a
+    stored float32 state), as plain launches and replayed as one CUDA graph."""
+    import torch
+    from selective_state_space_113_b300 import workloads as wl
+    w = wl.DECODE
+    inp = wl.make_step_inputs(w, device=dev)
+    state0 = inp["state"]
+    state = state0.clone()
+    ys = torch.empty((w.steps, w.batch, w.D), device=dev, dtype=w.dtype)
+
+    def run():
+        # torch's current stream: the capturing stream inside torch.cuda.graph
+        for s in range(w.steps):
+            ssm.ssm_step(state, inp["u"][s], inp["delta"][s], inp["dt_bias"], inp["A"],
+                         inp["B"][s], inp["C"][s], inp["Dskip"], inp["z"][s], ys[s])
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            state.copy_(state0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None or ms < best else best
+        return best
+
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize(dev)
+    plain_ms = timed(run)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    torch.cuda.synchronize(dev)
+    graph_ms = timed(g.replay)
+    # the graph must have done the work: its result equals the plain run's
+    state.copy_(state0)
+    run()
+    ref = state.clone()
+    state.copy_(state0)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    if not torch.equal(ref, state):
+        raise RuntimeError("decode graph replay differs from plain launches")
+    per_step = decode_bytes(w)
+    peak, kind = measured_peaks()
+    us = graph_ms * 1e3 / w.steps
+    gbs = per_step / (us * 1e-6) / 1e9
+    return {"workload": w.name, "steps": w.steps, "bytes_per_step": per_step,
+            "us_per_step_graph": us, "us_per_step_launches": plain_ms * 1e3 / w.steps,
+            "elements_per_s": w.batch * w.D / (us * 1e-6), "gbs": gbs,
+            "hbm_frac": gbs / peak, "peak_source": kind, "kernel_launches": w.steps,
+            "note": "best of %d; the 84 MB state can stay resident in the 126 MB L2 across "
+                    "steps, so GB/s is algorithmic bytes / time, not DRAM traffic" % reps}
 
 
 def launches_per_call(w) -> int:

@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "scan_tile_host.cuh"
 #include "scan_generic.cuh"
+#include "step_fast.cuh"
 #include "step_generic.cuh"
 
 namespace {
@@ -125,6 +126,20 @@ extern "C" int ssm_step(float* state, const void* u, const void* delta, const fl
     if (bd == 0) return SSM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     cudaError_t e;
+    if (N == ssm::stepk::NS && all_aligned16({state, A}) && !std::getenv("SSM_FORCE_GENERIC_STEP")) {
+        // Fast path: four threads per channel, one float4 of state each.
+        if (dtype == SSM_F32)
+            e = ssm::stepk::launch_step16<float>(
+                state, static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+                static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+                static_cast<const float*>(z), static_cast<float*>(y), batch, D, stream);
+        else
+            e = ssm::stepk::launch_step16<bf16>(
+                state, static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+                static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+                static_cast<const bf16*>(z), static_cast<bf16*>(y), batch, D, stream);
+        return from_cuda(e);
+    }
     if (dtype == SSM_F32)
         e = ssm::launch_step_generic<float>(
             state, static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
