@@ -126,7 +126,8 @@ extern "C" int ssm_step(float* state, const void* u, const void* delta, const fl
     if (bd == 0) return SSM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     cudaError_t e;
-    if (N == ssm::stepk::NS && all_aligned16({state, A}) && !std::getenv("SSM_FORCE_GENERIC_STEP")) {
+    if (N == ssm::stepk::NS && all_aligned16({state, A}) && D <= ssm::stepk::kMaxD &&
+        batch <= ssm::stepk::kMaxBatch && !std::getenv("SSM_FORCE_GENERIC_STEP")) {
         // Fast path: four threads per channel, one float4 of state each.
         if (dtype == SSM_F32)
             e = ssm::stepk::launch_step16<float>(
@@ -251,8 +252,7 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
     Params p;
     if (!setup<T>(maps, &p, u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D))
         return SSM_ERR_CUDA;
-    p.T = chained_steps<T>(p.nchains, workers, L);
-    p.P = cdiv(L, p.T);
+    p.G = chained_grid<T>(p.nchains, workers, L, 0);
     const size_t head = header_bytes(batch, D);
     // The array keeps the previous call's contents: reset the tickets, the
     // abort word and the sub-block flags, which must start at zero.
@@ -261,10 +261,8 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
     p.abort = reinterpret_cast<unsigned*>(ws + 32);
     p.flags = reinterpret_cast<unsigned*>(ws + 256);
     p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + head);
-    p.total_units = p.nchains * p.P;
-    return launch_mode<T, (int)kChained>(p.total_units, workers, maps, p, stream) == cudaSuccess
-               ? SSM_OK
-               : SSM_ERR_CUDA;
+    return launch_mode<T, (int)kChained>(p.G, maps, p, stream) == cudaSuccess ? SSM_OK
+                                                                             : SSM_ERR_CUDA;
 }
 
 }  // namespace

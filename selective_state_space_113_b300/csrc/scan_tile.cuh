@@ -6,12 +6,11 @@
 // 1304; the SiLU(z) gate of the agenticai-flow Mamba block diagram), in
 // float32 with a float32 state.
 //
-// Work decomposition.  A unit is one CTA tile: 128 channels of one batch
-// entry over T consecutive steps.  Units of one 128-channel block form a
-// chain along the sequence.  CTAs are persistent (one per SM) and take units
-// from an atomic ticket counter in chain-interleaved order.  A CTA has nine
-// warps with fixed roles:
-//   warp 8      TMA warp: takes tickets, loads each unit's per-channel
+// Work decomposition.  A chain is one 128-channel block of one batch entry
+// along the whole sequence; a piece is a run of consecutive stages of one
+// chain, the work of one CTA tile.  CTAs are persistent (one per SM).  A CTA
+// has nine warps with fixed roles:
+//   warp 8      TMA warp: walks the CTA's pieces, loads each piece's per-channel
 //               parameters and carried state into shared memory, and streams
 //               the unit's u, delta, z, B and C in stages of TC steps by TMA
 //               (one 128-channel box per tensor and stage).
@@ -26,11 +25,17 @@
 // consumer (FMA-bound) next to its helper (SFU-bound).
 //
 // Three plans use this kernel:
-//   kChained   -- each unit starts from its predecessor's final state, passed
-//                 through global memory with release/acquire flags (bounded
-//                 waits, done by the TMA warp while it prefetches).  Used
-//                 when the chains fill the GPU.
-//   kAggregate -- phase 1 of the narrow-problem plan: each unit runs from a
+//   kChained   -- a static split: the chain-major space of (chain, stage) is
+//                 cut into one equal contiguous range per CTA, and each CTA
+//                 walks its range from the last chain to the first.  A chain
+//                 cut between CTAs i-1 and i is then the first piece CTA i-1
+//                 runs and the last piece CTA i runs, so the state CTA i needs
+//                 (passed through global memory with release/acquire flags;
+//                 bounded waits, done by the TMA warp while it prefetches) is
+//                 ready long before it is wanted.  Used when the chains fill
+//                 the GPU.
+//   kAggregate -- phase 1 of the narrow-problem plan: chains are cut into P
+//                 units of T steps taken from an atomic ticket; each runs from a
 //                 zero state and records sum(log2-domain dt) and its final
 //                 state (the unit's affine summary; no y is written).
 //   kFromState -- phase 3: each unit starts from a state computed by the carry
@@ -72,17 +77,17 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 enum Mode : int { kChained = 0, kAggregate = 1, kFromState = 2 };
 
-// Stage flags: first / last stage of a unit, end of work, carried state
-// present in the stage header.
-enum MetaFlags : int { kFirst = 1, kLast = 2, kEnd = 4, kHasState = 8 };
+// Stage flags: first / last stage of a piece, end of work, carried state
+// present in the stage header, piece ends at the end of its chain.
+enum MetaFlags : int { kFirst = 1, kLast = 2, kEnd = 4, kHasState = 8, kChainEnd = 16 };
 
 struct Meta {
-    long long unit;
+    long long chain;
     long long t0;
     int nvalid;   // valid steps in the stage (< TC only at the sequence end)
     int flags;
     int geo;      // bit w: consumer warp w's 32 channels have a geometric A row
-    int pad;
+    int piece;    // index of the piece within its chain (the unit index k)
 };
 
 // Per-channel unit parameters, written by the TMA warp into the header of a
@@ -100,15 +105,18 @@ struct Params {
     int has_z;
     int test_stall;         // never publish chunk states (failure-detection tests)
     long long batch, L, D;
-    long long T;            // steps per unit (multiple of TC)
-    long long P;            // units per chain
+    long long T;            // steps per unit (narrow plan; multiple of TC)
+    long long P;            // units per chain (narrow plan)
+    long long nst;          // stages per chain, ceil(L / TC) (chained plan)
+    long long G;            // CTAs of the chained plan's static split
+    long long Wst;          // nchains * nst
     long long nchains;      // batch * nCB
     long long nCB;          // ceil(D / CB)
     long long nSB;          // ceil(D / CW): 32-channel sub-blocks per batch entry
     long long total_units;
     unsigned long long* ticket;
     unsigned* abort;
-    unsigned* flags;        // [batch * nSB] completed chunks per sub-block (kChained)
+    unsigned* flags;        // [batch * nSB] completed pieces per sub-block (kChained)
     float* carry;           // [batch, D, NS] chained state (h_last or scratch)
     float* agg;             // [P][batch*D][NS+1] phase-1 summaries (kAggregate)
     const float* hin;       // [P][batch*D][NS] phase-3 initial states (kFromState)
@@ -482,7 +490,15 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
         const uint32_t stage_tx =
             (MODE == kAggregate) ? 2 * C::kTile + C::kRaw
                                  : 2 * C::kTile + 2 * C::kRaw + (p.has_z ? C::kTile : 0);
-        long long cur_unit = -1, cur_t0 = 0, cur_end = 0, cur_b = 0, cur_d0 = 0, cur_k = 0;
+        // Piece source.  kChained: the CTA's range [r0, r1) of the
+        // chain-major stage space, walked from its last chain to its first.
+        // Narrow-plan modes: units k * T .. (k+1) * T of a chain, from the
+        // ticket counter.
+        const long long r0 = (long long)blockIdx.x * p.Wst / (p.G > 0 ? p.G : 1);
+        const long long r1 = ((long long)blockIdx.x + 1) * p.Wst / (p.G > 0 ? p.G : 1);
+        long long next_chain = (MODE == kChained) ? (r1 - 1) / (p.nst > 0 ? p.nst : 1) : 0;
+        long long cur_chain = -1, cur_t0 = 0, cur_end = 0, cur_b = 0, cur_d0 = 0, cur_k = 0;
+        bool chain_end = false;
         long long j = 0;
         bool failed = false;
         for (;; ++j) {
@@ -493,12 +509,38 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             }
             unsigned char* st = smem + slot * C::kStage;
             int flags = 0, geo = 0;
-            if (cur_unit < 0 || cur_t0 >= cur_end) {
-                unsigned long long tk = 0;
-                if (lane == 0) tk = atomicAdd(p.ticket, 1ull);
-                tk = __shfl_sync(0xffffffffu, tk, 0);
-                if ((long long)tk >= p.total_units ||
-                    *reinterpret_cast<const volatile unsigned*>(p.abort)) {
+            if (cur_chain < 0 || cur_t0 >= cur_end) {
+                bool more;
+                if (MODE == kChained) {
+                    more = r0 < r1 && next_chain >= r0 / p.nst;
+                    if (more) {
+                        const long long c = next_chain--;
+                        const long long s0 = (r0 > c * p.nst ? r0 : c * p.nst) - c * p.nst;
+                        const long long s1 =
+                            (r1 < (c + 1) * p.nst ? r1 : (c + 1) * p.nst) - c * p.nst;
+                        // CTA holding the chain's first stage; the pieces of a
+                        // chain sit on consecutive CTAs.
+                        const long long i0 = ((c * p.nst + 1) * p.G + p.Wst - 1) / p.Wst - 1;
+                        cur_chain = c;
+                        cur_k = (long long)blockIdx.x - i0;
+                        cur_t0 = s0 * TC;
+                        cur_end = s1 * TC < p.L ? s1 * TC : p.L;
+                        chain_end = s1 == p.nst;
+                    }
+                } else {
+                    unsigned long long tk = 0;
+                    if (lane == 0) tk = atomicAdd(p.ticket, 1ull);
+                    tk = __shfl_sync(0xffffffffu, tk, 0);
+                    more = (long long)tk < p.total_units;
+                    if (more) {
+                        cur_k = (long long)tk / p.nchains;
+                        cur_chain = (long long)tk % p.nchains;
+                        cur_t0 = cur_k * p.T;
+                        cur_end = cur_t0 + p.T < p.L ? cur_t0 + p.T : p.L;
+                        chain_end = cur_end == p.L;
+                    }
+                }
+                if (!more || *reinterpret_cast<const volatile unsigned*>(p.abort)) {
                     if (lane == 0) {
                         meta[slot].flags = kEnd;
                         ptx::mbar_arrive(&full[slot]);
@@ -506,13 +548,8 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                     ++j;
                     break;
                 }
-                cur_unit = (long long)tk;
-                cur_k = cur_unit / p.nchains;
-                const long long chain = cur_unit % p.nchains;
-                cur_b = chain / p.nCB;
-                cur_d0 = (chain % p.nCB) * CB;
-                cur_t0 = cur_k * p.T;
-                cur_end = cur_t0 + p.T < p.L ? cur_t0 + p.T : p.L;
+                cur_b = cur_chain / p.nCB;
+                cur_d0 = (cur_chain % p.nCB) * CB;
                 bool has_state = false, ok = true;
                 geo = fill_header<T, MODE>(st, p, cur_b, cur_d0, cur_k, &has_state, &ok, lane);
                 if (!ok) {
@@ -530,14 +567,15 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                 flags |= kFirst | (has_state ? kHasState : 0);
             }
             const int nvalid = (int)(cur_end - cur_t0 < TC ? cur_end - cur_t0 : TC);
-            if (cur_t0 + TC >= cur_end) flags |= kLast;
+            if (cur_t0 + TC >= cur_end) flags |= kLast | (chain_end ? kChainEnd : 0);
             __syncwarp();
             if (lane == 0) {
-                meta[slot].unit = cur_unit;
+                meta[slot].chain = cur_chain;
                 meta[slot].t0 = cur_t0;
                 meta[slot].nvalid = nvalid;
                 meta[slot].flags = flags;
                 meta[slot].geo = geo;
+                meta[slot].piece = (int)cur_k;
                 ptx::mbar_arrive_expect_tx(&full[slot], stage_tx);
                 const int x = (int)cur_d0, yy = (int)cur_t0, z = (int)cur_b;
                 ptx::tma_load_3d(st + C::offU, &tmU, &full[slot], x, yy, z);
@@ -628,8 +666,8 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
         if (m.flags & kEnd) break;
         const unsigned char* st = smem + slot * C::kStage;
         if (m.flags & kFirst) {
-            k = m.unit / p.nchains;
-            chain = m.unit % p.nchains;
+            k = m.piece;
+            chain = m.chain;
             b = chain / p.nCB;
             d0 = (chain % p.nCB) * CB + CW * w;
             d = d0 + lane;
@@ -691,7 +729,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
         if (lane == 0) ptx::mbar_arrive(&empty[slot]);
         if (m.flags & kLast) {
             if (MODE == kChained) {
-                if (k + 1 < p.P) {
+                if (!(m.flags & kChainEnd)) {
                     if (valid) {
                         float4* dst = reinterpret_cast<float4*>(p.carry + (b * p.D + d) * NS);
 #pragma unroll
@@ -720,7 +758,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                     }
                 }
             } else {
-                if (valid && p.h_last && k == p.P - 1) {
+                if (valid && p.h_last && (m.flags & kChainEnd)) {
                     float4* dst = reinterpret_cast<float4*>(p.h_last + (b * p.D + d) * NS);
 #pragma unroll
                     for (int i = 0; i < NS / 4; ++i)

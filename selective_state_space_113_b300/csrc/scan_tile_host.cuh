@@ -107,31 +107,24 @@ inline cudaError_t prepare(int sms, long long* workers) {
     return cudaSuccess;
 }
 
-// Steps per unit for the chained plan.  With no more chains than workers
-// every worker takes a whole chain (splitting a chain only adds hand-offs,
-// since its pieces run one after another).  Otherwise a chain is cut into P
-// units so that the units, handed out chain-interleaved, fill their last
-// wave nearly completely; longer units are preferred because each unit
-// start costs about as much as ~24 steps.
+// CTAs of the chained plan's static split.  With no more chains than
+// resident CTAs each CTA takes one whole chain; otherwise every resident CTA
+// takes an equal share of the chain-major stage space (at least one chain
+// each, so a cut chain's first piece is always run first by its holder).
+// `piece_steps` > 0 (development and tests) asks for pieces of about that many
+// steps instead, which cuts chains into consecutive pieces.
 template <typename T>
-inline long long chained_steps(long long nchains, long long workers, long long L) {
+inline long long chained_grid(long long nchains, long long workers, long long L,
+                              long long piece_steps) {
     constexpr long long TC = Cfg<T>::TC;
-    auto round_up = [](long long v) { return cdiv(v, TC) * TC; };
-    if (nchains <= workers) return round_up(L);
-    long long best = round_up(L);
-    double best_score = -1.0;
-    for (long long P = 1; P <= 64; ++P) {
-        const long long steps = round_up(cdiv(L, P));
-        const long long units = nchains * cdiv(L, steps);
-        const double waves = (double)units / (double)workers;
-        const double fill = waves / (double)cdiv(units, workers);
-        const double score = fill * (double)steps / (double)(steps + 24);
-        if (score > best_score + 1e-9) {
-            best_score = score;
-            best = steps;
-        }
+    const long long nst = cdiv(L, TC);
+    long long g = nchains <= workers ? nchains : workers;
+    if (piece_steps > 0) {
+        const long long want = cdiv(nchains * nst * TC, piece_steps);
+        g = want < workers ? want : workers;
     }
-    return best;
+    if (g > nchains * nst) g = nchains * nst;
+    return g < 1 ? 1 : g;
 }
 
 // Bytes of the workspace header: two tickets, the abort word, then one flag
@@ -141,9 +134,8 @@ inline size_t header_bytes(long long batch, long long D) {
 }
 
 template <typename T, int MODE>
-inline cudaError_t launch_mode(long long units, long long workers, const CUtensorMap* maps,
-                               const Params& p, cudaStream_t s) {
-    const long long grid = units < workers ? units : workers;
+inline cudaError_t launch_mode(long long grid, const CUtensorMap* maps, const Params& p,
+                               cudaStream_t s) {
     scan_tile_kernel<T, MODE><<<(unsigned)grid, THREADS, Cfg<T>::kSmemBytes, s>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
     return cudaGetLastError();
@@ -176,6 +168,8 @@ inline bool setup(CUtensorMap* maps, Params* p, const T* u, const T* delta, cons
     p->nCB = cdiv(D, CB);
     p->nSB = cdiv(D, CW);
     p->nchains = batch * p->nCB;
+    p->nst = cdiv(L, Cfg<T>::TC);
+    p->Wst = p->nchains * p->nst;
     p->wait_ns = (unsigned long long)env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
     return true;
 }
@@ -207,19 +201,17 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
     bool narrow = false;
     if (plan == kPlanNarrow) narrow = true;
     else if (plan == kPlanAuto) narrow = p.nchains * 100 < wc * 55;
-    long long steps;
     const long long forced_steps = env_ll("SSM_CHUNK_T", 0);
-    if (!narrow) {
-        steps = chained_steps<T>(p.nchains, wc, L);
-    } else {
+    if (narrow) {
         const long long P0 = cdiv(4 * wa, p.nchains);
-        steps = cdiv(cdiv(L, P0 < 2 ? 2 : P0), TC) * TC;
+        long long steps = cdiv(cdiv(L, P0 < 2 ? 2 : P0), TC) * TC;
+        if (forced_steps > 0) steps = cdiv(forced_steps, TC) * TC;
+        if (steps < TC) steps = TC;
+        p.T = steps;
+        p.P = cdiv(L, steps);
+        if (p.P < 2) narrow = false;
     }
-    if (forced_steps > 0) steps = cdiv(forced_steps, TC) * TC;
-    if (steps < TC) steps = TC;
-    p.T = steps;
-    p.P = cdiv(L, steps);
-    if (p.P < 2) narrow = false;
+    if (!narrow) p.G = chained_grid<T>(p.nchains, wc, L, forced_steps);
 
     // Workspace: [0,8) phase-A ticket, [16,24) phase-B ticket, [32,36) abort,
     // [256, 256 + 4*batch*nSB) sub-block flags, then the state buffers.
@@ -255,15 +247,15 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
         if (!narrow) {
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + off_carry);
-            p.total_units = p.nchains * p.P;
-            if (launch_mode<T, (int)kChained>(p.total_units, wc, maps, p, stream) != cudaSuccess)
+            if (launch_mode<T, (int)kChained>(p.G, maps, p, stream) != cudaSuccess)
                 status = SSM_ERR_CUDA;
         } else {
             p.agg = reinterpret_cast<float*>(ws + off_agg);
             p.hin = reinterpret_cast<float*>(ws + off_hin);
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.total_units = p.nchains * (p.P - 1);
-            if (launch_mode<T, (int)kAggregate>(p.total_units, wa, maps, p, stream) != cudaSuccess) {
+            if (launch_mode<T, (int)kAggregate>(p.total_units < wa ? p.total_units : wa, maps, p,
+                                                stream) != cudaSuccess) {
                 status = SSM_ERR_CUDA;
                 break;
             }
@@ -276,7 +268,8 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
             }
             p.ticket = reinterpret_cast<unsigned long long*>(ws + 16);
             p.total_units = p.nchains * p.P;
-            if (launch_mode<T, (int)kFromState>(p.total_units, wf, maps, p, stream) != cudaSuccess)
+            if (launch_mode<T, (int)kFromState>(p.total_units < wf ? p.total_units : wf, maps, p,
+                                                stream) != cudaSuccess)
                 status = SSM_ERR_CUDA;
         }
     } while (0);

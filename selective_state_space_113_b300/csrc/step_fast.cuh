@@ -33,86 +33,74 @@ __device__ __forceinline__ float expm1_from(float x, float ex) {
     return ex - 1.0f;
 }
 
-// Each group of four threads updates J channels, 1/J of the grid apart, with
-// every load issued before any arithmetic (J = 1 measured fastest).
-constexpr int J = 1;
-
+// Grid: x covers the 4*D threads of one batch entry, y is the batch entry, so
+// no thread divides by D.
 template <typename T>
 __global__ void __launch_bounds__(THREADS)
 step16_kernel(float* __restrict__ state, const T* __restrict__ u, const T* __restrict__ delta,
               const float* __restrict__ dt_bias, const float* __restrict__ A,
               const T* __restrict__ Bm, const T* __restrict__ Cm,
               const float* __restrict__ Dskip, const T* __restrict__ z, T* __restrict__ y,
-              long long batch, long long D, long long half) {
-    const long long gid = (long long)blockIdx.x * THREADS + threadIdx.x;
-    const int part = (int)(gid & 3);          // states 4*part .. 4*part + 3
-    const long long nch = batch * D;
-    long long ch[J];
-    bool valid[J];
-    float ut[J], v[J];
-    float4 a4[J], h4[J];
+              long long D) {
+    const long long b = blockIdx.y;
+    const int tid = blockIdx.x * THREADS + threadIdx.x;   // < 4*D (checked on the host)
+    const int part = tid & 3;                              // states 4*part .. 4*part + 3
     // Threads past the last channel stay (the shuffles below need the whole
     // warp) but work on channel 0 and store nothing.
+    const bool valid = (tid >> 2) < D;
+    const long long d = valid ? (tid >> 2) : 0;
+    const long long ch = b * D + d;
+    const float ut = to_f32(u[ch]);
+    const float v = to_f32(delta[ch]) + (dt_bias ? dt_bias[d] : 0.0f);
+    const float4 a4 = *reinterpret_cast<const float4*>(A + d * NS + 4 * part);
+    float4* hp = reinterpret_cast<float4*>(state + ch * NS + 4 * part);
+    const float4 h4 = *hp;
+    // softplus in the base-2 domain: dl = log2(1 + 2^(v log2 e)) = dt / ln 2
+    const float dl = v > 20.0f ? v * kLog2e : ptx::lg2(1.0f + ptx::ex2(v * kLog2e));
+    const float dt = dl * kLn2;
+    const T* Bt = Bm + b * NS + 4 * part;
+    const T* Ct = Cm + b * NS + 4 * part;
+    const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+    const float h[4] = {h4.x, h4.y, h4.z, h4.w};
+    float hn[4];
+    float acc = 0.0f;
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const long long c = (gid >> 2) + j * half;
-        valid[j] = (gid >> 2) < half && c < nch;
-        ch[j] = valid[j] ? c : 0;
-        const long long d = ch[j] % D;
-        ut[j] = to_f32(u[ch[j]]);
-        v[j] = to_f32(delta[ch[j]]) + (dt_bias ? dt_bias[d] : 0.0f);
-        a4[j] = *reinterpret_cast<const float4*>(A + d * NS + 4 * part);
-        h4[j] = *reinterpret_cast<const float4*>(state + ch[j] * NS + 4 * part);
+    for (int i = 0; i < 4; ++i) {
+        const float x = dt * a[i];
+        const float ex = ptx::ex2(dl * a[i]);                  // exp(dt A) = A_bar
+        const float em1 = expm1_from(x, ex);                   // A_bar - 1
+        // B_bar / B = (A_bar - 1) / A, or dt at A == 0; the approximate
+        // reciprocal (relative error ~1e-7) replaces an IEEE division.
+        const float coef = (a[i] != 0.0f) ? em1 * ptx::rcp(a[i]) : dt;
+        hn[i] = fmaf(ex, h[i], coef * to_f32(Bt[i]) * ut);
+        acc = fmaf(to_f32(Ct[i]), hn[i], acc);
     }
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const long long b = ch[j] / D, d = ch[j] - b * D;
-        // softplus in the base-2 domain: dl = log2(1 + 2^(v log2 e)) = dt / ln 2
-        const float dl = v[j] > 20.0f ? v[j] * kLog2e : ptx::lg2(1.0f + ptx::ex2(v[j] * kLog2e));
-        const float dt = dl * kLn2;
-        const T* Bt = Bm + b * NS + 4 * part;
-        const T* Ct = Cm + b * NS + 4 * part;
-        const float a[4] = {a4[j].x, a4[j].y, a4[j].z, a4[j].w};
-        const float h[4] = {h4[j].x, h4[j].y, h4[j].z, h4[j].w};
-        float hn[4];
-        float acc = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x = dt * a[i];
-            const float ex = ptx::ex2(dl * a[i]);                  // exp(dt A) = A_bar
-            const float em1 = expm1_from(x, ex);                   // A_bar - 1
-            // B_bar / B = (A_bar - 1) / A, or dt at A == 0; the approximate
-            // reciprocal (relative error ~1e-7) replaces an IEEE division.
-            const float coef = (a[i] != 0.0f) ? em1 * ptx::rcp(a[i]) : dt;
-            hn[i] = fmaf(ex, h[i], coef * to_f32(Bt[i]) * ut[j]);
-            acc = fmaf(to_f32(Ct[i]), hn[i], acc);
+    if (valid) *hp = make_float4(hn[0], hn[1], hn[2], hn[3]);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if (valid && part == 0) {
+        acc = fmaf(Dskip ? Dskip[d] : 0.0f, ut, acc);
+        if (z) {
+            const float zt = to_f32(z[ch]);
+            acc *= zt * ptx::rcp(1.0f + ptx::ex2(-zt * kLog2e));
         }
-        if (valid[j])
-            *reinterpret_cast<float4*>(state + ch[j] * NS + 4 * part) =
-                make_float4(hn[0], hn[1], hn[2], hn[3]);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        if (valid[j] && part == 0) {
-            acc = fmaf(Dskip ? Dskip[d] : 0.0f, ut[j], acc);
-            if (z) {
-                const float zt = to_f32(z[ch[j]]);
-                acc *= zt * ptx::rcp(1.0f + ptx::ex2(-zt * kLog2e));
-            }
-            y[ch[j]] = from_f32<T>(acc);
-        }
+        y[ch] = from_f32<T>(acc);
     }
 }
+
+// Largest D the one-launch grid takes (4*D threads of one batch entry must
+// fit an int, and batch fits the grid's y extent).
+constexpr long long kMaxD = (1LL << 29);
+constexpr long long kMaxBatch = 65535;
 
 template <typename T>
 static cudaError_t launch_step16(float* state, const T* u, const T* delta, const float* dt_bias,
                                  const float* A, const T* Bm, const T* Cm, const float* Dskip,
                                  const T* z, T* y, long long batch, long long D,
                                  cudaStream_t stream) {
-    const long long half = (batch * D + J - 1) / J;   // channel groups per pass
-    const long long threads = half * 4;
-    const long long blocks = (threads + THREADS - 1) / THREADS;
-    step16_kernel<T><<<(unsigned)blocks, THREADS, 0, stream>>>(state, u, delta, dt_bias, A, Bm,
-                                                               Cm, Dskip, z, y, batch, D, half);
+    const dim3 grid((unsigned)((4 * D + THREADS - 1) / THREADS), (unsigned)batch);
+    step16_kernel<T><<<grid, THREADS, 0, stream>>>(state, u, delta, dt_bias, A, Bm, Cm, Dskip,
+                                                   z, y, D);
     return cudaGetLastError();
 }
 
