@@ -85,6 +85,18 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of the ranks' values (each rank times its own replica; the
+    job's time is the slowest rank's).  world == 1 returns the value as is."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -230,11 +242,7 @@ def bench_ours(args, rank, world, local):
     status = ssm.ssm_device_status(stream)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    t = torch.tensor([total_ms], device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     elems = w.elements * world
     value = elems * args.steps / (total_ms / 1e3)

@@ -41,25 +41,33 @@ step16_kernel(float* __restrict__ state, const T* __restrict__ u, const T* __res
               const float* __restrict__ dt_bias, const float* __restrict__ A,
               const T* __restrict__ Bm, const T* __restrict__ Cm,
               const float* __restrict__ Dskip, const T* __restrict__ z, T* __restrict__ y,
-              long long D) {
-    const long long b = blockIdx.y;
+              int D) {
+    const int b = blockIdx.y;
     const int tid = blockIdx.x * THREADS + threadIdx.x;   // < 4*D (checked on the host)
     const int part = tid & 3;                              // states 4*part .. 4*part + 3
     // Threads past the last channel stay (the shuffles below need the whole
     // warp) but work on channel 0 and store nothing.
     const bool valid = (tid >> 2) < D;
-    const long long d = valid ? (tid >> 2) : 0;
-    const long long ch = b * D + d;
-    const float ut = to_f32(u[ch]);
-    const float v = to_f32(delta[ch]) + (dt_bias ? dt_bias[d] : 0.0f);
-    const float4 a4 = *reinterpret_cast<const float4*>(A + d * NS + 4 * part);
-    float4* hp = reinterpret_cast<float4*>(state + ch * NS + 4 * part);
+    const int d = valid ? (tid >> 2) : 0;
+    // 32-bit offsets within one batch entry (4*D*16 < 2^31 is checked on the
+    // host); the batch offset is applied to the base pointers once.
+    const size_t row = (size_t)b * (size_t)D;
+    const T* ub = u + row;
+    const float ut = to_f32(ub[d]);
+    float4* hp = reinterpret_cast<float4*>(state + row * NS) + (d * 4 + part);
     const float4 h4 = *hp;
-    // softplus in the base-2 domain: dl = log2(1 + 2^(v log2 e)) = dt / ln 2
-    const float dl = v > 20.0f ? v * kLog2e : ptx::lg2(1.0f + ptx::ex2(v * kLog2e));
+    const float4 a4 = reinterpret_cast<const float4*>(A)[d * 4 + part];
+    // softplus in the base-2 domain, dl = log2(1 + 2^(v log2 e)) = dt / ln 2,
+    // computed by the first lane of the channel and shared with the others.
+    float dl = 0.0f;
+    if (part == 0) {
+        const float v = to_f32(delta[row + d]) + (dt_bias ? dt_bias[d] : 0.0f);
+        dl = v > 20.0f ? v * kLog2e : ptx::lg2(1.0f + ptx::ex2(v * kLog2e));
+    }
+    dl = __shfl_sync(0xffffffffu, dl, threadIdx.x & ~3);
     const float dt = dl * kLn2;
-    const T* Bt = Bm + b * NS + 4 * part;
-    const T* Ct = Cm + b * NS + 4 * part;
+    const T* Bt = Bm + (size_t)b * NS + 4 * part;
+    const T* Ct = Cm + (size_t)b * NS + 4 * part;
     const float a[4] = {a4.x, a4.y, a4.z, a4.w};
     const float h[4] = {h4.x, h4.y, h4.z, h4.w};
     float hn[4];
@@ -81,16 +89,16 @@ step16_kernel(float* __restrict__ state, const T* __restrict__ u, const T* __res
     if (valid && part == 0) {
         acc = fmaf(Dskip ? Dskip[d] : 0.0f, ut, acc);
         if (z) {
-            const float zt = to_f32(z[ch]);
+            const float zt = to_f32(z[row + d]);
             acc *= zt * ptx::rcp(1.0f + ptx::ex2(-zt * kLog2e));
         }
-        y[ch] = from_f32<T>(acc);
+        y[row + d] = from_f32<T>(acc);
     }
 }
 
-// Largest D the one-launch grid takes (4*D threads of one batch entry must
-// fit an int, and batch fits the grid's y extent).
-constexpr long long kMaxD = (1LL << 29);
+// Largest D the one-launch grid takes (64*D, the state entries of one batch
+// entry, must fit an int; batch must fit the grid's y extent).
+constexpr long long kMaxD = (1LL << 25);
 constexpr long long kMaxBatch = 65535;
 
 template <typename T>
@@ -100,7 +108,7 @@ static cudaError_t launch_step16(float* state, const T* u, const T* delta, const
                                  cudaStream_t stream) {
     const dim3 grid((unsigned)((4 * D + THREADS - 1) / THREADS), (unsigned)batch);
     step16_kernel<T><<<grid, THREADS, 0, stream>>>(state, u, delta, dt_bias, A, Bm, Cm, Dskip,
-                                                   z, y, D);
+                                                   z, y, (int)D);
     return cudaGetLastError();
 }
 
