@@ -102,14 +102,17 @@ def test_step_small_dt_and_pure_decay():
     parity.check(parity.to_f64(state), want.cpu().numpy(), 1e-5, "pure decay")
 
 
+@pytest.mark.parametrize("per_group", ["1", "2", "4"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_fast_step_matches_generic(monkeypatch, dtype):
-    """The N == 16 decode kernel (four threads per channel) and the generic
-    one-thread-per-channel kernel agree step by step; a ragged channel count
-    leaves a partly filled last warp."""
+def test_fast_step_matches_generic(monkeypatch, dtype, per_group):
+    """The N == 16 decode kernel (four threads per channel, one, two or four
+    channels per thread group) and the generic one-thread-per-channel kernel
+    agree step by step; a ragged channel count leaves a partly filled last
+    warp."""
     w = wl.StepWorkload("small", 3, 203, 16, 4, dtype, 11)
     inp = wl.make_step_inputs(w, device=DEV)
     monkeypatch.delenv("SSM_FORCE_GENERIC_STEP", raising=False)
+    monkeypatch.setenv("SSM_STEP_J", per_group)
     st_fast, y_fast = gpu_steps(inp, 4)
     monkeypatch.setenv("SSM_FORCE_GENERIC_STEP", "1")
     st_gen, y_gen = gpu_steps(inp, 4)
