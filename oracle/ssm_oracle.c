@@ -187,5 +187,89 @@ int oracle_step(double *state, const void *u, const void *delta,
     return 0;
 }
 
+/*
+ * Discretisation variants of the input term (the decay Abar = exp(dt A) is
+ * the same in all three):
+ *   disc 0, zero-order hold (ultralytics "SSMの仕組み"):
+ *       h_t = Abar h_{t-1} + (Abar - 1)/A B_t u_t
+ *   disc 1, Euler (ta-paperlens, the selective-state pseudocode of
+ *       "Mamba: 状態を「選択的」にする"; the method news.han.ihouse.idv.tw article
+ *       1304 attributes to Mamba-2, error O(dt^2) per step):
+ *       h_t = Abar h_{t-1} + dt B_t u_t
+ *   disc 2, trapezoidal (news.han.ihouse.idv.tw article 1304, "より正確な
+ *       離散化：台形法則": both ends of the step, error O(dt^3) per step; the
+ *       page's data-dependent convex weight is not specified, read here as
+ *       the plain trapezoid, weight 1/2):
+ *       h_t = Abar h_{t-1} + dt/2 (B_t u_t + Abar B_{t-1} u_{t-1}),
+ *       with B_{-1} u_{-1} = 0.
+ * The readout, skip and gate are those of oracle_scan_fwd.  q is N doubles of
+ * scratch holding B_{t-1} u_{t-1}.
+ */
+static void scan_channel_disc(const void *u, const void *delta, const float *dt_bias,
+                              const float *A, const void *B, const void *C,
+                              const float *Dskip, const void *z, double *y,
+                              double *h_last, int64_t b, int64_t d, int64_t L,
+                              int64_t D, int64_t N, int dtype, int disc, double *h,
+                              double *q)
+{
+    for (int64_t n = 0; n < N; n++) {
+        h[n] = 0.0;
+        q[n] = 0.0;
+    }
+    double bias = dt_bias ? (double)dt_bias[d] : 0.0;
+    double dsk = Dskip ? (double)Dskip[d] : 0.0;
+    for (int64_t t = 0; t < L; t++) {
+        int64_t i_btd = (b * L + t) * D + d;
+        double ut = load_elem(u, i_btd, dtype);
+        double dt = softplus(load_elem(delta, i_btd, dtype) + bias);
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; n++) {
+            double a = (double)A[d * N + n];
+            double abar = exp(dt * a);
+            double qt = load_elem(B, (b * L + t) * N + n, dtype) * ut;
+            double ct = load_elem(C, (b * L + t) * N + n, dtype);
+            if (disc == 0)
+                h[n] = abar * h[n] + ((a == 0.0) ? dt : expm1(dt * a) / a) * qt;
+            else if (disc == 1)
+                h[n] = abar * h[n] + dt * qt;
+            else
+                h[n] = abar * h[n] + 0.5 * dt * (qt + abar * q[n]);
+            q[n] = qt;
+            acc += ct * h[n];
+        }
+        acc += dsk * ut;
+        if (z)
+            acc *= silu(load_elem(z, i_btd, dtype));
+        y[i_btd] = acc;
+    }
+    if (h_last)
+        for (int64_t n = 0; n < N; n++)
+            h_last[(b * D + d) * N + n] = h[n];
+}
+
+/* oracle_scan_fwd with a discretisation variant (disc 0, 1 or 2, above). */
+int oracle_scan_fwd_disc(const void *u, const void *delta, const float *dt_bias,
+                         const float *A, const void *B, const void *C,
+                         const float *Dskip, const void *z, double *y,
+                         double *h_last, int64_t batch, int64_t L, int64_t D,
+                         int64_t N, int dtype, int disc, int64_t d_begin, int64_t d_end)
+{
+    if (!u || !delta || !A || !B || !C || !y)
+        return -1;
+    if (batch < 0 || L < 0 || D < 0 || N < 1 || (dtype != 0 && dtype != 1))
+        return -1;
+    if (disc < 0 || disc > 2 || d_begin < 0 || d_end > D || d_begin > d_end)
+        return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N * 2);
+    if (!h)
+        return -2;
+    for (int64_t b = 0; b < batch; b++)
+        for (int64_t d = d_begin; d < d_end; d++)
+            scan_channel_disc(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, b, d,
+                              L, D, N, dtype, disc, h, h + N);
+    free(h);
+    return 0;
+}
+
 /* ABI probe used by the Python wrapper to refuse a stale build. */
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }

@@ -439,3 +439,97 @@ ALL_PINS = [
     pin_bf16_decode,
     pin_step_matches_library_pipeline,
 ]
+
+
+# ------------------------------------------------- discretisation variants
+def _disc(lib, p, disc):
+    return oracle.scan_fwd_disc(p["u"], p["delta"], p["dt_bias"], p["A"], p["B"], p["C"],
+                                p["Dskip"], p["z"], disc, dtype=oracle.F32, lib=lib)
+
+
+def _constant_problem(L, a_vals, dt, b, u):
+    """batch 1, D 1, N = len(a_vals): dt, B, u constant in t; C = 1, no gate,
+    no skip; dt_bias 0 and delta = softplus^-1(dt) (float32)."""
+    N = len(a_vals)
+    delta = np.float32(np.log(np.expm1(dt)))
+    dt_used = float(softplus_ref(np.float64(delta)))
+    return dict(u=_f32(np.full((1, L, 1), u)), delta=_f32(np.full((1, L, 1), delta)),
+                dt_bias=None, A=_f32(np.array([a_vals])), B=_f32(np.full((1, L, N), b)),
+                C=_f32(np.ones((1, L, N))), Dskip=None, z=None), dt_used
+
+
+def pin_disc_zoh_is_the_scan(lib):
+    """Variant 0 is the zero-order hold of oracle_scan_fwd (same inputs, same
+    results up to the order of two float64 products)."""
+    rng = np.random.default_rng(40)
+    p = random_problem(rng, 2, 24, 5, 6)
+    y0, h0 = scan(lib, p)
+    y1, h1 = _disc(lib, p, oracle.ZOH)
+    _close(y1, y0, 1e-13, 1e-15, "disc 0 y")
+    _close(h1, h0, 1e-13, 1e-15, "disc 0 h")
+
+
+def pin_disc_euler_constant_input(lib):
+    """Euler with constant dt, B, u: h_t = dt B u sum_{k<=t} Abar^k
+    = dt B u (1 - Abar^(t+1)) / (1 - Abar)  (ta-paperlens pseudocode update)."""
+    a_vals, L = [-0.3, -1.1, -2.5], 40
+    p, dt = _constant_problem(L, a_vals, 0.07, 0.8, -1.3)
+    _, h = _disc(lib, p, oracle.EULER)
+    q = np.float64(np.float32(0.8)) * np.float64(np.float32(-1.3))
+    ab = np.exp(dt * np.float64(np.float32(a_vals)))
+    want = dt * q * (1 - ab ** L) / (1 - ab)
+    _close(h[0, 0], want, 1e-12, 1e-14, "Euler constant input")
+
+
+def pin_disc_trapezoid_constant_input(lib):
+    """Trapezoid with constant dt, B, u: h_0 = dt/2 q, then
+    h_t = Abar h_{t-1} + dt/2 q (1 + Abar), so
+    h_t = Abar^t h_0 + dt/2 q (1 + Abar) (1 - Abar^t) / (1 - Abar)."""
+    a_vals, L = [-0.4, -1.7], 33
+    p, dt = _constant_problem(L, a_vals, 0.11, -0.6, 0.9)
+    _, h = _disc(lib, p, oracle.TRAPEZOID)
+    q = np.float64(np.float32(-0.6)) * np.float64(np.float32(0.9))
+    ab = np.exp(dt * np.float64(np.float32(a_vals)))
+    t = L - 1
+    want = ab ** t * (dt / 2 * q) + dt / 2 * q * (1 + ab) * (1 - ab ** t) / (1 - ab)
+    _close(h[0, 0], want, 1e-12, 1e-14, "trapezoid constant input")
+
+
+def pin_disc_orders_against_ode(lib):
+    """The error against the continuous system h' = a h + x(s) (ta-paperlens,
+    "仕組み: 連続時間の線形システム"), sampled at t_k = k dt from h(-dt) = 0,
+    falls with the order the news.han.ihouse.idv.tw page states: O(dt^2) per
+    step for Euler (so O(dt) over a fixed span), O(dt^3) per step for the
+    trapezoid (O(dt^2) over the span); the zero-order hold of a smooth input
+    is first order as well.  Halving dt must divide the error by ~2, ~2, ~4.
+    The input is zero up to s = 0 and continuous there (x(0) = 0), which is
+    what the trapezoid's start, B_{-1} u_{-1} = 0, assumes."""
+    a = -0.7
+    x = lambda s: np.where(s > 0, np.sin(1.3 * s) + 0.5 * np.sin(2.1 * s), 0.0)  # noqa: E731
+    span = 3.0
+    errs = {oracle.ZOH: [], oracle.EULER: [], oracle.TRAPEZOID: []}
+    for target in (0.02, 0.01):
+        delta = np.float32(np.log(np.expm1(target)))
+        dt = float(softplus_ref(np.float64(delta)))
+        L = int(round(span / dt)) + 1
+        tk = np.arange(L) * dt
+        p = dict(u=_f32(x(tk).reshape(1, L, 1)), delta=_f32(np.full((1, L, 1), delta)),
+                 dt_bias=None, A=_f32([[a]]), B=_f32(np.ones((1, L, 1))),
+                 C=_f32(np.ones((1, L, 1))), Dskip=None, z=None)
+        # the float32 samples differ from x by < 1e-7, far below the
+        # discretisation errors measured here
+        af = float(np.float32(a))
+        sol = scipy.integrate.solve_ivp(lambda s, h: af * h + x(s), (-dt, tk[-1]), [0.0],
+                                        rtol=1e-12, atol=1e-14)
+        exact = sol.y[0, -1]
+        for disc in errs:
+            _, h = _disc(lib, p, disc)
+            errs[disc].append(abs(h[0, 0, 0] - exact))
+    for disc, lo, hi in ((oracle.ZOH, 1.7, 2.4), (oracle.EULER, 1.7, 2.4),
+                         (oracle.TRAPEZOID, 3.3, 4.8)):
+        ratio = errs[disc][0] / errs[disc][1]
+        assert lo < ratio < hi, f"disc {disc}: error ratio {ratio:.2f} ({errs[disc]})"
+
+
+DISC_PINS = [pin_disc_zoh_is_the_scan, pin_disc_euler_constant_input,
+             pin_disc_trapezoid_constant_input, pin_disc_orders_against_ode]
