@@ -216,12 +216,12 @@ static void scan_channel_disc(const void *u, const void *delta, const float *dt_
         h[n] = 0.0;
         q[n] = 0.0;
     }
-    double bias = dt_bias ? (double)dt_bias[d] : 0.0;
-    double dsk = Dskip ? (double)Dskip[d] : 0.0;
+    const double bias_d = dt_bias ? (double)dt_bias[d] : 0.0;
+    const double skip_d = Dskip ? (double)Dskip[d] : 0.0;
     for (int64_t t = 0; t < L; t++) {
         int64_t i_btd = (b * L + t) * D + d;
         double ut = load_elem(u, i_btd, dtype);
-        double dt = softplus(load_elem(delta, i_btd, dtype) + bias);
+        double dt = softplus(load_elem(delta, i_btd, dtype) + bias_d);
         double acc = 0.0;
         for (int64_t n = 0; n < N; n++) {
             double a = (double)A[d * N + n];
@@ -229,7 +229,7 @@ static void scan_channel_disc(const void *u, const void *delta, const float *dt_
             double qt = load_elem(B, (b * L + t) * N + n, dtype) * ut;
             double ct = load_elem(C, (b * L + t) * N + n, dtype);
             if (disc == 0)
-                h[n] = abar * h[n] + ((a == 0.0) ? dt : expm1(dt * a) / a) * qt;
+                h[n] = abar * h[n] + (a != 0.0 ? expm1(dt * a) / a : dt) * qt;
             else if (disc == 1)
                 h[n] = abar * h[n] + dt * qt;
             else
@@ -237,14 +237,16 @@ static void scan_channel_disc(const void *u, const void *delta, const float *dt_
             q[n] = qt;
             acc += ct * h[n];
         }
-        acc += dsk * ut;
+        double out = acc + skip_d * ut;
         if (z)
-            acc *= silu(load_elem(z, i_btd, dtype));
-        y[i_btd] = acc;
+            out *= silu(load_elem(z, i_btd, dtype));
+        y[i_btd] = out;
     }
-    if (h_last)
+    if (h_last) {
+        double *hl = h_last + (b * D + d) * N;
         for (int64_t n = 0; n < N; n++)
-            h_last[(b * D + d) * N + n] = h[n];
+            hl[n] = h[n];
+    }
 }
 
 /* oracle_scan_fwd with a discretisation variant (disc 0, 1 or 2, above). */
