@@ -61,13 +61,21 @@ extern "C" {
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
 
+/* Discretisation of the input term for ssm_scan_fwd_disc (the decay
+ * A_bar = exp(dt A) is the same in all three). */
+typedef enum {
+    SSM_DISC_ZOH = 0,       /* (A_bar - 1)/A B_t u_t: zero-order hold (ssm_scan_fwd) */
+    SSM_DISC_EULER = 1,     /* dt B_t u_t */
+    SSM_DISC_TRAPEZOID = 2  /* dt/2 (B_t u_t + A_bar B_{t-1} u_{t-1}), B_{-1} u_{-1} = 0 */
+} ssm_disc_t;
+
 typedef enum {
     SSM_OK = 0,
     SSM_ERR_NULL = -1,        /* a required pointer is NULL */
     SSM_ERR_SIZE = -2,        /* negative size, N < 1, or a size that overflows */
     SSM_ERR_DTYPE = -3,       /* dtype is not an ssm_dtype_t value */
     SSM_ERR_ALIGN = -4,       /* a pointer is not aligned to its element size */
-    SSM_ERR_UNSUPPORTED = -5, /* N > SSM_MAX_N */
+    SSM_ERR_UNSUPPORTED = -5, /* N > SSM_MAX_N, or an unknown discretisation */
     SSM_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
     SSM_ERR_NOMEM = -7,       /* the stream-ordered workspace could not be allocated */
     SSM_ERR_TIMEOUT = -8,     /* a device-side bounded wait gave up (see ssm_device_status) */
@@ -99,6 +107,28 @@ SSM_API int ssm_scan_fwd(const void *u, const void *delta, const float *dt_bias,
                  const float *Dskip, const void *z, void *y, float *h_last,
                  int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
                  void *stream);
+
+/*
+ * ssm_scan_fwd_disc -- ssm_scan_fwd with another discretisation of the input
+ * term (ssm_disc_t; SSM_DISC_ZOH gives ssm_scan_fwd itself):
+ *   SSM_DISC_EULER      h_t = A_bar h_{t-1} + dt B_t u_t, the update of the
+ *                       selective-state pseudocode on the ta-paperlens page
+ *                       ("Mamba: 状態を「選択的」にする");
+ *   SSM_DISC_TRAPEZOID  h_t = A_bar h_{t-1} + dt/2 (B_t u_t + A_bar B_{t-1}
+ *                       u_{t-1}), from h = 0 and B_{-1} u_{-1} = 0: the
+ *                       trapezoidal rule Mamba-3 uses (news.han.ihouse.idv.tw
+ *                       article 1304, "より正確な離散化：台形法則"; its
+ *                       data-dependent weight is taken as 1/2).
+ * Arguments, layouts, ownership and errors are those of ssm_scan_fwd; an
+ * unknown `disc` returns SSM_ERR_UNSUPPORTED.  h_last is the state only (a
+ * trapezoidal prefill does not carry B_{L-1} u_{L-1} into ssm_step, whose
+ * update is the zero-order hold).
+ */
+SSM_API int ssm_scan_fwd_disc(const void *u, const void *delta, const float *dt_bias,
+                              const float *A, const void *B, const void *C,
+                              const float *Dskip, const void *z, void *y, float *h_last,
+                              int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                              int disc, void *stream);
 
 /*
  * ssm_step -- one decode token: the same per-token update as one step of

@@ -20,8 +20,9 @@ SSM_F32, SSM_BF16 = 0, 1
 STATUS = {0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_SIZE", -3: "SSM_ERR_DTYPE",
           -4: "SSM_ERR_ALIGN", -5: "SSM_ERR_UNSUPPORTED", -6: "SSM_ERR_CUDA",
           -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT", -9: "SSM_ERR_SCRATCH"}
-EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_step", "ssm_device_status", "ssm_status_string",
-           "ssm_abi_version")
+EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_scan_fwd_noalloc", "ssm_step",
+           "ssm_device_status", "ssm_status_string", "ssm_abi_version")
+SSM_DISC_ZOH, SSM_DISC_EULER, SSM_DISC_TRAPEZOID = 0, 1, 2
 
 
 class SsmError(RuntimeError):
@@ -38,6 +39,8 @@ def _load() -> ctypes.CDLL:
     vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.ssm_scan_fwd.restype = ci
     lib.ssm_scan_fwd.argtypes = [vp] * 10 + [i64] * 4 + [ci, vp]
+    lib.ssm_scan_fwd_disc.restype = ci
+    lib.ssm_scan_fwd_disc.argtypes = [vp] * 10 + [i64] * 4 + [ci, ci, vp]
     lib.ssm_scan_fwd_noalloc.restype = ci
     lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [i64] * 4 + [ci, vp]
     lib.ssm_step.restype = ci
@@ -99,6 +102,16 @@ def ssm_scan_fwd(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, stream=None) -
     _check(lib.ssm_scan_fwd(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip),
                             _p(z), _p(y), _p(h_last), batch, L, D, N, _dtype_code(u),
                             _stream(stream)), "ssm_scan_fwd")
+
+
+def ssm_scan_fwd_disc(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, disc, stream=None) -> None:
+    """ssm_scan_fwd with the discretisation `disc` (SSM_DISC_ZOH, _EULER or
+    _TRAPEZOID) of the input term."""
+    batch, L, D = u.shape
+    N = A.shape[-1]
+    _check(lib.ssm_scan_fwd_disc(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip),
+                                 _p(z), _p(y), _p(h_last), batch, L, D, N, _dtype_code(u),
+                                 int(disc), _stream(stream)), "ssm_scan_fwd_disc")
 
 
 def ssm_scan_fwd_noalloc(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, stream=None) -> None:

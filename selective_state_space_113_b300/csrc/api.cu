@@ -52,14 +52,19 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA; 
 
 }  // namespace
 
-extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bias,
-                            const float* A, const void* B, const void* C,
-                            const float* Dskip, const void* z, void* y, float* h_last,
-                            int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
-                            void* stream_) {
+namespace {
+
+// The scan with a discretisation variant (ssm_disc_t); ssm_scan_fwd is
+// variant 0.
+int scan_impl(const void* u, const void* delta, const float* dt_bias, const float* A,
+              const void* B, const void* C, const float* Dskip, const void* z, void* y,
+              float* h_last, int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+              int disc, void* stream_) {
     if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (disc != SSM_DISC_ZOH && disc != SSM_DISC_EULER && disc != SSM_DISC_TRAPEZOID)
+        return SSM_ERR_UNSUPPORTED;
     int64_t bl, bld, bln, bd, bdn, dn;
     if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) ||
         !mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || !mul_ok(D, N, &dn) ||
@@ -81,16 +86,21 @@ extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bi
     const int plan = ssm::tile::forced_plan();
     if (N == ssm::tile::NS && plan != ssm::tile::kPlanGeneric &&
         all_aligned16({u, delta, z, B, C, y, h_last, A}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
-        if (dtype == SSM_F32)
-            return ssm::tile::launch_scan_tile<float>(
-                static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
-                static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
-                static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D, plan,
-                stream);
-        return ssm::tile::launch_scan_tile<bf16>(
-            static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
-            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
-            static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, plan, stream);
+        using namespace ssm::tile;
+#define SSM_TILE_CALL(TT, DISC)                                                              \
+    launch_scan_tile<TT, DISC>(static_cast<const TT*>(u), static_cast<const TT*>(delta), dt_bias, \
+                               A, static_cast<const TT*>(B), static_cast<const TT*>(C), Dskip,   \
+                               static_cast<const TT*>(z), static_cast<TT*>(y), h_last, batch, L, \
+                               D, plan, stream)
+        if (dtype == SSM_F32) {
+            if (disc == SSM_DISC_EULER) return SSM_TILE_CALL(float, kEuler);
+            if (disc == SSM_DISC_TRAPEZOID) return SSM_TILE_CALL(float, kTrap);
+            return SSM_TILE_CALL(float, kZOH);
+        }
+        if (disc == SSM_DISC_EULER) return SSM_TILE_CALL(bf16, kEuler);
+        if (disc == SSM_DISC_TRAPEZOID) return SSM_TILE_CALL(bf16, kTrap);
+        return SSM_TILE_CALL(bf16, kZOH);
+#undef SSM_TILE_CALL
     }
     cudaError_t e;
     if (dtype == SSM_F32)
@@ -98,14 +108,34 @@ extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bi
             static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
             static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
             static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D, (int)N,
-            stream);
+            stream, disc);
     else
         e = ssm::launch_scan_generic<bf16>(
             static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
             static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
             static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, (int)N,
-            stream);
+            stream, disc);
     return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bias,
+                            const float* A, const void* B, const void* C,
+                            const float* Dskip, const void* z, void* y, float* h_last,
+                            int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                            void* stream_) {
+    return scan_impl(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
+                     SSM_DISC_ZOH, stream_);
+}
+
+extern "C" int ssm_scan_fwd_disc(const void* u, const void* delta, const float* dt_bias,
+                                 const float* A, const void* B, const void* C,
+                                 const float* Dskip, const void* z, void* y, float* h_last,
+                                 int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                                 int disc, void* stream_) {
+    return scan_impl(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
+                     disc, stream_);
 }
 
 extern "C" int ssm_step(float* state, const void* u, const void* delta, const float* dt_bias,
@@ -246,7 +276,7 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
     long long workers = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        prepare<T, (int)kChained>(sms, &workers) != cudaSuccess || workers < 1)
+        prepare<T, (int)kChained, (int)kZOH>(sms, &workers) != cudaSuccess || workers < 1)
         return SSM_ERR_CUDA;
     CUtensorMap maps[6];
     Params p;
@@ -261,7 +291,7 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
     p.abort = reinterpret_cast<unsigned*>(ws + 32);
     p.flags = reinterpret_cast<unsigned*>(ws + 256);
     p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + head);
-    return launch_mode<T, (int)kChained>(p.G, maps, p, stream) == cudaSuccess ? SSM_OK
+    return launch_mode<T, (int)kChained, (int)kZOH>(p.G, maps, p, stream) == cudaSuccess ? SSM_OK
                                                                              : SSM_ERR_CUDA;
 }
 

@@ -6,7 +6,10 @@
 // "SSMの仕組み": A_bar = exp(dt A), B_bar = (A_bar - 1)/A * B with expm1 for
 // accuracy; ta-paperlens page, Mamba pseudocode: dt = softplus(delta + bias),
 // h = A_bar h + B_bar u, y = C h; D skip from the output equation y = C h + D x;
-// SiLU(z) gate from the Mamba block diagram).
+// SiLU(z) gate from the Mamba block diagram).  `disc` selects the input term:
+// 0 zero-order hold as above, 1 Euler dt B_t u_t (the ta-paperlens
+// pseudocode), 2 trapezoid dt/2 (B_t u_t + A_bar B_{t-1} u_{t-1}) (the
+// news.han.ihouse.idv.tw Mamba-3 article, weight 1/2).
 #pragma once
 
 #include "common.cuh"
@@ -20,16 +23,18 @@ scan_generic_kernel(const T* __restrict__ u, const T* __restrict__ delta,
                     const T* __restrict__ Bm, const T* __restrict__ Cm,
                     const float* __restrict__ Dskip, const T* __restrict__ z,
                     T* __restrict__ y, float* __restrict__ h_last,
-                    int64_t batch, int64_t L, int64_t D, int N) {
+                    int64_t batch, int64_t L, int64_t D, int N, int disc) {
     const int64_t ch = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (ch >= batch * D) return;
     const int64_t b = ch / D, d = ch - b * D;
 
     float h[NMAX];
     float a[NMAX];
+    float q[NMAX];   // B_{t-1} u_{t-1} (trapezoid)
 #pragma unroll
     for (int n = 0; n < NMAX; ++n) {
         h[n] = 0.0f;
+        q[n] = 0.0f;
         a[n] = (n < N) ? A[d * N + n] : 0.0f;
     }
     const float bias = dt_bias ? dt_bias[d] : 0.0f;
@@ -47,8 +52,16 @@ scan_generic_kernel(const T* __restrict__ u, const T* __restrict__ delta,
             if (n < N) {
                 const float x = dt * a[n];
                 const float abar = expf(x);
-                const float bcoef = (a[n] != 0.0f) ? expm1f(x) / a[n] : dt;
-                h[n] = fmaf(abar, h[n], bcoef * to_f32(Bt[n]) * ut);
+                const float qt = to_f32(Bt[n]) * ut;
+                if (disc == 0) {
+                    const float bcoef = (a[n] != 0.0f) ? expm1f(x) / a[n] : dt;
+                    h[n] = fmaf(abar, h[n], bcoef * qt);
+                } else if (disc == 1) {
+                    h[n] = fmaf(abar, h[n], dt * qt);
+                } else {
+                    h[n] = fmaf(abar, fmaf(0.5f * dt, q[n], h[n]), 0.5f * dt * qt);
+                }
+                q[n] = qt;
                 acc = fmaf(to_f32(Ct[n]), h[n], acc);
             }
         }
@@ -68,12 +81,12 @@ static cudaError_t launch_scan_generic_n(const T* u, const T* delta, const float
                                          const float* A, const T* Bm, const T* Cm,
                                          const float* Dskip, const T* z, T* y, float* h_last,
                                          int64_t batch, int64_t L, int64_t D, int N,
-                                         cudaStream_t stream) {
+                                         int disc, cudaStream_t stream) {
     const int64_t channels = batch * D;
     const int threads = 128;
     const int64_t blocks = (channels + threads - 1) / threads;
     scan_generic_kernel<T, NMAX><<<(unsigned)blocks, threads, 0, stream>>>(
-        u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D, N);
+        u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D, N, disc);
     return cudaGetLastError();
 }
 
@@ -82,18 +95,18 @@ static cudaError_t launch_scan_generic(const T* u, const T* delta, const float* 
                                        const float* A, const T* Bm, const T* Cm,
                                        const float* Dskip, const T* z, T* y, float* h_last,
                                        int64_t batch, int64_t L, int64_t D, int N,
-                                       cudaStream_t stream) {
+                                       cudaStream_t stream, int disc = 0) {
     if (N <= 16)
         return launch_scan_generic_n<T, 16>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
-                                            batch, L, D, N, stream);
+                                            batch, L, D, N, disc, stream);
     if (N <= 32)
         return launch_scan_generic_n<T, 32>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
-                                            batch, L, D, N, stream);
+                                            batch, L, D, N, disc, stream);
     if (N <= 64)
         return launch_scan_generic_n<T, 64>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
-                                            batch, L, D, N, stream);
+                                            batch, L, D, N, disc, stream);
     return launch_scan_generic_n<T, 256>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last,
-                                         batch, L, D, N, stream);
+                                         batch, L, D, N, disc, stream);
 }
 
 }  // namespace ssm

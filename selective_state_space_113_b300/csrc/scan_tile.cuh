@@ -51,6 +51,16 @@
 // B_n/(n+1) is prepared once per stage by the helpers, and u/a0 once per
 // step, so B_n u / A[d,n] is one multiply-add away.  Any other A runs a
 // per-state path that uses exp(dt A) - 1 directly and the dt*B limit at A = 0.
+//
+// Discretisation variants of the input term (template parameter DISC; the
+// decay A_bar = exp(dt A) is common):
+//   kZOH    (A_bar - 1)/A B_t u_t                       (above)
+//   kEuler  dt B_t u_t  (ta-paperlens pseudocode):   h <- e (h) + (h + dt u B)
+//   kTrap   dt/2 (B_t u_t + A_bar B_{t-1} u_{t-1})  (news.han.ihouse.idv.tw,
+//           Mamba-3 "台形法則", weight 1/2):  s = h + dt/2 P_{t-1},
+//           h <- A_bar s + dt/2 P_t with P_t = B_t u_t kept per state; a
+//           piece's first step takes P from the step before it (header).
+// For kEuler and kTrap the helpers widen B without the 1/(n+1) scale.
 #pragma once
 
 #include <cuda.h>
@@ -77,6 +87,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 enum Mode : int { kChained = 0, kAggregate = 1, kFromState = 2 };
 
+enum Disc : int { kZOH = 0, kEuler = 1, kTrap = 2 };
+
 // Stage flags: first / last stage of a piece, end of work, carried state
 // present in the stage header, piece ends at the end of its chain.
 enum MetaFlags : int { kFirst = 1, kLast = 2, kEnd = 4, kHasState = 8, kChainEnd = 16 };
@@ -99,6 +111,8 @@ struct ChanPar {
 struct Params {
     void* y;
     float* h_last;
+    const void* u;          // raw u and B, read for the trapezoid's step before a piece
+    const void* Bm;
     const float* dt_bias;
     const float* A;
     const float* Dskip;
@@ -132,6 +146,8 @@ struct Cfg {
     static constexpr int kConv = TC * NS * 4;        // widened B/(n+1) or C rows
     static constexpr int kPar = CB * (int)sizeof(ChanPar);
     static constexpr int kState = CB * NS * 4;       // carried state of the tile
+    // Trapezoid: u and the B row of the step before the piece (1 KiB slot).
+    static constexpr int kPrev = 1024;
     static constexpr int offU = 0;
     static constexpr int offD = offU + kTile;
     static constexpr int offZ = offD + kTile;
@@ -141,7 +157,8 @@ struct Cfg {
     static constexpr int offCc = offBc + kConv;
     static constexpr int offPar = offCc + kConv;
     static constexpr int offState = offPar + kPar;
-    static constexpr int kStage = offState + kState;
+    static constexpr int offPrev = offState + kState;
+    static constexpr int kStage = offPrev + kPrev;
     // Prologue ring of one helper/consumer pair: 2 buffers x KP steps x
     // 32 lanes x float4.
     static constexpr int kProBuf = KP * CW * 16;
@@ -187,14 +204,16 @@ __device__ __forceinline__ void raise_failure(const Params& p) {
 }
 
 // Widening of rows [row0, row0 + kRowsPerHelper) of a stage's B and C to
-// float32, B scaled by 1/(n+1).  Lane l handles element pairs l, l+32, ...
-// of that row range; every pair a lane handles has n = 2*(l % 8) + {0, 1}.
-template <typename T, int MODE>
+// float32, B scaled by 1/(n+1) for the zero-order hold (unscaled for the
+// other variants).  Lane l handles element pairs l, l+32, ... of that row
+// range; every pair a lane handles has n = 2*(l % 8) + {0, 1}.
+template <typename T, int MODE, int DISC>
 __device__ __forceinline__ void widen_rows(unsigned char* st, int row0, int lane) {
     using C = Cfg<T>;
     constexpr int kPairs = C::kRowsPerHelper * NS / 2;
     const int n0 = 2 * (lane % (NS / 2));
-    const float s0 = 1.0f / (float)(n0 + 1), s1 = 1.0f / (float)(n0 + 2);
+    const float s0 = DISC == kZOH ? 1.0f / (float)(n0 + 1) : 1.0f;
+    const float s1 = DISC == kZOH ? 1.0f / (float)(n0 + 2) : 1.0f;
     const T* Br = reinterpret_cast<const T*>(st + C::offBr) + row0 * NS;
     const T* Cr = reinterpret_cast<const T*>(st + C::offCr) + row0 * NS;
     float2* Bc = reinterpret_cast<float2*>(st + C::offBc) + row0 * (NS / 2);
@@ -218,12 +237,25 @@ __device__ __forceinline__ void widen_rows(unsigned char* st, int row0, int lane
 // header of its first stage; returns the geometric-A bit mask of the four
 // 32-channel sub-blocks.  All 32 lanes take part; lane l handles channels
 // l, l+32, l+64, l+96 of the tile.
-template <typename T, int MODE>
+template <typename T, int MODE, int DISC>
 __device__ int fill_header(unsigned char* st, const Params& p, long long b, long long d0,
-                           long long k, bool* has_state, bool* ok_out, int lane) {
+                           long long k, long long t0, bool* has_state, bool* ok_out, int lane) {
     using C = Cfg<T>;
     ChanPar* par = reinterpret_cast<ChanPar*>(st + C::offPar);
     int geo = 0;
+    if (DISC == kTrap) {
+        // u and the B row of the step before the piece (zero before step 0):
+        // the trapezoid's first step needs B_{t0-1} u_{t0-1}.
+        float* prev = reinterpret_cast<float*>(st + C::offPrev);
+        const T* ur = static_cast<const T*>(p.u) + (b * p.L + (t0 > 0 ? t0 - 1 : 0)) * p.D;
+        const T* br = static_cast<const T*>(p.Bm) + (b * p.L + (t0 > 0 ? t0 - 1 : 0)) * NS;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const long long d = d0 + CW * w + lane;
+            prev[CW * w + lane] = (t0 > 0 && d < p.D) ? to_f32(ur[d]) : 0.0f;
+        }
+        if (lane < NS) prev[CB + lane] = t0 > 0 ? to_f32(br[lane]) : 0.0f;
+    }
 #pragma unroll
     for (int w = 0; w < NCW; ++w) {
         const long long d = d0 + CW * w + lane;
@@ -300,11 +332,14 @@ __device__ int fill_header(unsigned char* st, const Params& p, long long b, long
 }
 
 // ------------------------------------------------------------------ helpers
-// Per-step values of KP consecutive steps of the helper's 32 channels:
-// geometric A   {r = exp(dt a0), up = u / a0, g, sug}  (kAggregate: g = dl)
-// other A       {dl, u, g, sug}                          (kAggregate: g = dl)
-// with g = z sigmoid(z) (1 without z) and sug = Dskip u g.
-template <typename T, int MODE, bool HASZ>
+// Per-step values of KP consecutive steps of the helper's 32 channels, with
+// g = z sigmoid(z) (1 without z), sug = Dskip u g, dt = dl ln 2:
+//                       geometric A                  other A
+//   kZOH              {r = exp(dt a0), u/a0, g, sug}  {dl, u, g, sug}
+//   kEuler            {r, dt u, g, sug}               {dl, u, g, sug}
+//   kTrap             {r, dt/2, u, g}                 {dl, u, g, sug}
+//   kAggregate mode   the same .x/.y (kTrap: .x/.y/.z), .w = dl
+template <typename T, int MODE, int DISC, bool HASZ>
 __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0, int col,
                                                const ChanPar& cp, bool geo, float4* out) {
     using C = Cfg<T>;
@@ -323,19 +358,28 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
         const float dv = ld_elem(Dl + t * CB + col);
         const float v2 = fmaf(dv, kLog2e, cp.kb2);           // (delta + bias) log2(e)
         const float dl = ptx::lg2(1.0f + ptx::ex2(v2));      // softplus / ln 2
-        o[j].x = geo ? ptx::ex2(dl * cp.a0) : dl;
-        o[j].y = geo ? u * cp.ia0 : u;
-        if (MODE == kAggregate) {
-            o[j].z = dl;
-            o[j].w = 0.0f;
-        } else {
-            float g = 1.0f;
+        float g = 1.0f;
+        if (MODE != kAggregate) {
             if constexpr (HASZ) {
                 const float z = ld_elem(Z + t * CB + col);
                 g = z * ptx::rcp(1.0f + ptx::ex2(z * -kLog2e));
             }
-            o[j].z = g;
-            o[j].w = cp.dsk * u * g;
+        }
+        const float sug = cp.dsk * u * g;
+        if (geo) {
+            o[j].x = ptx::ex2(dl * cp.a0);
+            if (DISC == kZOH) o[j].y = u * cp.ia0;
+            else if (DISC == kEuler) o[j].y = dl * kLn2 * u;
+            else o[j].y = dl * (0.5f * kLn2);
+            if (DISC == kTrap) {
+                o[j].z = u;
+                o[j].w = MODE == kAggregate ? dl : g;
+            } else {
+                o[j].z = MODE == kAggregate ? 0.0f : g;
+                o[j].w = MODE == kAggregate ? dl : sug;
+            }
+        } else {
+            o[j] = make_float4(dl, u, MODE == kAggregate ? 0.0f : g, MODE == kAggregate ? dl : sug);
         }
     }
 #pragma unroll
@@ -346,11 +390,13 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
 // Recurrence and readout of cnt (<= KP) steps, geometric A.  FULL: cnt ==
 // KP, a straight-line body the compiler can schedule across steps.  The y
 // values are kept in registers and stored after the last step, so that no
-// shared-memory store sits between one step's loads and the next's.
-template <typename T, int MODE, bool FULL>
+// shared-memory store sits between one step's loads and the next's.  P holds
+// B_{t-1} u_{t-1} per state (kTrap only); dsk = Dskip[d] (kTrap only).
+template <typename T, int MODE, int DISC, bool FULL>
 __device__ __forceinline__ void steps_geo(const unsigned char* st, int row0, int cnt,
-                                          const float4* pro, float2 (&H)[NS / 2], float& S2,
-                                          T* ytile, int lane) {
+                                          const float4* pro, float2 (&H)[NS / 2],
+                                          float2 (&P)[NS / 2], float dsk, float& S2, T* ytile,
+                                          int lane) {
     using C = Cfg<T>;
     const float* Bc = reinterpret_cast<const float*>(st + C::offBc);
     const float* Cc = reinterpret_cast<const float*>(st + C::offCc);
@@ -368,27 +414,51 @@ __device__ __forceinline__ void steps_geo(const unsigned char* st, int row0, int
         const float e1 = fmaf(r, e0, e0);           // exp(dt A_1) - 1
         const float r2 = e1 + 1.0f;
         const float2 R2 = make_float2(r2, r2), E1 = make_float2(e1, e1);
+        // kZOH: u/a0; kEuler: dt u; kTrap: dt/2
         const float2 UP = make_float2(pv.y, pv.y);
+        const float2 U2 = make_float2(pv.z, pv.z);  // kTrap: u
         float2 E = make_float2(e0, e1);
         float2 Y0 = make_float2(0.f, 0.f), Y1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < NS / 4; ++q) {
             const float4 b4 = B4[q];
             const int k0 = 2 * q, k1 = 2 * q + 1;
+            const float2 Ba = make_float2(b4.x, b4.y), Bb = make_float2(b4.z, b4.w);
             if (k0 > 0) E = ffma2(R2, E, E1);      // (e_{n+2}, e_{n+3}) = r^2 (e_n, e_{n+1}) + e_1
-            const float2 Sa = ffma2(make_float2(b4.x, b4.y), UP, H[k0]);
-            H[k0] = ffma2(E, Sa, H[k0]);
+            if (DISC == kZOH) {
+                H[k0] = ffma2(E, ffma2(Ba, UP, H[k0]), H[k0]);   // h + e (h + B u / A)
+            } else if (DISC == kEuler) {
+                H[k0] = ffma2(E, H[k0], ffma2(Ba, UP, H[k0]));   // h + e h + dt u B
+            } else {
+                const float2 Pn = __fmul2_rn(Ba, U2);            // B_t u_t
+                const float2 Sv = ffma2(UP, P[k0], H[k0]);       // h + dt/2 P_{t-1}
+                H[k0] = ffma2(UP, Pn, ffma2(E, Sv, Sv));         // A_bar s + dt/2 P_t
+                P[k0] = Pn;
+            }
             E = ffma2(R2, E, E1);
-            const float2 Sb = ffma2(make_float2(b4.z, b4.w), UP, H[k1]);
-            H[k1] = ffma2(E, Sb, H[k1]);
+            if (DISC == kZOH) {
+                H[k1] = ffma2(E, ffma2(Bb, UP, H[k1]), H[k1]);
+            } else if (DISC == kEuler) {
+                H[k1] = ffma2(E, H[k1], ffma2(Bb, UP, H[k1]));
+            } else {
+                const float2 Pn = __fmul2_rn(Bb, U2);
+                const float2 Sv = ffma2(UP, P[k1], H[k1]);
+                H[k1] = ffma2(UP, Pn, ffma2(E, Sv, Sv));
+                P[k1] = Pn;
+            }
             if (MODE != kAggregate) {
                 const float4 c4 = C4[q];
                 Y0 = ffma2(make_float2(c4.x, c4.y), H[k0], Y0);
                 Y1 = ffma2(make_float2(c4.z, c4.w), H[k1], Y1);
             }
         }
-        if (MODE == kAggregate) S2 += pv.z;
-        else yv[j] = fmaf((Y0.x + Y0.y) + (Y1.x + Y1.y), pv.z, pv.w);
+        if (MODE == kAggregate) {
+            S2 += pv.w;
+        } else {
+            const float sum = (Y0.x + Y0.y) + (Y1.x + Y1.y);
+            if (DISC == kTrap) yv[j] = fmaf(dsk, pv.z, sum) * pv.w;   // (sum + D u) g
+            else yv[j] = fmaf(sum, pv.z, pv.w);                       // sum g + D u g
+        }
     }
     if (MODE != kAggregate) {
 #pragma unroll
@@ -399,13 +469,14 @@ __device__ __forceinline__ void steps_geo(const unsigned char* st, int row0, int
     }
 }
 
-// Any other A (including zeros): per state, A_bar - 1 = 2^(dl A) - 1 and
-// B_bar/B = (A_bar - 1)/A, or dt where A == 0.  Correct, not tuned.
-template <typename T, int MODE>
+// Any other A (including zeros): per state, A_bar - 1 = 2^(dl A) - 1 and,
+// for the zero-order hold, B_bar/B = (A_bar - 1)/A, or dt where A == 0.
+// Correct, not tuned.
+template <typename T, int MODE, int DISC>
 __device__ __forceinline__ void steps_general(const unsigned char* st, int row0, int cnt,
                                               const float4* pro, const float* __restrict__ Arow,
-                                              float2 (&H)[NS / 2], float& S2, T* ytile,
-                                              int lane) {
+                                              float2 (&H)[NS / 2], float2 (&P)[NS / 2],
+                                              float& S2, T* ytile, int lane) {
     using C = Cfg<T>;
     const float* Bc = reinterpret_cast<const float*>(st + C::offBc);
     const float* Cc = reinterpret_cast<const float*>(st + C::offCc);
@@ -418,16 +489,26 @@ __device__ __forceinline__ void steps_general(const unsigned char* st, int row0,
         const float4 pv = pro[j * CW];
         const float dl = pv.x, u = pv.y;
         const float dt = dl * kLn2;
-        if (MODE == kAggregate) S2 += pv.z;
+        if (MODE == kAggregate) S2 += pv.w;
         float y = 0.0f;
 #pragma unroll
         for (int n = 0; n < NS; ++n) {
             const float a = __ldg(Arow + n);
             const float e = ptx::ex2(dl * a) - 1.0f;
-            const float coef = (a != 0.0f) ? e / a : dt;
-            const float bn = Bc[t * NS + n] * (float)(n + 1);
             float hn = (n & 1) ? H[n / 2].y : H[n / 2].x;
-            hn = fmaf(coef * bn, u, fmaf(e, hn, hn));
+            if (DISC == kZOH) {
+                const float coef = (a != 0.0f) ? e / a : dt;
+                const float bn = Bc[t * NS + n] * (float)(n + 1);
+                hn = fmaf(coef * bn, u, fmaf(e, hn, hn));
+            } else if (DISC == kEuler) {
+                hn = fmaf(dt * Bc[t * NS + n], u, fmaf(e, hn, hn));
+            } else {
+                const float pn = Bc[t * NS + n] * u;
+                float& po = (n & 1) ? P[n / 2].y : P[n / 2].x;
+                const float sv = fmaf(0.5f * dt, po, hn);
+                hn = fmaf(0.5f * dt, pn, fmaf(e, sv, sv));
+                po = pn;
+            }
             if (n & 1) H[n / 2].y = hn; else H[n / 2].x = hn;
             if (MODE != kAggregate) y = fmaf(Cc[t * NS + n], hn, y);
         }
@@ -442,7 +523,7 @@ __device__ __forceinline__ void steps_general(const unsigned char* st, int row0,
     }
 }
 
-template <typename T, int MODE>
+template <typename T, int MODE, int DISC>
 __global__ void __launch_bounds__(THREADS, 1)
 scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmD,
                  const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmB,
@@ -551,7 +632,8 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                 cur_b = cur_chain / p.nCB;
                 cur_d0 = (cur_chain % p.nCB) * CB;
                 bool has_state = false, ok = true;
-                geo = fill_header<T, MODE>(st, p, cur_b, cur_d0, cur_k, &has_state, &ok, lane);
+                geo = fill_header<T, MODE, DISC>(st, p, cur_b, cur_d0, cur_k, cur_t0, &has_state,
+                                                 &ok, lane);
                 if (!ok) {
                     if (lane == 0) raise_failure(p);
                     failed = true;
@@ -615,7 +697,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             }
             const Meta m = meta[slot];
             unsigned char* st = smem + slot * C::kStage;
-            if (!(m.flags & kEnd)) widen_rows<T, MODE>(st, hi * C::kRowsPerHelper, lane);
+            if (!(m.flags & kEnd)) widen_rows<T, MODE, DISC>(st, hi * C::kRowsPerHelper, lane);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&convd[slot]);
             if (m.flags & kEnd) break;
@@ -632,9 +714,10 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                 }
                 float4* out = pro + buf * (C::kProBuf / 16) + lane;
                 if (p.has_z)
-                    prologue_chunk<T, MODE, true>(st, c * KP, CW * hi + lane, cp, geo, out);
+                    prologue_chunk<T, MODE, DISC, true>(st, c * KP, CW * hi + lane, cp, geo, out);
                 else
-                    prologue_chunk<T, MODE, false>(st, c * KP, CW * hi + lane, cp, geo, out);
+                    prologue_chunk<T, MODE, DISC, false>(st, c * KP, CW * hi + lane, cp, geo,
+                                                         out);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&pfull[2 * hi + buf]);
             }
@@ -650,12 +733,17 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
     long long k = 0, chain = 0, b = 0, d0 = 0, d = 0;
     bool valid = false, geo = true, block_live = false;
     float2 H[NS / 2];
+    float2 P[NS / 2];   // B_{t-1} u_{t-1} per state (trapezoid)
+    float dsk = 0.0f;
     const float* Arow = p.A;
     float S2 = 0.0f;
     long long q = 0;
     bool failed = false;
 #pragma unroll
-    for (int i = 0; i < NS / 2; ++i) H[i] = make_float2(0.f, 0.f);
+    for (int i = 0; i < NS / 2; ++i) {
+        H[i] = make_float2(0.f, 0.f);
+        P[i] = make_float2(0.f, 0.f);
+    }
     for (long long j = 0; !failed; ++j) {
         const int slot = (int)(j % S);
         if (!bwait(&convd[slot], (uint32_t)((j / S) & 1), p)) {
@@ -674,6 +762,14 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             valid = d < p.D;
             block_live = d0 < p.D;
             geo = (m.geo >> w) & 1;
+            dsk = reinterpret_cast<const ChanPar*>(st + C::offPar)[CW * w + lane].dsk;
+            if (DISC == kTrap) {
+                const float* prev = reinterpret_cast<const float*>(st + C::offPrev);
+                const float up = prev[CW * w + lane];
+#pragma unroll
+                for (int i = 0; i < NS / 2; ++i)
+                    P[i] = make_float2(prev[CB + 2 * i] * up, prev[CB + 2 * i + 1] * up);
+            }
             S2 = 0.0f;
             if (m.flags & kHasState) {
                 const float4* s4 = reinterpret_cast<const float4*>(st + C::offState) + (CW * w + lane) * (NS / 4);
@@ -706,10 +802,13 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             const int cnt = m.nvalid - c * KP < KP ? m.nvalid - c * KP : KP;
             const float4* pv = pro + buf * (C::kProBuf / 16) + lane;
             if (geo) {
-                if (cnt == KP) steps_geo<T, MODE, true>(st, c * KP, KP, pv, H, S2, ytile, lane);
-                else steps_geo<T, MODE, false>(st, c * KP, cnt, pv, H, S2, ytile, lane);
+                if (cnt == KP)
+                    steps_geo<T, MODE, DISC, true>(st, c * KP, KP, pv, H, P, dsk, S2, ytile, lane);
+                else
+                    steps_geo<T, MODE, DISC, false>(st, c * KP, cnt, pv, H, P, dsk, S2, ytile,
+                                                    lane);
             } else {
-                steps_general<T, MODE>(st, c * KP, cnt, pv, Arow, H, S2, ytile, lane);
+                steps_general<T, MODE, DISC>(st, c * KP, cnt, pv, Arow, H, P, S2, ytile, lane);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&pempty[2 * w + buf]);
