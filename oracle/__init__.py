@@ -48,6 +48,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_scan_fwd_disc.restype = ctypes.c_int
     lib.oracle_scan_fwd_disc.argtypes = [vp] * 10 + [i64] * 4 + [ctypes.c_int, ctypes.c_int,
                                                                  i64, i64]
+    lib.oracle_conv_scan_fwd.restype = ctypes.c_int
+    lib.oracle_conv_scan_fwd.argtypes = ([vp] * 3 + [ctypes.c_int] + [vp] * 9 + [i64] * 4
+                                         + [ctypes.c_int, i64, i64])
     lib.oracle_abi_version.restype = ctypes.c_int
     return lib
 
@@ -67,7 +70,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                     or os.path.getmtime(LIB) < os.path.getmtime(SRC)):
                 build()
             lib = _bind(ctypes.CDLL(LIB))
-            if lib.oracle_abi_version() != 2:
+            if lib.oracle_abi_version() != 3:
                 raise RuntimeError("stale oracle build: " + LIB)
             _lib = lib
         return _lib
@@ -167,6 +170,41 @@ def scan_fwd_disc(u, delta, dt_bias, A, B, C, Dskip, z, disc: int, dtype: int = 
                                       _ptr(y), _ptr(h), batch, L, D, N, dtype, int(disc), lo, hi)
         if rc != 0:
             raise RuntimeError(f"oracle_scan_fwd_disc returned {rc}")
+
+    if threads == 1:
+        run(0, D)
+    else:
+        bounds = np.linspace(0, D, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])),
+                        range(threads)))
+    return y, h
+
+
+def conv_scan_fwd(x, conv_w, conv_b, act, delta, dt_bias, A, B, C, Dskip, z,
+                  dtype: int = F32, threads: int = 1, lib: ctypes.CDLL | None = None):
+    """Causal depthwise width-4 convolution of x (conv_w [D,4] float32, conv_b
+    [D] or None; act 1 applies SiLU) feeding the zero-order-hold scan, float64.
+    Returns ``(y, h_last)`` as ``scan_fwd``."""
+    lib = lib or load()
+    x, delta, z = (_as_input(v, dtype) for v in (x, delta, z))
+    B, C = _as_input(B, dtype), _as_input(C, dtype)
+    A, dt_bias, Dskip = _as_f32(A), _as_f32(dt_bias), _as_f32(Dskip)
+    conv_w, conv_b = _as_f32(conv_w), _as_f32(conv_b)
+    batch, L, D = x.shape
+    N = A.shape[1]
+    if A.shape != (D, N) or B.shape != (batch, L, N) or conv_w.shape != (D, 4):
+        raise ValueError("inconsistent shapes")
+    y = np.zeros((batch, L, D), np.float64)
+    h = np.zeros((batch, D, N), np.float64)
+    threads = max(1, min(int(threads), D)) if D else 1
+
+    def run(lo, hi):
+        rc = lib.oracle_conv_scan_fwd(_ptr(x), _ptr(conv_w), _ptr(conv_b), int(act), _ptr(delta),
+                                      _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
+                                      _ptr(z), _ptr(y), _ptr(h), batch, L, D, N, dtype, lo, hi)
+        if rc != 0:
+            raise RuntimeError(f"oracle_conv_scan_fwd returned {rc}")
 
     if threads == 1:
         run(0, D)

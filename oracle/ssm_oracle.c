@@ -273,5 +273,82 @@ int oracle_scan_fwd_disc(const void *u, const void *delta, const float *dt_bias,
     return 0;
 }
 
+/*
+ * The short causal convolution before the SSM (ta-paperlens, "現場ではこう
+ * 使う": d_conv, a short 1-D convolution in front of the SSM; agenticai-flow,
+ * d_conv=4 with the causal-conv1d package), read as depthwise (one filter per
+ * channel), width 4, zero history before t = 0:
+ *     v_t = conv_b[d] + sum_{k=0}^{3} conv_w[d, k] x[t - 3 + k]
+ *     u_t = v_t                      (act 0)
+ *     u_t = v_t / (1 + exp(-v_t))    (act 1, SiLU as in the usual Mamba block)
+ * then the zero-order-hold scan of oracle_scan_fwd on u (in float64, u is not
+ * rounded to the input dtype).  x has the layout and dtype of u.
+ */
+static void conv_scan_channel(const void *x, const float *conv_w, const float *conv_b, int act,
+                              const void *delta, const float *dt_bias, const float *A,
+                              const void *B, const void *C, const float *Dskip,
+                              const void *z, double *y, double *h_last, int64_t b,
+                              int64_t d, int64_t L, int64_t D, int64_t N, int dtype,
+                              double *h)
+{
+    memset(h, 0, sizeof(double) * (size_t)N);
+    const double bias_d = dt_bias ? (double)dt_bias[d] : 0.0;
+    const double skip_d = Dskip ? (double)Dskip[d] : 0.0;
+    const double cb = conv_b ? (double)conv_b[d] : 0.0;
+    for (int64_t t = 0; t < L; t++) {
+        int64_t i_btd = (b * L + t) * D + d;
+        double v = cb;
+        for (int k = 0; k < 4; k++) {
+            int64_t ts = t - 3 + k;
+            if (ts >= 0)
+                v += (double)conv_w[d * 4 + k] * load_elem(x, (b * L + ts) * D + d, dtype);
+        }
+        const double ut = act ? v / (1.0 + exp(-v)) : v;
+        double dt = softplus(load_elem(delta, i_btd, dtype) + bias_d);
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; n++) {
+            double a = (double)A[d * N + n];
+            double abar = exp(dt * a);
+            double coef = a != 0.0 ? expm1(dt * a) / a : dt;
+            h[n] = abar * h[n] + coef * load_elem(B, (b * L + t) * N + n, dtype) * ut;
+            acc += load_elem(C, (b * L + t) * N + n, dtype) * h[n];
+        }
+        double out = acc + skip_d * ut;
+        if (z)
+            out *= silu(load_elem(z, i_btd, dtype));
+        y[i_btd] = out;
+    }
+    if (h_last) {
+        double *hl = h_last + (b * D + d) * N;
+        for (int64_t n = 0; n < N; n++)
+            hl[n] = h[n];
+    }
+}
+
+/* Convolution (conv_w [D, 4], conv_b [D] or NULL, act 0/1) then the scan. */
+int oracle_conv_scan_fwd(const void *x, const float *conv_w, const float *conv_b, int act,
+                         const void *delta, const float *dt_bias, const float *A,
+                         const void *B, const void *C, const float *Dskip, const void *z,
+                         double *y, double *h_last, int64_t batch, int64_t L, int64_t D,
+                         int64_t N, int dtype, int64_t d_begin, int64_t d_end)
+{
+    if (!x || !conv_w || !delta || !A || !B || !C || !y)
+        return -1;
+    if (batch < 0 || L < 0 || D < 0 || N < 1 || (dtype != 0 && dtype != 1) ||
+        (act != 0 && act != 1))
+        return -1;
+    if (d_begin < 0 || d_end > D || d_begin > d_end)
+        return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!h)
+        return -2;
+    for (int64_t b = 0; b < batch; b++)
+        for (int64_t d = d_begin; d < d_end; d++)
+            conv_scan_channel(x, conv_w, conv_b, act, delta, dt_bias, A, B, C, Dskip, z, y,
+                              h_last, b, d, L, D, N, dtype, h);
+    free(h);
+    return 0;
+}
+
 /* ABI probe used by the Python wrapper to refuse a stale build. */
-int oracle_abi_version(void) { return 2; }
+int oracle_abi_version(void) { return 3; }

@@ -533,3 +533,64 @@ def pin_disc_orders_against_ode(lib):
 
 DISC_PINS = [pin_disc_zoh_is_the_scan, pin_disc_euler_constant_input,
              pin_disc_trapezoid_constant_input, pin_disc_orders_against_ode]
+
+
+# ------------------------------------------------ convolution before the SSM
+def _conv(lib, p, w, cb, act):
+    return oracle.conv_scan_fwd(p["u"], _f32(w), None if cb is None else _f32(cb), act,
+                                p["delta"], p["dt_bias"], p["A"], p["B"], p["C"], p["Dskip"],
+                                p["z"], dtype=oracle.F32, lib=lib)
+
+
+def pin_conv_against_numpy(lib):
+    """With B = 0 the state stays 0 and y = Dskip u: with Dskip = 1 and no gate
+    y is the convolution output itself, checked against numpy.convolve (causal,
+    width 4, w[d, 3] on the current input) plus bias, and SiLU via scipy's
+    logistic function for act = 1."""
+    rng = np.random.default_rng(60)
+    p = random_problem(rng, 2, 30, 5, 4, gate=False)
+    p["B"] = _f32(np.zeros_like(p["B"]))
+    p["Dskip"] = _f32(np.ones(5))
+    w = rng.standard_normal((5, 4))
+    cb = rng.standard_normal(5)
+    for act in (0, 1):
+        y, _ = _conv(lib, p, w, cb, act)
+        x = np.float64(p["u"])
+        wf, cbf = np.float64(np.float32(w)), np.float64(np.float32(cb))
+        for b in range(2):
+            for d in range(5):
+                v = np.convolve(x[b, :, d], wf[d][::-1])[:30] + cbf[d]
+                want = v * scipy.special.expit(v) if act else v
+                _close(y[b, :, d], want, 1e-12, 1e-13, f"conv act={act} b={b} d={d}")
+
+
+def pin_conv_identity_is_the_scan(lib):
+    """Kernel (0, 0, 0, 1), no bias, no activation: u = x, so the result is the
+    plain scan of x."""
+    rng = np.random.default_rng(61)
+    p = random_problem(rng, 2, 20, 4, 6)
+    w = np.tile([0.0, 0.0, 0.0, 1.0], (4, 1))
+    y, h = _conv(lib, p, w, None, 0)
+    y0, h0 = scan(lib, p)
+    _close(y, y0, 1e-13, 1e-15, "identity kernel y")
+    _close(h, h0, 1e-13, 1e-15, "identity kernel h")
+
+
+def pin_conv_shift_is_a_delay(lib):
+    """Kernel (0, 0, 1, 0): u_t = x_{t-1} (0 at t = 0), the plain scan of the
+    delayed input."""
+    rng = np.random.default_rng(62)
+    p = random_problem(rng, 1, 25, 3, 5)
+    w = np.tile([0.0, 0.0, 1.0, 0.0], (3, 1))
+    y, h = _conv(lib, p, w, None, 0)
+    q = dict(p)
+    shifted = np.zeros_like(p["u"])
+    shifted[:, 1:] = p["u"][:, :-1]
+    q["u"] = _f32(shifted)
+    y0, h0 = scan(lib, q)
+    # the skip term uses the (delayed) u as well
+    _close(y, y0, 1e-13, 1e-15, "delay kernel y")
+    _close(h, h0, 1e-13, 1e-15, "delay kernel h")
+
+
+CONV_PINS = [pin_conv_against_numpy, pin_conv_identity_is_the_scan, pin_conv_shift_is_a_delay]
