@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--workload", default="mamba2.8b", choices=sorted(WORKLOADS),
                     help="scan shape (default: the Mamba-2.8B layer; the others are the "
                          "smaller cases used for ncu captures)")
@@ -253,6 +254,9 @@ def bench_ours(args, rank, world, local):
     achieved_tflops = 2 * FMA_PER_ELEMENT_N16 * w.elements / avg_launch_s / 1e12
     traffic, traffic_src = recorded_traffic()
 
+    variants = None
+    if not args.no_variants:
+        variants = bench_variants(ssm, inp, w, stream)
     decode = None
     if not args.no_decode:
         decode = bench_decode(ssm, dev, stream)
@@ -293,6 +297,7 @@ def bench_ours(args, rank, world, local):
                          "frac": achieved_gbs / peak, "peak_source": peak_kind},
         "clocks": clocks.summary(),
         "decode": decode,
+        "discretisation_variants": variants,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_call(w),
         "cpu_baseline": cpu,
@@ -370,6 +375,42 @@ def bench_decode(ssm, dev, stream, reps: int = 5):
             "hbm_frac": gbs / peak, "peak_source": kind, "kernel_launches": w.steps,
             "note": "best of %d; the 84 MB state can stay resident in the 126 MB L2 across "
                     "steps, so GB/s is algorithmic bytes / time, not DRAM traffic" % reps}
+
+
+def bench_variants(ssm, inp, w, stream, reps: int = 5):
+    """The Euler and trapezoidal discretisations (ssm_scan_fwd_disc) and the
+    convolution in front of the scan (ssm_conv_scan_fwd, SiLU; x in place of u)
+    on the same workload, timed like the headline (CUDA events, best of
+    `reps`)."""
+    import torch
+    from selective_state_space_113_b300 import workloads as wl
+    y = torch.empty_like(inp["u"])
+    h = torch.empty((w.batch, w.D, w.N), device=inp["u"].device, dtype=torch.float32)
+    conv_w, conv_b = wl.conv_params(w.D, w.seed + 1000, inp["u"].device)
+    out = {}
+    for name, disc in (("euler", 1), ("trapezoid", 2), ("conv_silu", None)):
+        def call():
+            if disc is None:
+                ssm.ssm_conv_scan_fwd(inp["u"], conv_w, conv_b, 1, inp["delta"],
+                                      inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                                      inp["Dskip"], inp["z"], y, h, stream=stream)
+                return
+            ssm.ssm_scan_fwd_disc(inp["u"], inp["delta"], inp["dt_bias"], inp["A"], inp["B"],
+                                  inp["C"], inp["Dskip"], inp["z"], y, h, disc, stream=stream)
+        for _ in range(3):
+            call()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None or ms < best else best
+        out[name] = {"ms": best, "elements_per_s": w.elements / (best * 1e-3),
+                     "hbm_gbs": algorithmic_bytes(w) / (best * 1e-3) / 1e9}
+    return out
 
 
 def launches_per_call(w) -> int:

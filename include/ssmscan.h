@@ -75,7 +75,7 @@ typedef enum {
     SSM_ERR_SIZE = -2,        /* negative size, N < 1, or a size that overflows */
     SSM_ERR_DTYPE = -3,       /* dtype is not an ssm_dtype_t value */
     SSM_ERR_ALIGN = -4,       /* a pointer is not aligned to its element size */
-    SSM_ERR_UNSUPPORTED = -5, /* N > SSM_MAX_N, or an unknown discretisation */
+    SSM_ERR_UNSUPPORTED = -5, /* N > SSM_MAX_N, an unknown discretisation or act */
     SSM_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
     SSM_ERR_NOMEM = -7,       /* the stream-ordered workspace could not be allocated */
     SSM_ERR_TIMEOUT = -8,     /* a device-side bounded wait gave up (see ssm_device_status) */
@@ -129,6 +129,31 @@ SSM_API int ssm_scan_fwd_disc(const void *u, const void *delta, const float *dt_
                               const float *Dskip, const void *z, void *y, float *h_last,
                               int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
                               int disc, void *stream);
+
+/*
+ * ssm_conv_scan_fwd -- the short causal convolution in front of the SSM,
+ * then ssm_scan_fwd on its output (ta-paperlens page, "現場ではこう使う":
+ * d_conv, a short convolution before the SSM; agenticai-flow page: d_conv=4
+ * with causal-conv1d).  Read as depthwise (one width-4 filter per channel),
+ * causal, zero input before step 0, with an optional SiLU after it (the
+ * pages name no activation; act selects one):
+ *     v_t[d] = conv_b[d] + sum_{k=0}^{3} conv_w[d, k] x_{t-3+k}[d]
+ *     u_t[d] = act ? v_t[d] sigmoid(v_t[d]) : v_t[d]
+ * and u feeds the zero-order-hold scan, also in the D skip term.
+ *
+ *   x           : [batch, L, D] dtype (in place of ssm_scan_fwd's u)
+ *   conv_w      : [D, 4] float32, conv_w[d, 3] multiplies the current x;
+ *                 required when D > 0 (else SSM_ERR_NULL)
+ *   conv_b      : [D] float32 (NULL means 0)
+ *   act         : 0 (none) or 1 (SiLU); another value is SSM_ERR_UNSUPPORTED
+ * The other arguments, layouts, ownership and errors are those of
+ * ssm_scan_fwd.  The fast path (N == 16) also wants conv_w 16-byte aligned.
+ */
+SSM_API int ssm_conv_scan_fwd(const void *x, const float *conv_w, const float *conv_b, int act,
+                              const void *delta, const float *dt_bias, const float *A,
+                              const void *B, const void *C, const float *Dskip, const void *z,
+                              void *y, float *h_last, int64_t batch, int64_t L, int64_t D,
+                              int64_t N, int dtype, void *stream);
 
 /*
  * ssm_step -- one decode token: the same per-token update as one step of

@@ -54,17 +54,25 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA; 
 
 namespace {
 
-// The scan with a discretisation variant (ssm_disc_t); ssm_scan_fwd is
-// variant 0.
+// The convolution in front of the scan (ssm_conv_scan_fwd): conv_w NULL = none.
+struct ConvArgs {
+    const float* w;
+    const float* b;
+    int act;
+};
+
+// The scan with a discretisation variant (ssm_disc_t) and an optional
+// convolution of u; ssm_scan_fwd is variant 0 without a convolution.
 int scan_impl(const void* u, const void* delta, const float* dt_bias, const float* A,
               const void* B, const void* C, const float* Dskip, const void* z, void* y,
               float* h_last, int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
-              int disc, void* stream_) {
+              int disc, void* stream_, ConvArgs conv = {nullptr, nullptr, 0}) {
     if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (disc != SSM_DISC_ZOH && disc != SSM_DISC_EULER && disc != SSM_DISC_TRAPEZOID)
         return SSM_ERR_UNSUPPORTED;
+    if (conv.act != 0 && conv.act != 1) return SSM_ERR_UNSUPPORTED;
     int64_t bl, bld, bln, bd, bdn, dn;
     if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) ||
         !mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || !mul_ok(D, N, &dn) ||
@@ -73,7 +81,8 @@ int scan_impl(const void* u, const void* delta, const float* dt_bias, const floa
     // A pointer may be NULL only when its tensor has no elements.
     if ((bld && (!u || !delta || !y)) || (bln && (!B || !C)) || (dn && !A))
         return SSM_ERR_NULL;
-    if (!elems_aligned(dtype, {u, delta, B, C, z, y}, {dt_bias, A, Dskip, h_last}))
+    if (!elems_aligned(dtype, {u, delta, B, C, z, y},
+                       {dt_bias, A, Dskip, h_last, conv.w, conv.b}))
         return SSM_ERR_ALIGN;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (bd == 0) return SSM_OK;
@@ -85,8 +94,22 @@ int scan_impl(const void* u, const void* delta, const float* dt_bias, const floa
     // Fast path: N == 16, 16-byte-aligned tensors and rows (TMA tiles).
     const int plan = ssm::tile::forced_plan();
     if (N == ssm::tile::NS && plan != ssm::tile::kPlanGeneric &&
-        all_aligned16({u, delta, z, B, C, y, h_last, A}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
+        all_aligned16({u, delta, z, B, C, y, h_last, A, conv.w}) &&
+        (D * (int64_t)elem_size(dtype)) % 16 == 0) {
         using namespace ssm::tile;
+        if (conv.w) {
+            if (dtype == SSM_F32)
+                return launch_scan_tile<float, kZOH, true>(
+                    static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+                    static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+                    static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D,
+                    plan, stream, conv.w, conv.b, conv.act);
+            return launch_scan_tile<bf16, kZOH, true>(
+                static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+                static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+                static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, plan,
+                stream, conv.w, conv.b, conv.act);
+        }
 #define SSM_TILE_CALL(TT, DISC)                                                              \
     launch_scan_tile<TT, DISC>(static_cast<const TT*>(u), static_cast<const TT*>(delta), dt_bias, \
                                A, static_cast<const TT*>(B), static_cast<const TT*>(C), Dskip,   \
@@ -108,13 +131,13 @@ int scan_impl(const void* u, const void* delta, const float* dt_bias, const floa
             static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
             static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
             static_cast<const float*>(z), static_cast<float*>(y), h_last, batch, L, D, (int)N,
-            stream, disc);
+            stream, disc, conv.w, conv.b, conv.act);
     else
         e = ssm::launch_scan_generic<bf16>(
             static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
             static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
             static_cast<const bf16*>(z), static_cast<bf16*>(y), h_last, batch, L, D, (int)N,
-            stream, disc);
+            stream, disc, conv.w, conv.b, conv.act);
     return from_cuda(e);
 }
 
@@ -136,6 +159,17 @@ extern "C" int ssm_scan_fwd_disc(const void* u, const void* delta, const float* 
                                  int disc, void* stream_) {
     return scan_impl(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
                      disc, stream_);
+}
+
+extern "C" int ssm_conv_scan_fwd(const void* x, const float* conv_w, const float* conv_b,
+                                 int act, const void* delta, const float* dt_bias,
+                                 const float* A, const void* B, const void* C,
+                                 const float* Dskip, const void* z, void* y, float* h_last,
+                                 int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                                 void* stream_) {
+    if (D > 0 && !conv_w) return SSM_ERR_NULL;
+    return scan_impl(x, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
+                     SSM_DISC_ZOH, stream_, ConvArgs{D > 0 ? conv_w : nullptr, conv_b, act});
 }
 
 extern "C" int ssm_step(float* state, const void* u, const void* delta, const float* dt_bias,

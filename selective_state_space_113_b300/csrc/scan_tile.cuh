@@ -61,6 +61,14 @@
 //           h <- A_bar s + dt/2 P_t with P_t = B_t u_t kept per state; a
 //           piece's first step takes P from the step before it (header).
 // For kEuler and kTrap the helpers widen B without the 1/(n+1) scale.
+//
+// CONV: the input is x, and u is the short causal convolution in front of the
+// SSM (ta-paperlens "現場ではこう使う": d_conv; agenticai-flow: d_conv=4,
+// causal-conv1d), depthwise, width 4, optional SiLU:
+//     u_t = act(conv_b[d] + sum_k conv_w[d, k] x_{t-3+k}).
+// Only the helpers change: they read x from the stage tile, keep x_{t-1..t-3}
+// of their channel in registers, and load the weights and the three x values
+// before a piece when the piece starts.
 #pragma once
 
 #include <cuda.h>
@@ -111,8 +119,11 @@ struct ChanPar {
 struct Params {
     void* y;
     float* h_last;
-    const void* u;          // raw u and B, read for the trapezoid's step before a piece
+    const void* u;          // raw u (x with CONV) and B: the steps before a piece
     const void* Bm;
+    const float* conv_w;    // [D, 4] (CONV)
+    const float* conv_b;    // [D] or NULL (CONV)
+    int act;                // CONV: 1 = SiLU after the convolution
     const float* dt_bias;
     const float* A;
     const float* Dskip;
@@ -339,9 +350,15 @@ __device__ int fill_header(unsigned char* st, const Params& p, long long b, long
 //   kEuler            {r, dt u, g, sug}               {dl, u, g, sug}
 //   kTrap             {r, dt/2, u, g}                 {dl, u, g, sug}
 //   kAggregate mode   the same .x/.y (kTrap: .x/.y/.z), .w = dl
-template <typename T, int MODE, int DISC, bool HASZ>
+// Per-lane state of the convolution (CONV): weights, bias, the last three x.
+struct ConvState {
+    float w0, w1, w2, w3, bias, x1, x2, x3;   // x1 = x_{t-1}, x2 = x_{t-2}, x3 = x_{t-3}
+};
+
+template <typename T, int MODE, int DISC, bool HASZ, bool CONV>
 __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0, int col,
-                                               const ChanPar& cp, bool geo, float4* out) {
+                                               const ChanPar& cp, bool geo, float4* out,
+                                               ConvState& cs, int act) {
     using C = Cfg<T>;
     const T* U = reinterpret_cast<const T*>(st + C::offU);
     const T* Dl = reinterpret_cast<const T*>(st + C::offD);
@@ -354,7 +371,18 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
 #pragma unroll
     for (int j = 0; j < KP; ++j) {
         const int t = row0 + j;
-        const float u = ld_elem(U + t * CB + col);
+        float u = ld_elem(U + t * CB + col);
+        if (CONV) {
+            const float x = u;
+            float v = fmaf(cs.w0, cs.x3, cs.bias);
+            v = fmaf(cs.w1, cs.x2, v);
+            v = fmaf(cs.w2, cs.x1, v);
+            v = fmaf(cs.w3, x, v);
+            u = act ? v * ptx::rcp(1.0f + ptx::ex2(v * -kLog2e)) : v;
+            cs.x3 = cs.x2;
+            cs.x2 = cs.x1;
+            cs.x1 = x;
+        }
         const float dv = ld_elem(Dl + t * CB + col);
         const float v2 = fmaf(dv, kLog2e, cp.kb2);           // (delta + bias) log2(e)
         const float dl = ptx::lg2(1.0f + ptx::ex2(v2));      // softplus / ln 2
@@ -523,7 +551,7 @@ __device__ __forceinline__ void steps_general(const unsigned char* st, int row0,
     }
 }
 
-template <typename T, int MODE, int DISC>
+template <typename T, int MODE, int DISC, bool CONV>
 __global__ void __launch_bounds__(THREADS, 1)
 scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmD,
                  const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmB,
@@ -686,6 +714,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
         const int hi = warp - NCW;
         float4* pro = reinterpret_cast<float4*>(smem + C::offPro + hi * C::kPro);
         ChanPar cp{0.f, 0.f, 0.f, 0.f};
+        ConvState cs{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         bool geo = true;
         long long q = 0;   // prologue chunks produced
         bool failed = false;
@@ -704,6 +733,25 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             if (m.flags & kFirst) {
                 cp = reinterpret_cast<const ChanPar*>(st + C::offPar)[CW * hi + lane];
                 geo = (m.geo >> hi) & 1;
+                if (CONV) {
+                    // weights and the three x values before the piece (zero
+                    // before step 0 and past the last channel)
+                    const long long b = m.chain / p.nCB;
+                    const long long d = (m.chain % p.nCB) * CB + CW * hi + lane;
+                    const bool valid = d < p.D;
+                    const float4 w4 = valid ? __ldg(reinterpret_cast<const float4*>(p.conv_w) + d)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    cs.w0 = w4.x;
+                    cs.w1 = w4.y;
+                    cs.w2 = w4.z;
+                    cs.w3 = w4.w;
+                    cs.bias = (valid && p.conv_b) ? __ldg(p.conv_b + d) : 0.0f;
+                    const T* xs = static_cast<const T*>(p.u) + b * p.L * p.D + (valid ? d : 0);
+                    const long long t0 = m.t0;
+                    cs.x1 = (valid && t0 >= 1) ? to_f32(xs[(t0 - 1) * p.D]) : 0.0f;
+                    cs.x2 = (valid && t0 >= 2) ? to_f32(xs[(t0 - 2) * p.D]) : 0.0f;
+                    cs.x3 = (valid && t0 >= 3) ? to_f32(xs[(t0 - 3) * p.D]) : 0.0f;
+                }
             }
             const int nchunks = (m.nvalid + KP - 1) / KP;
             for (int c = 0; c < nchunks; ++c, ++q) {
@@ -714,10 +762,11 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                 }
                 float4* out = pro + buf * (C::kProBuf / 16) + lane;
                 if (p.has_z)
-                    prologue_chunk<T, MODE, DISC, true>(st, c * KP, CW * hi + lane, cp, geo, out);
+                    prologue_chunk<T, MODE, DISC, true, CONV>(st, c * KP, CW * hi + lane, cp, geo,
+                                                              out, cs, p.act);
                 else
-                    prologue_chunk<T, MODE, DISC, false>(st, c * KP, CW * hi + lane, cp, geo,
-                                                         out);
+                    prologue_chunk<T, MODE, DISC, false, CONV>(st, c * KP, CW * hi + lane, cp, geo,
+                                                               out, cs, p.act);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&pfull[2 * hi + buf]);
             }

@@ -77,7 +77,7 @@ inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 // Sets the kernel's shared-memory limit and returns in *workers the number of
 // CTAs that can be resident at once.  Done once per device and kernel; later
 // calls read the cached count.
-template <typename T, int MODE, int DISC>
+template <typename T, int MODE, int DISC, bool CONV = false>
 inline cudaError_t prepare(int sms, long long* workers) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
@@ -92,7 +92,7 @@ inline cudaError_t prepare(int sms, long long* workers) {
             return cudaSuccess;
         }
     }
-    auto kern = scan_tile_kernel<T, MODE, DISC>;
+    auto kern = scan_tile_kernel<T, MODE, DISC, CONV>;
     const int smem = Cfg<T>::kSmemBytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -133,10 +133,10 @@ inline size_t header_bytes(long long batch, long long D) {
     return ((256 + (size_t)(batch * cdiv(D, CW)) * 4) + 255) & ~(size_t)255;
 }
 
-template <typename T, int MODE, int DISC>
+template <typename T, int MODE, int DISC, bool CONV = false>
 inline cudaError_t launch_mode(long long grid, const CUtensorMap* maps, const Params& p,
                                cudaStream_t s) {
-    scan_tile_kernel<T, MODE, DISC><<<(unsigned)grid, THREADS, Cfg<T>::kSmemBytes, s>>>(
+    scan_tile_kernel<T, MODE, DISC, CONV><<<(unsigned)grid, THREADS, Cfg<T>::kSmemBytes, s>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
     return cudaGetLastError();
 }
@@ -179,20 +179,22 @@ inline bool setup(CUtensorMap* maps, Params* p, const T* u, const T* delta, cons
 // Returns an ssm_status_t.  Preconditions (checked by the caller): N == 16,
 // u, delta, z, B, C, y, A and h_last 16-byte aligned, D * sizeof(T) % 16 == 0,
 // batch*D > 0, L > 0.
-template <typename T, int DISC>
+// CONV: u is x, convolved with conv_w/conv_b (act: SiLU) before the scan.
+template <typename T, int DISC, bool CONV = false>
 int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const float* A,
                      const T* Bm, const T* Cm, const float* Dskip, const T* z, T* y,
                      float* h_last, long long batch, long long L, long long D, int plan,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, const float* conv_w = nullptr,
+                     const float* conv_b = nullptr, int act = 0) {
     constexpr long long TC = Cfg<T>::TC;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SSM_ERR_CUDA;
     long long wc = 0, wa = 0, wf = 0;
-    if (prepare<T, (int)kChained, DISC>(sms, &wc) != cudaSuccess ||
-        prepare<T, (int)kAggregate, DISC>(sms, &wa) != cudaSuccess ||
-        prepare<T, (int)kFromState, DISC>(sms, &wf) != cudaSuccess || wc < 1 || wa < 1 ||
+    if (prepare<T, (int)kChained, DISC, CONV>(sms, &wc) != cudaSuccess ||
+        prepare<T, (int)kAggregate, DISC, CONV>(sms, &wa) != cudaSuccess ||
+        prepare<T, (int)kFromState, DISC, CONV>(sms, &wf) != cudaSuccess || wc < 1 || wa < 1 ||
         wf < 1)
         return SSM_ERR_CUDA;
 
@@ -200,6 +202,9 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
     Params p;
     if (!setup<T>(maps, &p, u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D))
         return SSM_ERR_CUDA;
+    p.conv_w = conv_w;
+    p.conv_b = conv_b;
+    p.act = act;
 
     bool narrow = false;
     if (plan == kPlanNarrow) narrow = true;
@@ -250,15 +255,15 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
         if (!narrow) {
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + off_carry);
-            if (launch_mode<T, (int)kChained, DISC>(p.G, maps, p, stream) != cudaSuccess)
+            if (launch_mode<T, (int)kChained, DISC, CONV>(p.G, maps, p, stream) != cudaSuccess)
                 status = SSM_ERR_CUDA;
         } else {
             p.agg = reinterpret_cast<float*>(ws + off_agg);
             p.hin = reinterpret_cast<float*>(ws + off_hin);
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.total_units = p.nchains * (p.P - 1);
-            if (launch_mode<T, (int)kAggregate, DISC>(p.total_units < wa ? p.total_units : wa,
-                                                      maps, p, stream) != cudaSuccess) {
+            if (launch_mode<T, (int)kAggregate, DISC, CONV>(
+                    p.total_units < wa ? p.total_units : wa, maps, p, stream) != cudaSuccess) {
                 status = SSM_ERR_CUDA;
                 break;
             }
@@ -271,8 +276,8 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
             }
             p.ticket = reinterpret_cast<unsigned long long*>(ws + 16);
             p.total_units = p.nchains * p.P;
-            if (launch_mode<T, (int)kFromState, DISC>(p.total_units < wf ? p.total_units : wf,
-                                                      maps, p, stream) != cudaSuccess)
+            if (launch_mode<T, (int)kFromState, DISC, CONV>(
+                    p.total_units < wf ? p.total_units : wf, maps, p, stream) != cudaSuccess)
                 status = SSM_ERR_CUDA;
         }
     } while (0);

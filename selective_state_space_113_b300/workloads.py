@@ -14,6 +14,9 @@ workload definitions fix):
   Dskip       ~ N(0, 1)   [D]                float32
   A[d, n]     = -(n + 1)                     float32 (S4D-real / Mamba init)
   decode state ~ N(0, 1)  [batch, D, N]      float32
+  conv_w, conv_b ~ U(-1/2, 1/2)  [D, 4], [D]  float32 (the default init of a
+                depthwise width-4 Conv1d, bound 1/sqrt(fan_in) = 1/2), drawn
+                by ``conv_params`` from a generator of their own
 Draws happen in float32 from one torch.Generator seeded with the workload's
 seed, in the order listed, then are rounded to bf16 where the workload is bf16.
 The time-invariant variant repeats the t = 0 draws of delta, B and C along t.
@@ -126,6 +129,15 @@ def make_scan_inputs(w: ScanWorkload, device="cpu", seed: int | None = None,
         C = _randn((batch, L, N), g, device, dt)
     dt_bias, Dskip, A = channel_params(D, N, g, device)
     return dict(u=u, delta=delta, dt_bias=dt_bias, A=A, B=B, C=C, Dskip=Dskip, z=z)
+
+
+def conv_params(D: int, seed: int, device="cpu"):
+    """conv_w [D, 4] and conv_b [D], float32, U(-1/2, 1/2), for the causal
+    convolution in front of the scan (x takes the place of u)."""
+    g = _gen(seed, device)
+    w = (torch.rand((D, 4), generator=g, device=device) - 0.5).contiguous()
+    b = torch.rand(D, generator=g, device=device) - 0.5
+    return w, b
 
 
 def make_step_inputs(w: StepWorkload, device="cpu", seed: int | None = None,
