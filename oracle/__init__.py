@@ -51,6 +51,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_conv_scan_fwd.restype = ctypes.c_int
     lib.oracle_conv_scan_fwd.argtypes = ([vp] * 3 + [ctypes.c_int] + [vp] * 9 + [i64] * 4
                                          + [ctypes.c_int, i64, i64])
+    lib.oracle_scan_bwd.restype = ctypes.c_int
+    lib.oracle_scan_bwd.argtypes = [vp] * 18 + [i64] * 4 + [ctypes.c_int, i64, i64]
     lib.oracle_abi_version.restype = ctypes.c_int
     return lib
 
@@ -70,7 +72,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                     or os.path.getmtime(LIB) < os.path.getmtime(SRC)):
                 build()
             lib = _bind(ctypes.CDLL(LIB))
-            if lib.oracle_abi_version() != 3:
+            if lib.oracle_abi_version() != 4:
                 raise RuntimeError("stale oracle build: " + LIB)
             _lib = lib
         return _lib
@@ -214,6 +216,55 @@ def conv_scan_fwd(x, conv_w, conv_b, act, delta, dt_bias, A, B, C, Dskip, z,
             list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])),
                         range(threads)))
     return y, h
+
+
+def scan_bwd(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last=None, dtype: int = F32,
+             threads: int = 1, lib: ctypes.CDLL | None = None):
+    """Backward pass of the zero-order-hold scan, float64: the derivatives of a
+    loss with dLoss/dy = dy ([Bt,L,D], the input dtype) and dLoss/dh_last =
+    dh_last ([Bt,D,N] float32, None = 0).
+
+    Returns a dict of float64 arrays: du, ddelta, dz ([Bt,L,D]; dz None
+    without z), dB, dC ([Bt,L,N]), dA ([D,N]), ddt_bias, dDskip ([D]).
+    """
+    lib = lib or load()
+    u, delta, z, dy = (_as_input(x, dtype) for x in (u, delta, z, dy))
+    B, C = _as_input(B, dtype), _as_input(C, dtype)
+    A, dt_bias, Dskip = _as_f32(A), _as_f32(dt_bias), _as_f32(Dskip)
+    dh_last = _as_f32(dh_last)
+    batch, L, D = u.shape
+    N = A.shape[1]
+    if (A.shape != (D, N) or B.shape != (batch, L, N) or C.shape != (batch, L, N)
+            or dy.shape != u.shape or (dh_last is not None and dh_last.shape != (batch, D, N))):
+        raise ValueError("inconsistent shapes")
+    du = np.zeros((batch, L, D), np.float64)
+    ddelta = np.zeros((batch, L, D), np.float64)
+    dz = np.zeros((batch, L, D), np.float64) if z is not None else None
+    dA = np.zeros((D, N), np.float64)
+    ddt_bias = np.zeros(D, np.float64)
+    dDskip = np.zeros(D, np.float64)
+    threads = max(1, min(int(threads), D)) if D else 1
+    parts = [(np.zeros((batch, L, N)), np.zeros((batch, L, N))) for _ in range(threads)]
+
+    def run(i, lo, hi):
+        dB_i, dC_i = parts[i]
+        rc = lib.oracle_scan_bwd(_ptr(u), _ptr(delta), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
+                                 _ptr(Dskip), _ptr(z), _ptr(dy), _ptr(dh_last), _ptr(du),
+                                 _ptr(ddelta), _ptr(ddt_bias), _ptr(dA), _ptr(dB_i), _ptr(dC_i),
+                                 _ptr(dDskip), _ptr(dz), batch, L, D, N, dtype, lo, hi)
+        if rc != 0:
+            raise RuntimeError(f"oracle_scan_bwd returned {rc}")
+
+    bounds = np.linspace(0, D, threads + 1).astype(np.int64)
+    if threads == 1:
+        run(0, 0, D)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda i: run(i, int(bounds[i]), int(bounds[i + 1])), range(threads)))
+    dB = sum(p[0] for p in parts)
+    dC = sum(p[1] for p in parts)
+    return dict(du=du, ddelta=ddelta, dz=dz, dB=dB, dC=dC, dA=dA, ddt_bias=ddt_bias,
+                dDskip=dDskip)
 
 
 def step(state, u, delta, dt_bias, A, B, C, Dskip, z, dtype: int = F32,

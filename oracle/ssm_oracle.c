@@ -350,5 +350,153 @@ int oracle_conv_scan_fwd(const void *x, const float *conv_w, const float *conv_b
     return 0;
 }
 
+/*
+ * Backward pass of the zero-order-hold scan: the reverse-mode derivative
+ * (adjoint) of oracle_scan_fwd for a loss whose derivative is dy with
+ * respect to y and dh_last (NULL means 0) with respect to h_last.  The
+ * backward half of the layer is what the fused kernel on the ta-paperlens
+ * page recomputes states for instead of storing them ("代償と、それを払う方法
+ * （並列スキャン）"); this oracle simply keeps every state of the channel.
+ *
+ * With s_t = sum_n C_t[n] h_t[n] + Dskip u_t, y_t = s_t g_t, g = silu(z)
+ * (g = 1 without z), q[n] = (Abar[n] - 1)/a[n] and lam[n] the derivative of
+ * the loss with respect to h_t[n], walking t from L-1 down to 0:
+ *   ds_t     = dy_t g_t
+ *   dz_t     = dy_t s_t silu'(z_t),   silu'(z) = sig(z) (1 + z (1 - sig(z)))
+ *   lam[n]  += ds_t C_t[n]                      (h_t is read out at step t)
+ *   dC_t[n] += ds_t h_t[n]
+ *   dB_t[n] += lam[n] q[n] u_t
+ *   du_t     = ds_t Dskip + sum_n lam[n] q[n] B_t[n]
+ *   ddt      = sum_n lam[n] Abar[n] (a[n] h_{t-1}[n] + B_t[n] u_t)
+ *              (d Abar/d dt = a Abar, d q/d dt = Abar)
+ *   dA[n]   += lam[n] (dt Abar[n] h_{t-1}[n] + q'[n] B_t[n] u_t),
+ *              q' = d q/d a = dt^2 (x e^x - (e^x - 1)) / x^2 with x = dt a,
+ *              dt^2/2 at a == 0
+ *   ddelta_t = ddt sig(delta_t + bias)          (softplus' = sigmoid)
+ *   ddt_bias += ddelta_t;  dDskip += ds_t u_t
+ *   lam[n]   = Abar[n] lam[n]                   (h_{t-1} feeds h_t)
+ * starting from lam = dh_last and h_{-1} = 0.
+ * Outputs (float64): du, ddelta, dz [B, L, D] (dz may be NULL, and is
+ * ignored without z); dA [D, N], ddt_bias [D], dDskip [D] are written for the
+ * channels in [d_begin, d_end) (sums over batch and steps); dB, dC [B, L, N]
+ * are ADDED to (sums over channels: the caller zeroes them, and gives each
+ * thread its own pair when it splits the channel range).
+ */
+static double sigmoid_of(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+/* d/da of (exp(dt a) - 1)/a. */
+static double dq_da(double dt, double a)
+{
+    double x = dt * a;
+    if (fabs(x) < 1e-3) /* Taylor series of (x e^x - e^x + 1)/x^2 */
+        return dt * dt * (0.5 + x * (1.0 / 3.0 + x * (1.0 / 8.0 + x * (1.0 / 30.0))));
+    return dt * dt * (x * exp(x) - expm1(x)) / (x * x);
+}
+
+static void bwd_channel(const void *u, const void *delta, const float *dt_bias, const float *A,
+                        const void *B, const void *C, const float *Dskip, const void *z,
+                        const void *dy, const float *dh_last, double *du, double *ddelta,
+                        double *ddt_bias, double *dA, double *dB, double *dC, double *dDskip,
+                        double *dz, int64_t b, int64_t d, int64_t L, int64_t D, int64_t N,
+                        int dtype, double *traj, double *lam)
+{
+    const double bias_v = dt_bias ? (double)dt_bias[d] : 0.0;
+    const double skip_v = Dskip ? (double)Dskip[d] : 0.0;
+    /* forward: every state h_t, kept in traj[t * N + n] */
+    for (int64_t t = 0; t < L; t++) {
+        const int64_t e = (b * L + t) * D + d;
+        const double ut = load_elem(u, e, dtype);
+        const double dt = softplus(load_elem(delta, e, dtype) + bias_v);
+        for (int64_t n = 0; n < N; n++) {
+            double abar, q;
+            zoh(dt, (double)A[d * N + n], &abar, &q);
+            const double prev = t > 0 ? traj[(t - 1) * N + n] : 0.0;
+            traj[t * N + n] = abar * prev + q * load_elem(B, (b * L + t) * N + n, dtype) * ut;
+        }
+    }
+    for (int64_t n = 0; n < N; n++)
+        lam[n] = dh_last ? (double)dh_last[(b * D + d) * N + n] : 0.0;
+    /* backward */
+    for (int64_t t = L - 1; t >= 0; t--) {
+        const int64_t e = (b * L + t) * D + d;
+        const double ut = load_elem(u, e, dtype);
+        const double pre = load_elem(delta, e, dtype) + bias_v;
+        const double dt = softplus(pre);
+        const double dyt = load_elem(dy, e, dtype);
+        double s = skip_v * ut;
+        for (int64_t n = 0; n < N; n++)
+            s += load_elem(C, (b * L + t) * N + n, dtype) * traj[t * N + n];
+        double g = 1.0, ds = dyt;
+        if (z) {
+            const double zt = load_elem(z, e, dtype);
+            const double sg = sigmoid_of(zt);
+            g = zt * sg;
+            ds = dyt * g;
+            if (dz)
+                dz[e] = dyt * s * sg * (1.0 + zt * (1.0 - sg));
+        }
+        double du_t = ds * skip_v, ddt = 0.0;
+        for (int64_t n = 0; n < N; n++) {
+            const int64_t r = (b * L + t) * N + n;
+            const double a = (double)A[d * N + n];
+            const double bt = load_elem(B, r, dtype);
+            const double ht = traj[t * N + n];
+            const double hp = t > 0 ? traj[(t - 1) * N + n] : 0.0;
+            double abar, q;
+            zoh(dt, a, &abar, &q);
+            lam[n] += ds * load_elem(C, r, dtype);
+            dC[r] += ds * ht;
+            dB[r] += lam[n] * q * ut;
+            du_t += lam[n] * q * bt;
+            ddt += lam[n] * abar * (a * hp + bt * ut);
+            dA[d * N + n] += lam[n] * (dt * abar * hp + dq_da(dt, a) * bt * ut);
+            lam[n] *= abar;
+        }
+        du[e] = du_t;
+        const double dd = ddt * sigmoid_of(pre);
+        ddelta[e] = dd;
+        if (ddt_bias)
+            ddt_bias[d] += dd;
+        if (dDskip)
+            dDskip[d] += ds * ut;
+    }
+}
+
+int oracle_scan_bwd(const void *u, const void *delta, const float *dt_bias, const float *A,
+                    const void *B, const void *C, const float *Dskip, const void *z,
+                    const void *dy, const float *dh_last, double *du, double *ddelta,
+                    double *ddt_bias, double *dA, double *dB, double *dC, double *dDskip,
+                    double *dz, int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                    int64_t d_begin, int64_t d_end)
+{
+    if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC)
+        return -1;
+    if (batch < 0 || L < 0 || D < 0 || N < 1 || (dtype != 0 && dtype != 1))
+        return -1;
+    if (d_begin < 0 || d_end > D || d_begin > d_end)
+        return -1;
+    double *traj = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)N);
+    double *lam = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!traj || !lam) {
+        free(traj);
+        free(lam);
+        return -2;
+    }
+    for (int64_t d = d_begin; d < d_end; d++) {
+        for (int64_t n = 0; n < N; n++)
+            dA[d * N + n] = 0.0;
+        if (ddt_bias)
+            ddt_bias[d] = 0.0;
+        if (dDskip)
+            dDskip[d] = 0.0;
+        for (int64_t b = 0; b < batch; b++)
+            bwd_channel(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last, du, ddelta, ddt_bias,
+                        dA, dB, dC, dDskip, dz, b, d, L, D, N, dtype, traj, lam);
+    }
+    free(traj);
+    free(lam);
+    return 0;
+}
+
 /* ABI probe used by the Python wrapper to refuse a stale build. */
-int oracle_abi_version(void) { return 3; }
+int oracle_abi_version(void) { return 4; }

@@ -594,3 +594,118 @@ def pin_conv_shift_is_a_delay(lib):
 
 
 CONV_PINS = [pin_conv_against_numpy, pin_conv_identity_is_the_scan, pin_conv_shift_is_a_delay]
+
+
+# ------------------------------------------------- backward-pass pins
+def _bwd(lib, p, dy, dh, dtype=oracle.F32):
+    return oracle.scan_bwd(p["u"], p["delta"], p["dt_bias"], p["A"], p["B"], p["C"], p["Dskip"],
+                           p["z"], dy, dh, dtype=dtype, lib=lib)
+
+
+def _loss(lib, p, dy, dh):
+    """The scalar whose derivatives the backward pass returns:
+    sum(dy * y) + sum(dh * h_last), from the (separately pinned) forward."""
+    y, h = scan(lib, p)
+    out = float(np.sum(dy.astype(np.float64) * y))
+    if dh is not None:
+        out += float(np.sum(dh.astype(np.float64) * h))
+    return out
+
+
+GRAD_OF = {"u": "du", "delta": "ddelta", "z": "dz", "B": "dB", "C": "dC", "A": "dA",
+           "dt_bias": "ddt_bias", "Dskip": "dDskip"}
+
+
+def pin_bwd_finite_differences(lib):
+    """Every gradient element against a central difference of the forward
+    scan: (loss(x + e) - loss(x - e)) / (x+ - x-), with the perturbed values
+    rounded to float32 first and the actual step used.  One channel has tiny
+    and zero A entries (the small-x series and the a == 0 limit)."""
+    rng = np.random.default_rng(11)
+    p = random_problem(rng, 2, 10, 4, 5)
+    p["A"][3] = _f32([-1e-4, -3e-6, 0.0, -2e-3, -1.0])
+    dy = _f32(rng.standard_normal(p["u"].shape))
+    dh = _f32(rng.standard_normal((2, 4, 5)))
+    g = _bwd(lib, p, dy, dh)
+    for key, gname in GRAD_OF.items():
+        x0 = p[key]
+        fd = np.zeros(x0.shape)
+        for idx in np.ndindex(x0.shape):
+            step = 1e-4 * max(abs(float(x0[idx])), 0.1)
+            xp, xm = x0.copy(), x0.copy()
+            xp[idx] = np.float32(float(x0[idx]) + step)
+            xm[idx] = np.float32(float(x0[idx]) - step)
+            lp = _loss(lib, dict(p, **{key: xp}), dy, dh)
+            lm = _loss(lib, dict(p, **{key: xm}), dy, dh)
+            fd[idx] = (lp - lm) / (float(xp[idx]) - float(xm[idx]))
+        _close(g[gname], fd, 1e-6, 1e-6, f"finite differences, {gname}")
+
+
+def pin_bwd_homogeneity(lib):
+    """Exact identities from linearity (Euler's theorem for functions of
+    degree 1): with the others fixed, y is linear in C, in u, in B (through
+    h) and in Dskip, and the gate depends on none of them.  So, with y0 the
+    output at Dskip = 0:  <dC, C> = <dy, y0>;  <du, u> = <dy, y> + <dh, h>;
+    <dB, B> = <dy, y0> + <dh, h>;  <dDskip, Dskip> = <dy, y - y0>."""
+    rng = np.random.default_rng(12)
+    p = random_problem(rng, 2, 30, 6, 4)
+    dy = _f32(rng.standard_normal(p["u"].shape))
+    dh = _f32(rng.standard_normal((2, 6, 4)))
+    g = _bwd(lib, p, dy, dh)
+    y, h = scan(lib, p)
+    y0, _ = scan(lib, dict(p, Dskip=None))            # the C h part of y (gated)
+    dy64, dh64 = dy.astype(np.float64), dh.astype(np.float64)
+    pairs = [
+        ("C", np.sum(dy64 * y0)),                      # h_last does not depend on C
+        ("u", np.sum(dy64 * y) + np.sum(dh64 * h)),
+        ("B", np.sum(dy64 * y0) + np.sum(dh64 * h)),
+        ("Dskip", np.sum(dy64 * (y - y0))),
+    ]
+    for key, want in pairs:
+        got = float(np.sum(g[GRAD_OF[key]] * p[key].astype(np.float64)))
+        _close(got, want, 1e-10, 1e-10, f"homogeneity in {key}")
+
+
+def pin_bwd_matches_autograd(lib):
+    """All gradients against torch.autograd of a float64 torch statement of
+    the forward (the derivative is the library's, not a hand derivation)."""
+    rng = np.random.default_rng(13)
+    p = random_problem(rng, 2, 9, 3, 4)
+    dy = _f32(rng.standard_normal(p["u"].shape))
+    dh = _f32(rng.standard_normal((2, 3, 4)))
+    g = _bwd(lib, p, dy, dh)
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in p.items()}
+    dt = torch.nn.functional.softplus(t["delta"] + t["dt_bias"])       # [b, L, D]
+    a = t["A"]                                                          # [D, N]
+    h = torch.zeros((2, 3, 4), dtype=torch.float64)
+    ys = []
+    for step in range(p["u"].shape[1]):
+        x = dt[:, step, :, None] * a                                    # [b, D, N]
+        h = torch.exp(x) * h + torch.expm1(x) / a * t["B"][:, step, None, :] * t["u"][:, step, :, None]
+        s = (h * t["C"][:, step, None, :]).sum(-1) + t["Dskip"] * t["u"][:, step]
+        ys.append(s * torch.nn.functional.silu(t["z"][:, step]))
+    y = torch.stack(ys, 1)
+    loss = (y * torch.tensor(dy, dtype=torch.float64)).sum() + \
+        (h * torch.tensor(dh, dtype=torch.float64)).sum()
+    grads = torch.autograd.grad(loss, [t[k] for k in GRAD_OF])
+    for key, gr in zip(GRAD_OF, grads):
+        _close(g[GRAD_OF[key]], gr.numpy(), 1e-9, 1e-9, f"autograd, {GRAD_OF[key]}")
+
+
+def pin_bwd_optional_inputs(lib):
+    """NULL gate, skip and bias: the gradients equal those of the explicit
+    neutral values (z -> SiLU gate absent, Dskip = 0, dt_bias = 0), and no
+    dh_last equals dh_last = 0."""
+    rng = np.random.default_rng(14)
+    p = random_problem(rng, 1, 12, 3, 4, gate=False, skip=False, bias=False)
+    dy = _f32(rng.standard_normal(p["u"].shape))
+    g = _bwd(lib, p, dy, None)
+    q = dict(p, Dskip=np.zeros(3, np.float32), dt_bias=np.zeros(3, np.float32))
+    g2 = _bwd(lib, q, dy, np.zeros((1, 3, 4), np.float32))
+    for k in ("du", "ddelta", "dB", "dC", "dA"):
+        _close(g[k], g2[k], 0.0, 0.0, f"optional inputs, {k}")
+    assert g["dz"] is None
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_homogeneity, pin_bwd_matches_autograd,
+            pin_bwd_optional_inputs]
