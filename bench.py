@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--workload", default="mamba2.8b", choices=sorted(WORKLOADS),
                     help="scan shape (default: the Mamba-2.8B layer; the others are the "
                          "smaller cases used for ncu captures)")
@@ -257,6 +258,9 @@ def bench_ours(args, rank, world, local):
     variants = None
     if not args.no_variants:
         variants = bench_variants(ssm, inp, w, stream)
+    backward = None
+    if not args.no_backward:
+        backward = bench_backward(ssm, inp, w, stream)
     decode = None
     if not args.no_decode:
         decode = bench_decode(ssm, dev, stream)
@@ -296,6 +300,7 @@ def bench_ours(args, rank, world, local):
         "hbm_roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                          "frac": achieved_gbs / peak, "peak_source": peak_kind},
         "clocks": clocks.summary(),
+        "backward": backward,
         "decode": decode,
         "discretisation_variants": variants,
         "e2e": e2e,
@@ -411,6 +416,49 @@ def bench_variants(ssm, inp, w, stream, reps: int = 5):
         out[name] = {"ms": best, "elements_per_s": w.elements / (best * 1e-3),
                      "hbm_gbs": algorithmic_bytes(w) / (best * 1e-3) / 1e9}
     return out
+
+
+def bench_backward(ssm, inp, w, stream, reps: int = 5):
+    """ssm_scan_bwd on the same workload (dy and dh_last seeded), timed like
+    the headline (CUDA events on the launching stream, best of `reps`).
+    Algorithmic bytes: u, delta, z, dy read and du, ddelta, dz written (input
+    dtype), B, C read and dB, dC written (float32 outputs), the per-channel
+    parameters and dA."""
+    import torch
+    from selective_state_space_113_b300 import workloads as wl
+    dev = inp["u"].device
+    dy, dh = wl.grad_inputs(w.batch, w.L, w.D, w.N, w.dtype, w.seed + 500, dev)
+    u = inp["u"]
+    du, ddelta, dz = torch.empty_like(u), torch.empty_like(u), torch.empty_like(u)
+    dB = torch.empty((w.batch, w.L, w.N), device=dev)
+    dC = torch.empty_like(dB)
+    dA = torch.empty((w.D, w.N), device=dev)
+    ddt_bias, dDskip = torch.empty(w.D, device=dev), torch.empty(w.D, device=dev)
+
+    def call():
+        ssm.ssm_scan_bwd(u, inp["delta"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                         inp["Dskip"], inp["z"], dy, dh, du, ddelta, ddt_bias, dA, dB, dC, dDskip,
+                         dz, stream=stream)
+    for _ in range(3):
+        call()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None or ms < best else best
+    es = 2 if "bf16" in w.name else 4
+    nbytes = (7 * es * w.elements + 2 * w.batch * w.L * w.N * (es + 4)
+              + w.D * w.N * 8 + w.batch * w.D * w.N * 4 + 6 * w.D * 4)
+    return {"ms": best, "elements_per_s": w.elements / (best * 1e-3),
+            "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (best * 1e-3) / 1e9,
+            "kernel_launches": 6 if w.L > 32 else 3,
+            "note": "one ssm_scan_bwd call: forward unit summaries + carry (state checkpoints "
+                    "every 32 steps), adjoint summaries + carry, the unit kernel, the dB/dC "
+                    "reduction; best of %d" % reps}
 
 
 def launches_per_call(w) -> int:

@@ -156,6 +156,42 @@ SSM_API int ssm_conv_scan_fwd(const void *x, const float *conv_w, const float *c
                               int64_t N, int dtype, void *stream);
 
 /*
+ * ssm_scan_bwd -- backward pass of ssm_scan_fwd (zero-order hold): the
+ * derivatives of a loss with respect to every input, given its derivatives
+ * dy with respect to y and dh_last with respect to h_last.  The states are
+ * recomputed from the inputs, never stored (ta-paperlens page, "代償と、
+ * それを払う方法（並列スキャン）": the fused kernel recomputes instead of
+ * keeping the intermediate states for the backward pass).
+ *
+ *   inputs      : u, delta, dt_bias, A, B, C, Dskip, z exactly as given to
+ *                 ssm_scan_fwd (same layouts, same NULL meanings)
+ *   dy          : [batch, L, D] dtype
+ *   dh_last     : [batch, D, N] float32, NULL means 0
+ *   du, ddelta  : [batch, L, D] dtype, written
+ *   dz          : [batch, L, D] dtype, written; required when z is given,
+ *                 ignored when z is NULL
+ *   dB, dC      : [batch, L, N] float32, written (sums over channels);
+ *                 NULL: not computed
+ *   dA          : [D, N] float32, written (sum over batch and steps)
+ *   ddt_bias, dDskip : [D] float32, written (sums over batch and steps);
+ *                 NULL: not computed
+ * Sizes as for ssm_scan_fwd.  With L == 0 or batch == 0 the sums are zero.
+ * Takes a stream-ordered workspace (SSM_ERR_NOMEM if that fails): about
+ * 3.2 * batch * L * D * N bytes / 16 for N == 16 (the states entering every
+ * 32-step unit, the adjoints leaving it and their summaries), plus
+ * 128 * ceil(D / 128) * batch * L bytes of per-block dB/dC sums.  The sums
+ * over channels, batch and steps are formed in float32 (dA, dDskip and
+ * ddt_bias with atomic adds, so their last bits can vary between calls).
+ * Returns an ssm_status_t.
+ */
+SSM_API int ssm_scan_bwd(const void *u, const void *delta, const float *dt_bias, const float *A,
+                         const void *B, const void *C, const float *Dskip, const void *z,
+                         const void *dy, const float *dh_last, void *du, void *ddelta,
+                         float *ddt_bias, float *dA, float *dB, float *dC, float *dDskip,
+                         void *dz, int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                         void *stream);
+
+/*
  * ssm_step -- one decode token: the same per-token update as one step of
  * ssm_scan_fwd, applied in place to a stored state (the recurrent,
  * constant-cost inference form; ta-paperlens page, S4 section).

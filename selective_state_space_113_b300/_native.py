@@ -20,8 +20,8 @@ SSM_F32, SSM_BF16 = 0, 1
 STATUS = {0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_SIZE", -3: "SSM_ERR_DTYPE",
           -4: "SSM_ERR_ALIGN", -5: "SSM_ERR_UNSUPPORTED", -6: "SSM_ERR_CUDA",
           -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT", -9: "SSM_ERR_SCRATCH"}
-EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_fwd_noalloc",
-           "ssm_step",
+EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd",
+           "ssm_scan_fwd_noalloc", "ssm_step",
            "ssm_device_status", "ssm_status_string", "ssm_abi_version")
 SSM_DISC_ZOH, SSM_DISC_EULER, SSM_DISC_TRAPEZOID = 0, 1, 2
 
@@ -44,6 +44,8 @@ def _load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_disc.argtypes = [vp] * 10 + [i64] * 4 + [ci, ci, vp]
     lib.ssm_conv_scan_fwd.restype = ci
     lib.ssm_conv_scan_fwd.argtypes = [vp] * 3 + [ci] + [vp] * 9 + [i64] * 4 + [ci, vp]
+    lib.ssm_scan_bwd.restype = ci
+    lib.ssm_scan_bwd.argtypes = [vp] * 18 + [i64] * 4 + [ci, vp]
     lib.ssm_scan_fwd_noalloc.restype = ci
     lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [i64] * 4 + [ci, vp]
     lib.ssm_step.restype = ci
@@ -127,6 +129,18 @@ def ssm_conv_scan_fwd(x, conv_w, conv_b, act, delta, dt_bias, A, B, C, Dskip, z,
                                  _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip), _p(z), _p(y),
                                  _p(h_last), batch, L, D, N, _dtype_code(x), _stream(stream)),
            "ssm_conv_scan_fwd")
+
+
+def ssm_scan_bwd(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last, du, ddelta, ddt_bias, dA,
+                 dB, dC, dDskip, dz, stream=None) -> None:
+    """Backward pass of ssm_scan_fwd: writes du, ddelta, dz (input dtype) and
+    dB, dC, dA, ddt_bias, dDskip (float32) from dy (and dh_last, or None)."""
+    batch, L, D = u.shape
+    N = A.shape[-1]
+    _check(lib.ssm_scan_bwd(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip), _p(z),
+                            _p(dy), _p(dh_last), _p(du), _p(ddelta), _p(ddt_bias), _p(dA), _p(dB),
+                            _p(dC), _p(dDskip), _p(dz), batch, L, D, N, _dtype_code(u),
+                            _stream(stream)), "ssm_scan_bwd")
 
 
 def ssm_scan_fwd_noalloc(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, stream=None) -> None:

@@ -12,6 +12,8 @@
 
 #include "common.cuh"
 #include "scan_tile_host.cuh"
+#include "scan_bwd_generic.cuh"
+#include "scan_bwd_host.cuh"
 #include "scan_generic.cuh"
 #include "step_fast.cuh"
 #include "step_generic.cuh"
@@ -170,6 +172,80 @@ extern "C" int ssm_conv_scan_fwd(const void* x, const float* conv_w, const float
     if (D > 0 && !conv_w) return SSM_ERR_NULL;
     return scan_impl(x, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
                      SSM_DISC_ZOH, stream_, ConvArgs{D > 0 ? conv_w : nullptr, conv_b, act});
+}
+
+extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bias,
+                            const float* A, const void* B, const void* C, const float* Dskip,
+                            const void* z, const void* dy, const float* dh_last, void* du,
+                            void* ddelta, float* ddt_bias, float* dA, float* dB, float* dC,
+                            float* dDskip, void* dz, int64_t batch, int64_t L, int64_t D,
+                            int64_t N, int dtype, void* stream_) {
+    if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
+    if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    int64_t bl, bld, bln, bd, bdn, dn;
+    if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) ||
+        !mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || !mul_ok(D, N, &dn) ||
+        bld > (INT64_MAX >> 5) || bln > (INT64_MAX >> 5) || bdn > (INT64_MAX >> 5))
+        return SSM_ERR_SIZE;
+    if ((bld && (!u || !delta || !dy || !du || !ddelta || (z && !dz))) || (bln && (!B || !C)) ||
+        (dn && (!A || !dA)))
+        return SSM_ERR_NULL;
+    if (!elems_aligned(dtype, {u, delta, B, C, z, dy, du, ddelta, dz},
+                       {dt_bias, A, Dskip, dh_last, ddt_bias, dA, dB, dC, dDskip}))
+        return SSM_ERR_ALIGN;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    // Sums start from zero: with no step or no channel they stay zero.
+    if (dn && cudaMemsetAsync(dA, 0, sizeof(float) * dn, stream) != cudaSuccess) return SSM_ERR_CUDA;
+    if (D && dDskip && cudaMemsetAsync(dDskip, 0, sizeof(float) * D, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (D && ddt_bias && cudaMemsetAsync(ddt_bias, 0, sizeof(float) * D, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (bln && dB && cudaMemsetAsync(dB, 0, sizeof(float) * bln, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (bln && dC && cudaMemsetAsync(dC, 0, sizeof(float) * bln, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (bd == 0 || L == 0) return SSM_OK;
+    const int plan = ssm::tile::forced_plan();
+    if (N == ssm::bwd::NS && plan != ssm::tile::kPlanGeneric &&
+        all_aligned16({u, delta, z, B, C, A, du}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
+        if (dtype == SSM_F32)
+            return ssm::bwd::launch_scan_bwd16<float>(
+                static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+                static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+                static_cast<const float*>(z), static_cast<const float*>(dy), dh_last,
+                static_cast<float*>(du), static_cast<float*>(ddelta), ddt_bias, dA, dB, dC,
+                dDskip, static_cast<float*>(dz), batch, L, D, stream);
+        return ssm::bwd::launch_scan_bwd16<bf16>(
+            static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+            static_cast<const bf16*>(z), static_cast<const bf16*>(dy), dh_last,
+            static_cast<bf16*>(du), static_cast<bf16*>(ddelta), ddt_bias, dA, dB, dC, dDskip,
+            static_cast<bf16*>(dz), batch, L, D, stream);
+    }
+    float* scratch = nullptr;
+    const size_t bytes = sizeof(float) * ssm::bwdg::bwd_generic_scratch_floats(batch, L, D, N);
+    if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_NOMEM;
+    }
+    cudaError_t e;
+    if (dtype == SSM_F32)
+        e = ssm::bwdg::launch_scan_bwd_generic<float>(
+            static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
+            static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+            static_cast<const float*>(z), static_cast<const float*>(dy), dh_last,
+            static_cast<float*>(du), static_cast<float*>(ddelta), ddt_bias, dA, dB, dC, dDskip,
+            static_cast<float*>(dz), scratch, batch, L, D, (int)N, stream);
+    else
+        e = ssm::bwdg::launch_scan_bwd_generic<bf16>(
+            static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
+            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+            static_cast<const bf16*>(z), static_cast<const bf16*>(dy), dh_last,
+            static_cast<bf16*>(du), static_cast<bf16*>(ddelta), ddt_bias, dA, dB, dC, dDskip,
+            static_cast<bf16*>(dz), scratch, batch, L, D, (int)N, stream);
+    const cudaError_t ef = cudaFreeAsync(scratch, stream);
+    return from_cuda(e != cudaSuccess ? e : ef);
 }
 
 extern "C" int ssm_step(float* state, const void* u, const void* delta, const float* dt_bias,

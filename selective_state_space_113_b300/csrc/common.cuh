@@ -25,6 +25,16 @@ __device__ __forceinline__ float softplus_ref(float v) {
 // SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)); tends to -0 as z -> -inf.
 __device__ __forceinline__ float silu_ref(float z) { return z / (1.0f + expf(-z)); }
 
+// exp(x) - 1 given ex = 2^(x log2 e) (an approximate exp(x)): below |x| =
+// 1/32 a degree-4 Taylor polynomial (truncation below 1e-9 relative), since
+// ex - 1 there keeps only the few bits of x that survive the rounding of ex
+// to a number near 1; elsewhere ex - 1, which loses no significant digits.
+__device__ __forceinline__ float em1_near0(float x, float ex) {
+    if (fabsf(x) < 0.03125f)
+        return x * fmaf(x, fmaf(x, fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+    return ex - 1.0f;
+}
+
 // Device-wide error word (one per device that loads the library).  Bounded
 // waits that give up OR their code in; ssm_device_status() reads and clears it.
 // The library is one translation unit (api.cu includes every kernel file), so

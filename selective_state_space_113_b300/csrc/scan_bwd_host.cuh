@@ -1,0 +1,162 @@
+// scan_bwd_host.cuh -- workspace and launches of the N == 16 backward pass
+// (scan_bwd.cuh): the forward unit summaries and carry for the states entering
+// every unit, the adjoint summaries and their carry, the unit kernel and the
+// dB/dC reduction, all on one stream.
+#pragma once
+
+#include "scan_bwd.cuh"
+#include "scan_tile_host.cuh"
+
+namespace ssm {
+namespace bwd {
+
+inline size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// CTAs of a kernel resident per SM, set up once per device (shared-memory
+// limit raised first where the kernel needs more than 48 KiB).
+template <typename K>
+inline cudaError_t resident(K kern, int threads, int smem, int* per_sm) {
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, threads, smem);
+}
+
+// Returns an ssm_status_t.  Preconditions (checked by the caller): N == 16;
+// u, delta, z, B, C, A and du 16-byte aligned; D * sizeof(T) % 16 == 0;
+// batch*D > 0; L > 0; dz given when z is.
+template <typename T>
+int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const float* A,
+                      const T* Bm, const T* Cm, const float* Dskip, const T* z, const T* dy,
+                      const float* dh_last, T* du, T* ddelta, float* ddt_bias, float* dA,
+                      float* dB, float* dC, float* dDskip, T* dz, long long batch, long long L,
+                      long long D, cudaStream_t stream) {
+    using namespace tile;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    long long wa = 0;
+    if (prepare<T, (int)kAggregate, (int)kZOH>(sms, &wa) != cudaSuccess || wa < 1)
+        return SSM_ERR_CUDA;
+    int occ_sum = 0, occ_unit = 0;
+    if (resident(adjoint_summary_kernel<T>, CB, 0, &occ_sum) != cudaSuccess ||
+        resident(bwd_unit_kernel<T>, CB, (int)sizeof(BwdSmem), &occ_unit) != cudaSuccess ||
+        occ_sum < 1 || occ_unit < 1)
+        return SSM_ERR_CUDA;
+
+    const long long P = cdiv(L, TU);
+    const long long nch = batch * D;
+    const long long nCB = cdiv(D, CB);
+    const size_t head = header_bytes(batch, D);
+    size_t off = head;
+    const size_t off_agg = off;
+    off = round256(off + (size_t)(P > 1 ? P - 1 : 0) * nch * (NS + 1) * 4);
+    const size_t off_hin = off;
+    off = round256(off + (size_t)P * nch * NS * 4);
+    const size_t off_adj = off;
+    off = round256(off + (size_t)P * nch * (NS + 1) * 4);
+    const size_t off_mu = off;
+    off = round256(off + (size_t)P * nch * NS * 4);
+    const size_t off_part = off;
+    off = round256(off + (size_t)nCB * batch * L * 32 * 4);
+
+    unsigned char* ws = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), off, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_NOMEM;
+    }
+    int status = SSM_OK;
+    do {
+        if (cudaMemsetAsync(ws, 0, head, stream) != cudaSuccess ||
+            cudaMemsetAsync(dA, 0, (size_t)D * NS * 4, stream) != cudaSuccess ||
+            (dDskip && cudaMemsetAsync(dDskip, 0, (size_t)D * 4, stream) != cudaSuccess) ||
+            (ddt_bias && cudaMemsetAsync(ddt_bias, 0, (size_t)D * 4, stream) != cudaSuccess)) {
+            status = SSM_ERR_CUDA;
+            break;
+        }
+        float* hin = reinterpret_cast<float*>(ws + off_hin);
+        // 1. the states entering every unit (unit 0 starts from zero)
+        if (P > 1) {
+            CUtensorMap maps[6];
+            Params p;
+            if (!setup<T>(maps, &p, u, delta, dt_bias, A, Bm, Cm, Dskip, z, du, nullptr, batch,
+                          L, D)) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
+            p.T = TU;
+            p.P = P;
+            p.agg = reinterpret_cast<float*>(ws + off_agg);
+            p.ticket = reinterpret_cast<unsigned long long*>(ws);
+            p.abort = reinterpret_cast<unsigned*>(ws + 32);
+            p.flags = reinterpret_cast<unsigned*>(ws + 256);
+            p.total_units = p.nchains * (P - 1);
+            if (launch_mode<T, (int)kAggregate, (int)kZOH>(p.total_units < wa ? p.total_units : wa,
+                                                          maps, p, stream) != cudaSuccess) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
+            carry_kernel<<<(unsigned)cdiv(nch * NS, 256), 256, 0, stream>>>(p.agg, A, hin, batch, D, P);
+            if (cudaGetLastError() != cudaSuccess) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
+        }
+        BwdParams bp{};
+        bp.u = u;
+        bp.delta = delta;
+        bp.z = z;
+        bp.dy = dy;
+        bp.Bm = Bm;
+        bp.Cm = Cm;
+        bp.dt_bias = dt_bias;
+        bp.A = A;
+        bp.Dskip = Dskip;
+        bp.dh_last = dh_last;
+        bp.du = du;
+        bp.ddelta = ddelta;
+        bp.dz = dz;
+        bp.ddt_bias = ddt_bias;
+        bp.dA = dA;
+        bp.dDskip = dDskip;
+        bp.part = reinterpret_cast<float*>(ws + off_part);
+        bp.hin = hin;
+        bp.adj = reinterpret_cast<float*>(ws + off_adj);
+        bp.mu = reinterpret_cast<float*>(ws + off_mu);
+        bp.batch = batch;
+        bp.L = L;
+        bp.D = D;
+        bp.P = P;
+        bp.nCB = nCB;
+        bp.units = nCB * batch * P;
+        // 2. adjoint summaries of units 1..P-1, then the adjoint entering each unit
+        if (P > 1) {
+            const long long nsum = nCB * batch * (P - 1);
+            const long long g = (long long)sms * occ_sum;
+            adjoint_summary_kernel<T><<<(unsigned)(nsum < g ? nsum : g), CB, 0, stream>>>(bp);
+            if (cudaGetLastError() != cudaSuccess) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
+        }
+        adj_carry_kernel<<<(unsigned)cdiv(nch * NS, 256), 256, 0, stream>>>(bp.adj, A, dh_last,
+                                                                           bp.mu, batch, D, P);
+        // 3. the unit kernel
+        {
+            const long long g = (long long)sms * occ_unit;
+            bwd_unit_kernel<T><<<(unsigned)(bp.units < g ? bp.units : g), CB, sizeof(BwdSmem),
+                                 stream>>>(bp);
+        }
+        // 4. dB and dC
+        bwd_reduce_bc_kernel<<<(unsigned)cdiv(batch * L * 32, 256), 256, 0, stream>>>(
+            bp.part, dB, dC, batch * L, nCB);
+        if (cudaGetLastError() != cudaSuccess) status = SSM_ERR_CUDA;
+    } while (0);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && status == SSM_OK) status = SSM_ERR_CUDA;
+    return status;
+}
+
+}  // namespace bwd
+}  // namespace ssm

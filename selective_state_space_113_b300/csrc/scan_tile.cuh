@@ -44,8 +44,9 @@
 // Per-step arithmetic (geometric A, A[d,n] = (n+1) a0, detected per warp):
 //   v2 = delta*log2(e) + dt_bias*log2(e);  x = 2^v2 = e^(delta+bias)
 //   dl = log2(1 + x)                          (dt = dl * ln2 = softplus)
-//   r  = 2^(dl a0) = exp(dt a0);  e_n = r^(n+1) - 1 = exp(dt A[d,n]) - 1
-//        e_0 = r - 1, e_1 = r e_0 + e_0, e_(n+2) = r^2 e_n + e_1
+//   e_0 = exp(dt a0) - 1 (from 2^(dl a0), or its Taylor polynomial where
+//         |dt a0| < 1/32);  r = e_0 + 1;  e_n = r^(n+1) - 1 = exp(dt A[d,n]) - 1
+//        e_1 = r e_0 + e_0, e_(n+2) = r^2 e_n + e_1
 //   h_n <- h_n + e_n (h_n + B_n u / A[d,n])  (= A_bar h + (A_bar - 1)/A B u)
 //   y  = (sum_n C_n h_n + Dskip u) * z / (1 + 2^(-z log2(e)))
 // B_n/(n+1) is prepared once per stage by the helpers, and u/a0 once per
@@ -346,9 +347,9 @@ __device__ int fill_header(unsigned char* st, const Params& p, long long b, long
 // Per-step values of KP consecutive steps of the helper's 32 channels, with
 // g = z sigmoid(z) (1 without z), sug = Dskip u g, dt = dl ln 2:
 //                       geometric A                  other A
-//   kZOH              {r = exp(dt a0), u/a0, g, sug}  {dl, u, g, sug}
-//   kEuler            {r, dt u, g, sug}               {dl, u, g, sug}
-//   kTrap             {r, dt/2, u, g}                 {dl, u, g, sug}
+//   kZOH              {e0 = exp(dt a0) - 1, u/a0, g, sug}  {dl, u, g, sug}
+//   kEuler            {e0, dt u, g, sug}                   {dl, u, g, sug}
+//   kTrap             {e0, dt/2, u, g}                     {dl, u, g, sug}
 //   kAggregate mode   the same .x/.y (kTrap: .x/.y/.z), .w = dl
 // Per-lane state of the convolution (CONV): weights, bias, the last three x.
 struct ConvState {
@@ -395,7 +396,7 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
         }
         const float sug = cp.dsk * u * g;
         if (geo) {
-            o[j].x = ptx::ex2(dl * cp.a0);
+            o[j].x = em1_near0(dl * cp.a0 * kLn2, ptx::ex2(dl * cp.a0));   // e_0
             if (DISC == kZOH) o[j].y = u * cp.ia0;
             else if (DISC == kEuler) o[j].y = dl * kLn2 * u;
             else o[j].y = dl * (0.5f * kLn2);
@@ -437,8 +438,8 @@ __device__ __forceinline__ void steps_geo(const unsigned char* st, int row0, int
         const float4 pv = pro[j * CW];
         const float4* B4 = reinterpret_cast<const float4*>(Bc + t * NS);
         const float4* C4 = reinterpret_cast<const float4*>(Cc + t * NS);
-        const float r = pv.x;
-        const float e0 = r - 1.0f;                  // exp(dt A_0) - 1
+        const float e0 = pv.x;                      // exp(dt A_0) - 1
+        const float r = e0 + 1.0f;
         const float e1 = fmaf(r, e0, e0);           // exp(dt A_1) - 1
         const float r2 = e1 + 1.0f;
         const float2 R2 = make_float2(r2, r2), E1 = make_float2(e1, e1);
@@ -522,7 +523,7 @@ __device__ __forceinline__ void steps_general(const unsigned char* st, int row0,
 #pragma unroll
         for (int n = 0; n < NS; ++n) {
             const float a = __ldg(Arow + n);
-            const float e = ptx::ex2(dl * a) - 1.0f;
+            const float e = em1_near0(dl * a * kLn2, ptx::ex2(dl * a));
             float hn = (n & 1) ? H[n / 2].y : H[n / 2].x;
             if (DISC == kZOH) {
                 const float coef = (a != 0.0f) ? e / a : dt;

@@ -17,6 +17,9 @@ workload definitions fix):
   conv_w, conv_b ~ U(-1/2, 1/2)  [D, 4], [D]  float32 (the default init of a
                 depthwise width-4 Conv1d, bound 1/sqrt(fan_in) = 1/2), drawn
                 by ``conv_params`` from a generator of their own
+  backward: dy ~ N(0, 1) [batch, L, D] (workload dtype), dh_last ~ N(0, 1)
+                [batch, D, N] float32, by ``grad_inputs`` from a generator of
+                their own
 Draws happen in float32 from one torch.Generator seeded with the workload's
 seed, in the order listed, then are rounded to bf16 where the workload is bf16.
 The time-invariant variant repeats the t = 0 draws of delta, B and C along t.
@@ -138,6 +141,16 @@ def conv_params(D: int, seed: int, device="cpu"):
     w = (torch.rand((D, 4), generator=g, device=device) - 0.5).contiguous()
     b = torch.rand(D, generator=g, device=device) - 0.5
     return w, b
+
+
+def grad_inputs(batch: int, L: int, D: int, N: int, dtype, seed: int, device="cpu"):
+    """Upstream derivatives for the backward pass: dy [batch, L, D] ~ N(0, 1)
+    in the workload dtype and dh_last [batch, D, N] ~ N(0, 1) float32, from a
+    generator of their own."""
+    g = _gen(seed, device)
+    dy = _randn((batch, L, D), g, device, dtype)
+    dh = torch.randn((batch, D, N), generator=g, device=device, dtype=torch.float32)
+    return dy, dh
 
 
 def make_step_inputs(w: StepWorkload, device="cpu", seed: int | None = None,

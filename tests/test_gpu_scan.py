@@ -167,3 +167,20 @@ def test_fp32_mamba_shape_sampled():
     """float32 inputs at a Mamba-130M-like shape (multi-tile, long L)."""
     inp = wl.make_scan_inputs(wl.TINY_F32, device=DEV, batch=2, L=2048, D=512, seed=31)
     sampled_parity(inp, "f32 2x2048x512", 32)
+
+
+@pytest.mark.parametrize("plan", [None, "narrow"])
+def test_small_dt_times_a_f32(monkeypatch, plan):
+    """fp32 inputs with |dt A| far below 1: geometric rows with a tiny a0,
+    non-geometric tiny rows, and ordinary rows, all at the fp32 tolerance.
+    exp(dt A) - 1 must not be formed by subtracting 1 from a number near 1
+    there (a few surviving bits), on either path of the kernel."""
+    if plan:
+        monkeypatch.setenv("SSM_FORCE_PLAN", plan)
+        monkeypatch.setenv("SSM_CHUNK_T", "64")
+    inp = wl.make_scan_inputs(wl.TINY_F32, device="cuda", batch=2, L=300, D=64, seed=17)
+    n1 = torch.arange(1, 17, device="cuda", dtype=torch.float32)
+    inp["A"][0:16] = -1e-4 * n1                    # geometric, tiny a0
+    inp["A"][16:32] = -1e-4                        # not geometric, tiny
+    inp["A"][32:48] = -3e-3 * n1                   # geometric, small
+    full_parity(inp, f"small dt*A plan={plan}")
