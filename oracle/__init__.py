@@ -267,6 +267,34 @@ def scan_bwd(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last=None, dtype: int 
                 dDskip=dDskip)
 
 
+def ssd_fwd(x, dt, dt_bias, A, B, C, Dskip, dtype: int = F32, threads: int = 1,
+            lib: ctypes.CDLL | None = None):
+    """The Mamba-2 form of the scan (structured state-space duality), float64:
+    one scalar A per head, the input term dt B x (Euler), head dimension P.
+
+    x [Bt,L,H,P], dt [Bt,L,H] (before softplus), B/C [Bt,L,N] (input dtype);
+    dt_bias [H], A [H], Dskip [H] (float32, dt_bias/Dskip may be None).
+    For channel (h, p) this is exactly the Euler scan with A[d, n] = A[h] for
+    every n, delta[b, t, d] = dt[b, t, h], dt_bias[d] = dt_bias[h] and
+    Dskip[d] = Dskip[h], without a gate; the oracle is that scan, on channels
+    numbered d = h P + p.  Returns (y [Bt,L,H,P], h_last [Bt,H,P,N]).
+    """
+    x = np.ascontiguousarray(x)
+    dt = np.ascontiguousarray(dt)
+    batch, L, H, P = x.shape
+    N = B.shape[-1]
+    if dt.shape != (batch, L, H) or B.shape != (batch, L, N) or C.shape != (batch, L, N):
+        raise ValueError("inconsistent shapes")
+    u = x.reshape(batch, L, H * P)
+    delta = np.ascontiguousarray(np.repeat(dt, P, axis=2))
+    Ad = np.ascontiguousarray(np.repeat(np.asarray(A, np.float32), P)[:, None] * np.ones(N, np.float32))
+    bias = None if dt_bias is None else np.repeat(np.asarray(dt_bias, np.float32), P)
+    skip = None if Dskip is None else np.repeat(np.asarray(Dskip, np.float32), P)
+    y, h = scan_fwd_disc(u, delta, bias, Ad, B, C, skip, None, EULER, dtype=dtype,
+                         threads=threads, lib=lib)
+    return y.reshape(batch, L, H, P), h.reshape(batch, H, P, N)
+
+
 def step(state, u, delta, dt_bias, A, B, C, Dskip, z, dtype: int = F32,
          lib: ctypes.CDLL | None = None):
     """One decode step, float64.  state [Bt,D,N] (copied), u/delta/z [Bt,D], B/C [Bt,N].

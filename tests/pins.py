@@ -709,3 +709,78 @@ def pin_bwd_optional_inputs(lib):
 
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_homogeneity, pin_bwd_matches_autograd,
             pin_bwd_optional_inputs]
+
+
+# ------------------------------------------------------ SSD (Mamba-2) pins
+def _ssd_problem(rng, batch=2, L=24, H=3, P=4, N=8):
+    x = _f32(rng.standard_normal((batch, L, H, P)))
+    dt = _f32(rng.standard_normal((batch, L, H)))
+    dt_bias = _f32(np.log(np.expm1(np.exp(rng.uniform(np.log(1e-2), np.log(0.5), H)))))
+    A = _f32(-(0.1 + 2.0 * rng.random(H)))
+    B = _f32(rng.standard_normal((batch, L, N)))
+    C = _f32(rng.standard_normal((batch, L, N)))
+    Dskip = _f32(rng.standard_normal(H))
+    return dict(x=x, dt=dt, dt_bias=dt_bias, A=A, B=B, C=C, Dskip=Dskip)
+
+
+def _ssd_run(ssd, lib, p):
+    return ssd(p["x"], p["dt"], p["dt_bias"], p["A"], p["B"], p["C"], p["Dskip"], lib=lib)
+
+
+def pin_ssd_masked_matmul(lib, ssd=oracle.ssd_fwd):
+    """The pages' duality statement written out: per head, y = (L o C B^T) X
+    with the decay mask L[t, s] = exp(a sum_{r=s+1..t} dt_r) dt_s for s <= t
+    (0 above the diagonal), plus D x; the final state is
+    sum_s exp(a sum_{r>s} dt_r) dt_s B_s^T x_s.  numpy matmuls, float64."""
+    rng = np.random.default_rng(21)
+    p = _ssd_problem(rng)
+    y, h = _ssd_run(ssd, lib, p)
+    batch, L, H, P = p["x"].shape
+    for b in range(batch):
+        CB = p["C"][b].astype(np.float64) @ p["B"][b].astype(np.float64).T      # [t, s]
+        for hh in range(H):
+            dt = softplus_ref(p["dt"][b, :, hh].astype(np.float64) + float(p["dt_bias"][hh]))
+            cum = np.cumsum(dt) * float(p["A"][hh])                              # a sum_{r<=t} dt
+            seg = np.exp(np.tril(cum[:, None] - cum[None, :]))                    # exp(a sum_{s<r<=t})
+            mask = np.tril(seg * dt[None, :])
+            xh = p["x"][b, :, hh, :].astype(np.float64)
+            want = (mask * CB) @ xh + float(p["Dskip"][hh]) * xh
+            _close(y[b, :, hh, :], want, 1e-10, 1e-10, f"SSD masked matmul b={b} h={hh}")
+            wlast = np.exp(cum[-1] - cum) * dt                                     # [s]
+            hw = (p["B"][b].astype(np.float64) * wlast[:, None]).T @ xh          # [N, P]
+            _close(h[b, hh], hw.T, 1e-10, 1e-10, f"SSD final state b={b} h={hh}")
+
+
+def pin_ssd_chunked_form(lib, ssd=oracle.ssd_fwd):
+    """The chunked form of the duality (the one the tensor-core kernel uses):
+    within each chunk the masked matmul from a zero state, across chunks the
+    N x P state carried with the chunk's total decay and read out as
+    exp(a cum_t) C_t H.  Chunks of 7 steps over L = 24 (a ragged last chunk)."""
+    rng = np.random.default_rng(22)
+    p = _ssd_problem(rng)
+    y, h = _ssd_run(ssd, lib, p)
+    batch, L, H, P = p["x"].shape
+    N = p["B"].shape[-1]
+    Q = 7
+    for b in range(batch):
+        for hh in range(H):
+            a = float(p["A"][hh])
+            dt = softplus_ref(p["dt"][b, :, hh].astype(np.float64) + float(p["dt_bias"][hh]))
+            Hs = np.zeros((N, P))
+            for t0 in range(0, L, Q):
+                t1 = min(t0 + Q, L)
+                d = dt[t0:t1]
+                cum = np.cumsum(d) * a
+                Bc = p["B"][b, t0:t1].astype(np.float64)
+                Cc = p["C"][b, t0:t1].astype(np.float64)
+                xc = p["x"][b, t0:t1, hh, :].astype(np.float64)
+                mask = np.tril(np.exp(np.tril(cum[:, None] - cum[None, :])) * d[None, :])
+                yc = (mask * (Cc @ Bc.T)) @ xc + np.exp(cum)[:, None] * (Cc @ Hs) \
+                    + float(p["Dskip"][hh]) * xc
+                _close(y[b, t0:t1, hh, :], yc, 1e-10, 1e-10, f"SSD chunk t0={t0}")
+                w = np.exp(cum[-1] - cum) * d
+                Hs = np.exp(cum[-1]) * Hs + (Bc * w[:, None]).T @ xc
+            _close(h[b, hh], Hs.T, 1e-10, 1e-10, f"SSD chunked final state b={b} h={hh}")
+
+
+SSD_PINS = [pin_ssd_masked_matmul, pin_ssd_chunked_form]
