@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--workload", default="mamba2.8b", choices=sorted(WORKLOADS),
                     help="scan shape (default: the Mamba-2.8B layer; the others are the "
                          "smaller cases used for ncu captures)")
@@ -261,6 +262,9 @@ def bench_ours(args, rank, world, local):
     backward = None
     if not args.no_backward:
         backward = bench_backward(ssm, inp, w, stream)
+    ssd = None
+    if not args.no_ssd:
+        ssd = bench_ssd(ssm, dev, stream)
     decode = None
     if not args.no_decode:
         decode = bench_decode(ssm, dev, stream)
@@ -301,6 +305,7 @@ def bench_ours(args, rank, world, local):
                          "frac": achieved_gbs / peak, "peak_source": peak_kind},
         "clocks": clocks.summary(),
         "backward": backward,
+        "ssd": ssd,
         "decode": decode,
         "discretisation_variants": variants,
         "e2e": e2e,
@@ -459,6 +464,45 @@ def bench_backward(ssm, inp, w, stream, reps: int = 5):
             "note": "one ssm_scan_bwd call: forward unit summaries + carry (state checkpoints "
                     "every 32 steps), adjoint summaries + carry, the unit kernel, the dB/dC "
                     "reduction; best of %d" % reps}
+
+
+def bench_ssd(ssm, dev, stream, reps: int = 5):
+    """ssm_ssd_fwd (the Mamba-2 form) on a Mamba-2 2.7B-shaped layer (4 x 4096,
+    80 heads of 64, N = 128, bf16): one tensor-core launch per call, timed
+    like the headline.  Algorithmic FLOPs are those of the chunked form's four
+    dense products per 64-step chunk (C B^T, scores X, C H, (B w)^T X), with
+    no credit for the causal half the kernel skips."""
+    import torch
+    from selective_state_space_113_b300 import workloads as wl
+    w = wl.SSD_2P7B
+    inp = wl.make_ssd_inputs(w, device=dev)
+    y = torch.empty_like(inp["x"])
+    h = torch.empty((w.batch, w.H, w.P, w.N), device=dev)
+
+    def call():
+        ssm.ssm_ssd_fwd(inp["x"], inp["dt"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                        inp["Dskip"], y, h, stream=stream)
+    for _ in range(3):
+        call()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None or ms < best else best
+    Q = 64
+    chunks = w.batch * w.H * ((w.L + Q - 1) // Q)
+    flops = chunks * 2 * (Q * Q * w.N + Q * Q * w.P + 2 * Q * w.N * w.P)
+    nbytes = 2 * w.elements * 2 + w.batch * w.L * w.H * 2 + 2 * w.batch * w.L * w.N * 2 \
+        + w.batch * w.H * w.P * w.N * 4
+    return {"workload": w.name, "ms": best, "elements_per_s": w.elements / (best * 1e-3),
+            "algorithmic_flops": flops, "tflops": flops / (best * 1e-3) / 1e12,
+            "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (best * 1e-3) / 1e9,
+            "tensor_path": "mma.sync m16n8k16 bf16 -> fp32",
+            "note": "best of %d; one launch per call" % reps}
 
 
 def launches_per_call(w) -> int:

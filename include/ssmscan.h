@@ -192,6 +192,32 @@ SSM_API int ssm_scan_bwd(const void *u, const void *delta, const float *dt_bias,
                          void *stream);
 
 /*
+ * ssm_ssd_fwd -- the Mamba-2 form of the scan (structured state-space
+ * duality; news.han.ihouse.idv.tw article 1304: most of the SSM computation is
+ * a masked matrix multiplication, A is a scalar, Euler discretisation):
+ * per batch b, head h, channel p < P of the head, state n < N,
+ *   dt_t   = softplus(dt[b,t,h] + dt_bias[h])
+ *   h_t[n] = exp(dt_t A[h]) h_{t-1}[n] + dt_t B[b,t,n] x[b,t,h,p],   from 0
+ *   y[b,t,h,p] = sum_n C[b,t,n] h_t[n] + Dskip[h] x[b,t,h,p]
+ *
+ *   x, y        : [batch, L, H, P] dtype
+ *   dt          : [batch, L, H] dtype (before the softplus)
+ *   B, C        : [batch, L, N] dtype (one group shared by all heads)
+ *   dt_bias     : [H] float32 (NULL means 0);  A : [H] float32
+ *   Dskip       : [H] float32 (NULL means 0)
+ *   h_last      : [batch, H, P, N] float32, written (NULL: not written); the
+ *                 layout of ssm_step's state with D = H * P channels
+ * bf16 with P == 64, N == 64 or 128 and x, B, C, y 16-byte aligned runs the
+ * tensor-core chunked kernel (the products in bf16, every sum in fp32);
+ * anything else runs a one-thread-per-channel kernel.  Allocates nothing.
+ * Returns an ssm_status_t.
+ */
+SSM_API int ssm_ssd_fwd(const void *x, const void *dt, const float *dt_bias, const float *A,
+                        const void *B, const void *C, const float *Dskip, void *y, float *h_last,
+                        int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, int dtype,
+                        void *stream);
+
+/*
  * ssm_step -- one decode token: the same per-token update as one step of
  * ssm_scan_fwd, applied in place to a stored state (the recurrent,
  * constant-cost inference form; ta-paperlens page, S4 section).

@@ -21,7 +21,7 @@ STATUS = {0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_SIZE", -3: "SSM_ERR_DTYP
           -4: "SSM_ERR_ALIGN", -5: "SSM_ERR_UNSUPPORTED", -6: "SSM_ERR_CUDA",
           -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT", -9: "SSM_ERR_SCRATCH"}
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd",
-           "ssm_scan_fwd_noalloc", "ssm_step",
+           "ssm_ssd_fwd", "ssm_scan_fwd_noalloc", "ssm_step",
            "ssm_device_status", "ssm_status_string", "ssm_abi_version")
 SSM_DISC_ZOH, SSM_DISC_EULER, SSM_DISC_TRAPEZOID = 0, 1, 2
 
@@ -46,6 +46,8 @@ def _load() -> ctypes.CDLL:
     lib.ssm_conv_scan_fwd.argtypes = [vp] * 3 + [ci] + [vp] * 9 + [i64] * 4 + [ci, vp]
     lib.ssm_scan_bwd.restype = ci
     lib.ssm_scan_bwd.argtypes = [vp] * 18 + [i64] * 4 + [ci, vp]
+    lib.ssm_ssd_fwd.restype = ci
+    lib.ssm_ssd_fwd.argtypes = [vp] * 9 + [i64] * 5 + [ci, vp]
     lib.ssm_scan_fwd_noalloc.restype = ci
     lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [i64] * 4 + [ci, vp]
     lib.ssm_step.restype = ci
@@ -141,6 +143,16 @@ def ssm_scan_bwd(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last, du, ddelta, 
                             _p(dy), _p(dh_last), _p(du), _p(ddelta), _p(ddt_bias), _p(dA), _p(dB),
                             _p(dC), _p(dDskip), _p(dz), batch, L, D, N, _dtype_code(u),
                             _stream(stream)), "ssm_scan_bwd")
+
+
+def ssm_ssd_fwd(x, dt, dt_bias, A, B, C, Dskip, y, h_last, stream=None) -> None:
+    """y, h_last <- the Mamba-2 (SSD) scan: x [Bt,L,H,P], dt [Bt,L,H], A [H],
+    B/C [Bt,L,N]; h_last [Bt,H,P,N] float32 or None."""
+    batch, L, H, P = x.shape
+    N = B.shape[-1]
+    _check(lib.ssm_ssd_fwd(_p(x), _p(dt), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip), _p(y),
+                           _p(h_last), batch, L, H, P, N, _dtype_code(x), _stream(stream)),
+           "ssm_ssd_fwd")
 
 
 def ssm_scan_fwd_noalloc(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, stream=None) -> None:

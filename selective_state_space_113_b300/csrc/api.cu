@@ -15,6 +15,7 @@
 #include "scan_bwd_generic.cuh"
 #include "scan_bwd_host.cuh"
 #include "scan_generic.cuh"
+#include "ssd.cuh"
 #include "step_fast.cuh"
 #include "step_generic.cuh"
 
@@ -246,6 +247,52 @@ extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bi
             static_cast<bf16*>(dz), scratch, batch, L, D, (int)N, stream);
     const cudaError_t ef = cudaFreeAsync(scratch, stream);
     return from_cuda(e != cudaSuccess ? e : ef);
+}
+
+extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float* A,
+                           const void* B, const void* C, const float* Dskip, void* y,
+                           float* h_last, int64_t batch, int64_t L, int64_t H, int64_t P,
+                           int64_t N, int dtype, void* stream_) {
+    if (batch < 0 || L < 0 || H < 0 || P < 1 || N < 1) return SSM_ERR_SIZE;
+    if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    int64_t bl, blh, blhp, bln, bh, bhp, bhpn;
+    if (!mul_ok(batch, L, &bl) || !mul_ok(bl, H, &blh) || !mul_ok(blh, P, &blhp) ||
+        !mul_ok(bl, N, &bln) || !mul_ok(batch, H, &bh) || !mul_ok(bh, P, &bhp) ||
+        !mul_ok(bhp, N, &bhpn) || blhp > (INT64_MAX >> 4) || bhpn > (INT64_MAX >> 4))
+        return SSM_ERR_SIZE;
+    if ((blhp && (!x || !y)) || (blh && !dt) || (bln && (!B || !C)) || (H && !A))
+        return SSM_ERR_NULL;
+    if (!elems_aligned(dtype, {x, dt, B, C, y}, {dt_bias, A, Dskip, h_last})) return SSM_ERR_ALIGN;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (bhp == 0) return SSM_OK;
+    if (L == 0) {
+        if (h_last) return from_cuda(cudaMemsetAsync(h_last, 0, sizeof(float) * bhpn, stream));
+        return SSM_OK;
+    }
+    const bool tc = dtype == SSM_BF16 && P == ssm::ssd::P && (N == 64 || N == 128) &&
+                    all_aligned16({x, B, C, y}) && ssm::tile::forced_plan() != ssm::tile::kPlanGeneric;
+    cudaError_t e;
+    if (tc) {
+        const bf16 *xb = static_cast<const bf16*>(x), *db = static_cast<const bf16*>(dt),
+                   *Bb = static_cast<const bf16*>(B), *Cb = static_cast<const bf16*>(C);
+        bf16* yb = static_cast<bf16*>(y);
+        e = N == 64 ? ssm::ssd::launch_ssd_chunk<64>(xb, db, dt_bias, A, Bb, Cb, Dskip, yb, h_last,
+                                                    batch, L, H, stream)
+                    : ssm::ssd::launch_ssd_chunk<128>(xb, db, dt_bias, A, Bb, Cb, Dskip, yb,
+                                                     h_last, batch, L, H, stream);
+    } else if (dtype == SSM_F32) {
+        e = ssm::ssd::launch_ssd_generic<float>(
+            static_cast<const float*>(x), static_cast<const float*>(dt), dt_bias, A,
+            static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+            static_cast<float*>(y), h_last, batch, L, H, P, (int)N, stream);
+    } else {
+        e = ssm::ssd::launch_ssd_generic<bf16>(
+            static_cast<const bf16*>(x), static_cast<const bf16*>(dt), dt_bias, A,
+            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+            static_cast<bf16*>(y), h_last, batch, L, H, P, (int)N, stream);
+    }
+    return from_cuda(e);
 }
 
 extern "C" int ssm_step(float* state, const void* u, const void* delta, const float* dt_bias,

@@ -106,7 +106,7 @@ __device__ __forceinline__ float psi_of(float x, float em1) {
 // Per-channel constants of the unit.
 struct Chan {
     float a0, ia0, kb2, dsk;   // A[d,0], 1/A[d,0], dt_bias log2(e), Dskip
-    bool geo;                  // the warp's rows are all (n+1) a0 (a0 != 0)
+    bool geo;                  // the warp's rows are all (n+1) a0 with |a0| >= 1/16
 };
 
 __device__ __forceinline__ Chan load_chan(const BwdParams& p, long long d, bool valid,
@@ -122,7 +122,7 @@ __device__ __forceinline__ Chan load_chan(const BwdParams& p, long long d, bool 
         arow[4 * q + 2] = v.z;
         arow[4 * q + 3] = v.w;
     }
-    bool g = arow[0] != 0.0f && isfinite(arow[0]);
+    bool g = fabsf(arow[0]) >= 0.0625f && isfinite(arow[0]);
 #pragma unroll
     for (int n = 1; n < NS; ++n) g = g && (arow[n] == (float)(n + 1) * arow[0]);
     c.geo = __all_sync(0xffffffffu, g || !valid);

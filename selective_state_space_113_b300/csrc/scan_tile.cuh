@@ -44,9 +44,11 @@
 // Per-step arithmetic (geometric A, A[d,n] = (n+1) a0, detected per warp):
 //   v2 = delta*log2(e) + dt_bias*log2(e);  x = 2^v2 = e^(delta+bias)
 //   dl = log2(1 + x)                          (dt = dl * ln2 = softplus)
-//   e_0 = exp(dt a0) - 1 (from 2^(dl a0), or its Taylor polynomial where
-//         |dt a0| < 1/32);  r = e_0 + 1;  e_n = r^(n+1) - 1 = exp(dt A[d,n]) - 1
-//        e_1 = r e_0 + e_0, e_(n+2) = r^2 e_n + e_1
+//   r  = 2^(dl a0) = exp(dt a0);  e_n = r^(n+1) - 1 = exp(dt A[d,n]) - 1
+//        e_0 = r - 1, e_1 = r e_0 + e_0, e_(n+2) = r^2 e_n + e_1
+//   (r - 1 carries the SFU's absolute error, about 2^-22, so e_0 is good to
+//   about 2^-22 / |dt a0| relative; rows with |a0| < 1/16 therefore take the
+//   per-state path, which forms exp(x) - 1 from its Taylor polynomial near 0)
 //   h_n <- h_n + e_n (h_n + B_n u / A[d,n])  (= A_bar h + (A_bar - 1)/A B u)
 //   y  = (sum_n C_n h_n + Dskip u) * z / (1 + 2^(-z log2(e)))
 // B_n/(n+1) is prepared once per stage by the helpers, and u/a0 once per
@@ -286,7 +288,7 @@ __device__ int fill_header(unsigned char* st, const Params& p, long long b, long
         const float bias = p.dt_bias ? __ldg(p.dt_bias + ds) : 0.0f;
         const float dsk = p.Dskip ? __ldg(p.Dskip + ds) : 0.0f;
         const float a0 = av[0];
-        bool g = (a0 != 0.0f) && isfinite(a0);
+        bool g = fabsf(a0) >= 0.0625f && isfinite(a0);
 #pragma unroll
         for (int n = 1; n < NS; ++n) g = g && (av[n] == (float)(n + 1) * a0);
         if (__all_sync(0xffffffffu, g || !valid)) geo |= 1 << w;
@@ -347,9 +349,9 @@ __device__ int fill_header(unsigned char* st, const Params& p, long long b, long
 // Per-step values of KP consecutive steps of the helper's 32 channels, with
 // g = z sigmoid(z) (1 without z), sug = Dskip u g, dt = dl ln 2:
 //                       geometric A                  other A
-//   kZOH              {e0 = exp(dt a0) - 1, u/a0, g, sug}  {dl, u, g, sug}
-//   kEuler            {e0, dt u, g, sug}                   {dl, u, g, sug}
-//   kTrap             {e0, dt/2, u, g}                     {dl, u, g, sug}
+//   kZOH              {r = exp(dt a0), u/a0, g, sug}  {dl, u, g, sug}
+//   kEuler            {r, dt u, g, sug}               {dl, u, g, sug}
+//   kTrap             {r, dt/2, u, g}                 {dl, u, g, sug}
 //   kAggregate mode   the same .x/.y (kTrap: .x/.y/.z), .w = dl
 // Per-lane state of the convolution (CONV): weights, bias, the last three x.
 struct ConvState {
@@ -396,7 +398,7 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
         }
         const float sug = cp.dsk * u * g;
         if (geo) {
-            o[j].x = em1_near0(dl * cp.a0 * kLn2, ptx::ex2(dl * cp.a0));   // e_0
+            o[j].x = ptx::ex2(dl * cp.a0);   // r
             if (DISC == kZOH) o[j].y = u * cp.ia0;
             else if (DISC == kEuler) o[j].y = dl * kLn2 * u;
             else o[j].y = dl * (0.5f * kLn2);
@@ -438,8 +440,8 @@ __device__ __forceinline__ void steps_geo(const unsigned char* st, int row0, int
         const float4 pv = pro[j * CW];
         const float4* B4 = reinterpret_cast<const float4*>(Bc + t * NS);
         const float4* C4 = reinterpret_cast<const float4*>(Cc + t * NS);
-        const float e0 = pv.x;                      // exp(dt A_0) - 1
-        const float r = e0 + 1.0f;
+        const float r = pv.x;
+        const float e0 = r - 1.0f;                  // exp(dt A_0) - 1
         const float e1 = fmaf(r, e0, e0);           // exp(dt A_1) - 1
         const float r2 = e1 + 1.0f;
         const float2 R2 = make_float2(r2, r2), E1 = make_float2(e1, e1);

@@ -1,0 +1,383 @@
+// ssd.cuh -- the Mamba-2 form of the scan (structured state-space duality):
+// one scalar A per head, the input term dt B x, head dimension P, a state of
+// N per channel shared across the head's P channels through B and C.
+//
+// What it computes (news.han.ihouse.idv.tw article 1304: Mamba-2 found most
+// of the SSM's computation equal to a masked matrix multiplication, reduced A
+// to a scalar and supports a larger state; Mamba-2 discretises with Euler's
+// rule; ta-paperlens and ultralytics pages: Mamba-2's state-space duality),
+// per batch b, head h, channel p of the head, step t, state n:
+//   dt_t = softplus(dt[b,t,h] + dt_bias[h]);  h_t[n] = exp(dt_t A[h]) h_{t-1}[n]
+//          + dt_t B_t[n] x_t[p];   y_t[p] = sum_n C_t[n] h_t[n] + Dskip[h] x_t[p]
+// from h = 0.  The tensor-core kernel evaluates it in the chunked matrix form
+// (chunks of Q = 64 steps, cum_t = A sum_{r<=t in chunk} dt_r):
+//   y_chunk = (Lmask o C B^T) X + diag(exp(cum)) C H_in + Dskip X,
+//     Lmask[t, s] = exp(cum_t - cum_s) dt_s  for s <= t, 0 above the diagonal
+//   H_out = exp(cum_end) H_in + (B o w)^T X,   w_s = exp(cum_end - cum_s) dt_s
+// with H the N x P state of the head.  One CTA (4 warps) owns one (b, h) and
+// walks its chunks in order, the fp32 state in registers (warp w holds state
+// rows (N/4)w .. (N/4)(w+1)-1 as mma accumulators).  The four products run on the
+// tensor cores as bf16 x bf16 -> fp32 m16n8k16 mma: C B^T (K = N), the masked
+// scores times X (K = Q, causal: warp w, which owns steps 16w..16w+15, needs
+// only the first w+1 key tiles), C H_in (K = N) and (B o w)^T X (K = Q).  The
+// masked scores, B o w and H_in are rounded to bf16 for their products
+// (relative 2^-9); every sum is fp32.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace ssm {
+namespace ssd {
+
+constexpr int Q = 64;      // steps per chunk
+constexpr int P = 64;      // head dimension
+constexpr int THREADS = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t ld32(const bf16* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
+// Shared-memory layout; every row is padded by 8 elements so that the eight
+// rows a fragment load touches fall in different banks.
+template <int N>
+struct Smem {
+    static constexpr int NP = N + 8, QP = Q + 8;
+    bf16 Xt[P][QP];    // x of the chunk, transposed: [p][s]
+    bf16 Bs[Q][NP];    // B rows: [s][n]
+    bf16 Cs[Q][NP];    // C rows: [t][n]
+    bf16 Bwt[N][QP];   // (B o w) transposed: [n][s]
+    bf16 Ht[P][NP];    // the state entering the chunk, transposed: [p][n]
+    float dts[Q], cum[Q], w[Q], ecum[Q];
+};
+
+template <int N>
+__global__ void __launch_bounds__(THREADS, 2)
+ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
+                 const float* __restrict__ dt_bias, const float* __restrict__ A,
+                 const bf16* __restrict__ Bm, const bf16* __restrict__ Cm,
+                 const float* __restrict__ Dskip, bf16* __restrict__ y, float* __restrict__ h_last,
+                 long long batch, long long L, long long H) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Smem<N>& sm = *reinterpret_cast<Smem<N>*>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tq = lane & 3;
+    const long long b = blockIdx.x / H, hh = blockIdx.x % H;
+    const float a = A[hh];
+    const float kb2 = dt_bias ? dt_bias[hh] * kLog2e : 0.0f;
+    const float dsk = Dskip ? Dskip[hh] : 0.0f;
+    constexpr int MT = 2;          // state m-tiles per warp (32 rows)
+    constexpr int NT = P / 8;      // n-tiles over p
+    float Hs[MT][NT][4];           // state rows RW*warp + 16*mt + {g, g+8}, cols 8*nt + 2tq + {0,1}
+    static_assert(N == 64 || N == 128, "state size");
+    constexpr int RW = N / 4;      // state rows per warp
+    static_assert(RW == 16 * MT || RW == 16, "rows per warp");
+    constexpr int MTW = RW / 16;   // m-tiles per warp actually used (1 for N = 64)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) Hs[mt][nt][i] = 0.0f;
+    // Ht starts at zero
+    for (int i = tid; i < P * (N + 8); i += THREADS)
+        (&sm.Ht[0][0])[i] = __float2bfloat16_rn(0.0f);
+
+    const long long nchunks = (L + Q - 1) / Q;
+    for (long long c = 0; c < nchunks; ++c) {
+        const long long t0 = c * Q;
+        const int nv = (int)(L - t0 < Q ? L - t0 : Q);
+        // ---- loads: x (transposed), B, C, dt
+        for (int i = tid; i < Q * (P / 8); i += THREADS) {
+            const int s = i / (P / 8), p8 = (i % (P / 8)) * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (s < nv)
+                v = *reinterpret_cast<const uint4*>(x + ((b * L + t0 + s) * H + hh) * P + p8);
+            const bf16* e = reinterpret_cast<const bf16*>(&v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sm.Xt[p8 + k][s] = e[k];
+        }
+        for (int i = tid; i < Q * (N / 8); i += THREADS) {
+            const int s = i / (N / 8), n8 = (i % (N / 8)) * 8;
+            uint4 vb = make_uint4(0, 0, 0, 0), vc = make_uint4(0, 0, 0, 0);
+            if (s < nv) {
+                vb = *reinterpret_cast<const uint4*>(Bm + (b * L + t0 + s) * N + n8);
+                vc = *reinterpret_cast<const uint4*>(Cm + (b * L + t0 + s) * N + n8);
+            }
+            *reinterpret_cast<uint4*>(&sm.Bs[s][n8]) = vb;
+            *reinterpret_cast<uint4*>(&sm.Cs[s][n8]) = vc;
+        }
+        if (tid < Q) {
+            float d = 0.0f;
+            if (tid < nv) {
+                const float v2 = fmaf(__bfloat162float(dtr[(b * L + t0 + tid) * H + hh]), kLog2e, kb2);
+                d = (v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2))) * 0.6931471805599453f;
+            }
+            sm.dts[tid] = d;
+        }
+        __syncthreads();
+        // ---- cumulative decay (warp 0: a scan over 64 steps, two per lane)
+        if (warp == 0) {
+            const float d0 = sm.dts[2 * lane] * a, d1 = sm.dts[2 * lane + 1] * a;
+            float s = d0 + d1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += v;
+            }
+            const float c1 = s, c0 = s - d1;   // inclusive sums at steps 2*lane, 2*lane+1
+            const float cend = __shfl_sync(0xffffffffu, s, 31);
+            sm.cum[2 * lane] = c0;
+            sm.cum[2 * lane + 1] = c1;
+            sm.ecum[2 * lane] = ptx::ex2(c0 * kLog2e);
+            sm.ecum[2 * lane + 1] = ptx::ex2(c1 * kLog2e);
+            sm.w[2 * lane] = ptx::ex2((cend - c0) * kLog2e) * sm.dts[2 * lane];
+            sm.w[2 * lane + 1] = ptx::ex2((cend - c1) * kLog2e) * sm.dts[2 * lane + 1];
+        }
+        __syncthreads();
+        // ---- (B o w)^T
+        for (int i = tid; i < Q * N; i += THREADS) {
+            const int s = i / N, n = i % N;
+            sm.Bwt[n][s] = __float2bfloat16_rn(__bfloat162float(sm.Bs[s][n]) * sm.w[s]);
+        }
+        // ---- outputs of this warp's 16 steps: exp(cum_t) C_t H_in + masked scores X + D x
+        {
+            const int r0 = 16 * warp;
+            float Y[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Y[nt][i] = 0.0f;
+            // C H_in (K = N)
+#pragma unroll
+            for (int k0 = 0; k0 < N; k0 += 16) {
+                const uint32_t a0 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq]);
+                const uint32_t a1 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq]);
+                const uint32_t a2 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq + 8]);
+                const uint32_t a3 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq + 8]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint32_t b0 = ld32(&sm.Ht[8 * nt + g][k0 + 2 * tq]);
+                    const uint32_t b1 = ld32(&sm.Ht[8 * nt + g][k0 + 2 * tq + 8]);
+                    mma16816(Y[nt], a0, a1, a2, a3, b0, b1);
+                }
+            }
+            const float e_lo = sm.ecum[r0 + g], e_hi = sm.ecum[r0 + g + 8];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                Y[nt][0] *= e_lo;
+                Y[nt][1] *= e_lo;
+                Y[nt][2] *= e_hi;
+                Y[nt][3] *= e_hi;
+            }
+            // scores S = C B^T for key tiles 0..2*warp+1 (keys s <= r0 + 15)
+            float S[8][4];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) S[j][i] = 0.0f;
+#pragma unroll
+            for (int k0 = 0; k0 < N; k0 += 16) {
+                const uint32_t a0 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq]);
+                const uint32_t a1 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq]);
+                const uint32_t a2 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq + 8]);
+                const uint32_t a3 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq + 8]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j <= 2 * warp + 1) {
+                        const uint32_t b0 = ld32(&sm.Bs[8 * j + g][k0 + 2 * tq]);
+                        const uint32_t b1 = ld32(&sm.Bs[8 * j + g][k0 + 2 * tq + 8]);
+                        mma16816(S[j], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+            }
+            // mask and decay: S[t][s] *= exp(cum_t - cum_s) dt_s for s <= t, else 0
+            const int tlo = r0 + g, thi = r0 + g + 8;
+            const float clo = sm.cum[tlo], chi = sm.cum[thi];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j <= 2 * warp + 1) {
+                    const int s0 = 8 * j + 2 * tq, s1 = s0 + 1;
+                    const float cs0 = sm.cum[s0], cs1 = sm.cum[s1];
+                    const float d0 = sm.dts[s0], d1 = sm.dts[s1];
+                    S[j][0] = s0 <= tlo ? S[j][0] * ptx::ex2((clo - cs0) * kLog2e) * d0 : 0.0f;
+                    S[j][1] = s1 <= tlo ? S[j][1] * ptx::ex2((clo - cs1) * kLog2e) * d1 : 0.0f;
+                    S[j][2] = s0 <= thi ? S[j][2] * ptx::ex2((chi - cs0) * kLog2e) * d0 : 0.0f;
+                    S[j][3] = s1 <= thi ? S[j][3] * ptx::ex2((chi - cs1) * kLog2e) * d1 : 0.0f;
+                }
+            }
+            // masked scores times X (K = keys, tiles of 16: 0..warp)
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                if (kt <= warp) {
+                    const uint32_t a0 = pack_bf16(S[2 * kt][0], S[2 * kt][1]);
+                    const uint32_t a1 = pack_bf16(S[2 * kt][2], S[2 * kt][3]);
+                    const uint32_t a2 = pack_bf16(S[2 * kt + 1][0], S[2 * kt + 1][1]);
+                    const uint32_t a3 = pack_bf16(S[2 * kt + 1][2], S[2 * kt + 1][3]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint32_t b0 = ld32(&sm.Xt[8 * nt + g][16 * kt + 2 * tq]);
+                        const uint32_t b1 = ld32(&sm.Xt[8 * nt + g][16 * kt + 2 * tq + 8]);
+                        mma16816(Y[nt], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+            }
+            // + D x, store
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int p0 = 8 * nt + 2 * tq;
+                if (tlo < nv) {
+                    const float x0 = __bfloat162float(sm.Xt[p0][tlo]), x1 = __bfloat162float(sm.Xt[p0 + 1][tlo]);
+                    *reinterpret_cast<__nv_bfloat162*>(y + ((b * L + t0 + tlo) * H + hh) * P + p0) =
+                        __floats2bfloat162_rn(fmaf(dsk, x0, Y[nt][0]), fmaf(dsk, x1, Y[nt][1]));
+                }
+                if (thi < nv) {
+                    const float x0 = __bfloat162float(sm.Xt[p0][thi]), x1 = __bfloat162float(sm.Xt[p0 + 1][thi]);
+                    *reinterpret_cast<__nv_bfloat162*>(y + ((b * L + t0 + thi) * H + hh) * P + p0) =
+                        __floats2bfloat162_rn(fmaf(dsk, x0, Y[nt][2]), fmaf(dsk, x1, Y[nt][3]));
+                }
+            }
+        }
+        __syncthreads();   // Ht and Bwt: all readers done / all writers done
+        // ---- the state: H <- exp(cum_end) H + (B o w)^T X   (K = Q)
+        {
+            const float dec = sm.ecum[Q - 1];
+#pragma unroll
+            for (int mt = 0; mt < MTW; ++mt) {
+                const int m0 = RW * warp + 16 * mt;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) Hs[mt][nt][i] *= dec;
+#pragma unroll
+                for (int k0 = 0; k0 < Q; k0 += 16) {
+                    const uint32_t a0 = ld32(&sm.Bwt[m0 + g][k0 + 2 * tq]);
+                    const uint32_t a1 = ld32(&sm.Bwt[m0 + g + 8][k0 + 2 * tq]);
+                    const uint32_t a2 = ld32(&sm.Bwt[m0 + g][k0 + 2 * tq + 8]);
+                    const uint32_t a3 = ld32(&sm.Bwt[m0 + g + 8][k0 + 2 * tq + 8]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint32_t b0 = ld32(&sm.Xt[8 * nt + g][k0 + 2 * tq]);
+                        const uint32_t b1 = ld32(&sm.Xt[8 * nt + g][k0 + 2 * tq + 8]);
+                        mma16816(Hs[mt][nt], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+                // the bf16 copy the next chunk reads, transposed to [p][n]
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int p0 = 8 * nt + 2 * tq;
+                    sm.Ht[p0][m0 + g] = __float2bfloat16_rn(Hs[mt][nt][0]);
+                    sm.Ht[p0 + 1][m0 + g] = __float2bfloat16_rn(Hs[mt][nt][1]);
+                    sm.Ht[p0][m0 + g + 8] = __float2bfloat16_rn(Hs[mt][nt][2]);
+                    sm.Ht[p0 + 1][m0 + g + 8] = __float2bfloat16_rn(Hs[mt][nt][3]);
+                }
+            }
+        }
+        __syncthreads();   // Ht complete; the chunk's tiles are free
+    }
+    if (h_last) {
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) {
+            const int m0 = RW * warp + 16 * mt;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int p0 = 8 * nt + 2 * tq;
+                float* base = h_last + ((b * H + hh) * P) * N;
+                base[(long long)p0 * N + m0 + g] = Hs[mt][nt][0];
+                base[(long long)(p0 + 1) * N + m0 + g] = Hs[mt][nt][1];
+                base[(long long)p0 * N + m0 + g + 8] = Hs[mt][nt][2];
+                base[(long long)(p0 + 1) * N + m0 + g + 8] = Hs[mt][nt][3];
+            }
+        }
+    }
+}
+
+// Any dtype, P and N <= 256: one thread per channel (b, t-walk, h, p), the
+// recurrence in float32.  Correct, not tuned.
+template <typename T, int NMAX>
+__global__ void __launch_bounds__(128)
+ssd_generic_kernel(const T* __restrict__ x, const T* __restrict__ dtr,
+                   const float* __restrict__ dt_bias, const float* __restrict__ A,
+                   const T* __restrict__ Bm, const T* __restrict__ Cm,
+                   const float* __restrict__ Dskip, T* __restrict__ y, float* __restrict__ h_last,
+                   long long batch, long long L, long long H, long long P, int N) {
+    const long long ch = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (ch >= batch * H * P) return;
+    const long long b = ch / (H * P), hp = ch % (H * P), hh = hp / P;
+    const float a = A[hh];
+    const float bias = dt_bias ? dt_bias[hh] : 0.0f;
+    const float dsk = Dskip ? Dskip[hh] : 0.0f;
+    float h[NMAX];
+#pragma unroll
+    for (int n = 0; n < NMAX; ++n) h[n] = 0.0f;
+    for (long long t = 0; t < L; ++t) {
+        const float dt = softplus_ref(to_f32(dtr[(b * L + t) * H + hh]) + bias);
+        const float ab = expf(dt * a);
+        const float xt = to_f32(x[(b * L + t) * H * P + hp]);
+        float acc = dsk * xt;
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n) {
+            if (n < N) {
+                h[n] = fmaf(ab, h[n], dt * to_f32(Bm[(b * L + t) * N + n]) * xt);
+                acc = fmaf(to_f32(Cm[(b * L + t) * N + n]), h[n], acc);
+            }
+        }
+        y[(b * L + t) * H * P + hp] = from_f32<T>(acc);
+    }
+    if (h_last) {
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n)
+            if (n < N) h_last[ch * N + n] = h[n];
+    }
+}
+
+template <int N>
+inline cudaError_t launch_ssd_chunk(const bf16* x, const bf16* dt, const float* dt_bias,
+                                   const float* A, const bf16* Bm, const bf16* Cm,
+                                   const float* Dskip, bf16* y, float* h_last, long long batch,
+                                   long long L, long long H, cudaStream_t s) {
+    const int smem = (int)sizeof(Smem<N>);
+    cudaError_t e = cudaFuncSetAttribute(ssd_chunk_kernel<N>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    ssd_chunk_kernel<N><<<(unsigned)(batch * H), THREADS, smem, s>>>(x, dt, dt_bias, A, Bm, Cm,
+                                                                    Dskip, y, h_last, batch, L, H);
+    return cudaGetLastError();
+}
+
+template <typename T>
+inline cudaError_t launch_ssd_generic(const T* x, const T* dt, const float* dt_bias,
+                                      const float* A, const T* Bm, const T* Cm,
+                                      const float* Dskip, T* y, float* h_last, long long batch,
+                                      long long L, long long H, long long P, int N,
+                                      cudaStream_t s) {
+    const long long nch = batch * H * P;
+    const unsigned blocks = (unsigned)((nch + 127) / 128);
+#define SSM_SSDG(NM)                                                                            \
+    ssd_generic_kernel<T, NM><<<blocks, 128, 0, s>>>(x, dt, dt_bias, A, Bm, Cm, Dskip, y, h_last, \
+                                                     batch, L, H, P, N)
+    if (N <= 16) SSM_SSDG(16);
+    else if (N <= 64) SSM_SSDG(64);
+    else if (N <= 128) SSM_SSDG(128);
+    else SSM_SSDG(256);
+#undef SSM_SSDG
+    return cudaGetLastError();
+}
+
+}  // namespace ssd
+}  // namespace ssm

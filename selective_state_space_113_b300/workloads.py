@@ -153,6 +153,51 @@ def grad_inputs(batch: int, L: int, D: int, N: int, dtype, seed: int, device="cp
     return dy, dh
 
 
+@dataclasses.dataclass(frozen=True)
+class SsdWorkload:
+    """A Mamba-2 (SSD) layer: H heads of dimension P, one B/C group of state N."""
+    name: str
+    batch: int
+    L: int
+    H: int
+    P: int
+    N: int
+    dtype: torch.dtype
+    seed: int
+
+    @property
+    def elements(self) -> int:
+        return self.batch * self.L * self.H * self.P
+
+
+SSD_SMALL = SsdWorkload("ssd_small_2x256_h4_p64_n128_bf16", 2, 256, 4, 64, 128, torch.bfloat16, 7)
+SSD_2P7B = SsdWorkload("mamba2_2.7b_4x4096_h80_p64_n128_bf16", 4, 4096, 80, 64, 128,
+                       torch.bfloat16, 8)
+
+
+def make_ssd_inputs(w: SsdWorkload, device="cpu", seed: int | None = None, **over):
+    """Inputs of the SSD form, drawn in this order from one generator:
+    x ~ N(0,1) [batch,L,H,P], dt ~ N(0,1) [batch,L,H] (before the softplus),
+    B, C ~ N(0,1) [batch,L,N] (input dtype); dt_bias = log(expm1(dt0)) with
+    dt0 log-uniform in [1e-3, 1e-1], A = -U(1, 16), Dskip ~ N(0,1) per head
+    (float32) -- the Mamba-2 initialisation ranges.  ``over`` replaces
+    batch/L/H/P/N."""
+    v = {k: over.get(k, getattr(w, k)) for k in ("batch", "L", "H", "P", "N")}
+    dtype = over.get("dtype", w.dtype)
+    g = _gen(w.seed if seed is None else seed, device)
+    b, L, H, P, N = v["batch"], v["L"], v["H"], v["P"], v["N"]
+    x = _randn((b, L, H, P), g, device, dtype)
+    dt = _randn((b, L, H), g, device, dtype)
+    B = _randn((b, L, N), g, device, dtype)
+    C = _randn((b, L, N), g, device, dtype)
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt0 = torch.exp(torch.rand(H, generator=g, device=device) * (hi - lo) + lo)
+    dt_bias = torch.log(torch.expm1(dt0)).to(torch.float32)
+    A = -(1.0 + 15.0 * torch.rand(H, generator=g, device=device))
+    Dskip = torch.randn(H, generator=g, device=device, dtype=torch.float32)
+    return dict(x=x, dt=dt, dt_bias=dt_bias, A=A, B=B, C=C, Dskip=Dskip)
+
+
 def make_step_inputs(w: StepWorkload, device="cpu", seed: int | None = None,
                      batch: int | None = None, D: int | None = None,
                      N: int | None = None, steps: int | None = None):
