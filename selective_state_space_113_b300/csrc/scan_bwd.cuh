@@ -428,22 +428,40 @@ bwd_unit_kernel(const BwdParams p) {
             }
         }
         const int nsteps = (int)(w.t1 - w.t0);
+        // Sub-chunk s is needed here only if another follows it (then it is
+        // full); its loads are issued one sub-chunk ahead.
+        const int nsw1 = (nsteps - 1) / KS;   // sub-chunks walked by sweep 1
+        float u1[KS], d1[KS];
+        if (nsw1 > 0) {
+#pragma unroll
+            for (int j = 0; j < KS; ++j) {
+                u1[j] = valid ? ldf(usrc + (w.t0 + j) * p.D) : 0.0f;
+                d1[j] = valid ? ldf(dsrc + (w.t0 + j) * p.D) : 0.0f;
+            }
+        }
         for (int s = 0; s < NSUB; ++s) {
 #pragma unroll
             for (int q = 0; q < NS / 4; ++q)
                 sm.starts[s][q][tid] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-            if (s == NSUB - 1 || (s + 1) * KS >= nsteps) break;   // later starts are not used
-            float u1[KS], d1[KS];
+            if (s >= nsw1) break;   // later starts are not used
+            float uc[KS], dc[KS];
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
-                const long long t = w.t0 + s * KS + j;   // < t1: this sub-chunk is full
-                u1[j] = valid ? ldf(usrc + t * p.D) : 0.0f;
-                d1[j] = valid ? ldf(dsrc + t * p.D) : 0.0f;
+                uc[j] = u1[j];
+                dc[j] = d1[j];
+            }
+            if (s + 1 < nsw1) {
+#pragma unroll
+                for (int j = 0; j < KS; ++j) {
+                    const long long t = w.t0 + (s + 1) * KS + j;   // a full sub-chunk
+                    u1[j] = valid ? ldf(usrc + t * p.D) : 0.0f;
+                    d1[j] = valid ? ldf(dsrc + t * p.D) : 0.0f;
+                }
             }
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
                 const int tt = s * KS + j;
-                fwd_step(h, c, arow, u1[j], softplus_l2(fmaf(d1[j], kLog2e, c.kb2)),
+                fwd_step(h, c, arow, uc[j], softplus_l2(fmaf(dc[j], kLog2e, c.kb2)),
                          sm.Bs + tt * NS, sm.Bp + tt * NS);
             }
         }
@@ -463,9 +481,24 @@ bwd_unit_kernel(const BwdParams p) {
         }
 
         // sweep 2: sub-chunks from the last, each recomputed then walked back
-        for (int s = NSUB - 1; s >= 0; --s) {
+        // Inputs of the sub-chunk walked next, loaded one sub-chunk ahead
+        // (raw u, delta, z, dy; zero past the unit's end).
+        float nu[KS], nd[KS], nz[KS], ny[KS];
+        auto load_sub = [&](int tb2) {
+#pragma unroll
+            for (int j = 0; j < KS; ++j) {
+                const bool in = valid && tb2 + j < nsteps;
+                const long long t = w.t0 + tb2 + j;
+                nu[j] = in ? ldf(usrc + t * p.D) : 0.0f;
+                nd[j] = in ? ldf(dsrc + t * p.D) : 0.0f;
+                nz[j] = (in && zsrc) ? ldf(zsrc + t * p.D) : 0.0f;
+                ny[j] = in ? ldf(ysrc + t * p.D) : 0.0f;
+            }
+        };
+        const int s_last = (nsteps - 1) / KS;
+        load_sub(s_last * KS);
+        for (int s = s_last; s >= 0; --s) {
             const int tb = s * KS;
-            if (tb >= nsteps) continue;   // uniform over the CTA
             const int cnt = nsteps - tb < KS ? nsteps - tb : KS;
 #pragma unroll
             for (int q = 0; q < NS / 4; ++q) {
@@ -478,17 +511,13 @@ bwd_unit_kernel(const BwdParams p) {
             float uj[KS], dlj[KS], vj[KS], zj[KS], dyj[KS];
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
-                uj[j] = dlj[j] = vj[j] = zj[j] = dyj[j] = 0.0f;
-                if (j < cnt) {
-                    const long long t = w.t0 + tb + j;
-                    uj[j] = valid ? ldf(usrc + t * p.D) : 0.0f;
-                    const float dv = valid ? ldf(dsrc + t * p.D) : 0.0f;
-                    zj[j] = (valid && zsrc) ? ldf(zsrc + t * p.D) : 0.0f;
-                    dyj[j] = valid ? ldf(ysrc + t * p.D) : 0.0f;
-                    vj[j] = fmaf(dv, kLog2e, c.kb2);
-                    dlj[j] = softplus_l2(vj[j]);
-                }
+                uj[j] = nu[j];
+                zj[j] = nz[j];
+                dyj[j] = ny[j];
+                vj[j] = fmaf(nd[j], kLog2e, c.kb2);
+                dlj[j] = j < cnt ? softplus_l2(vj[j]) : 0.0f;
             }
+            if (s > 0) load_sub(tb - KS);
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
                 if (j < cnt) {
