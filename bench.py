@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--workload", default="mamba2.8b", choices=sorted(WORKLOADS),
                     help="scan shape (default: the Mamba-2.8B layer; the others are the "
                          "smaller cases used for ncu captures)")
@@ -262,6 +263,9 @@ def bench_ours(args, rank, world, local):
     backward = None
     if not args.no_backward:
         backward = bench_backward(ssm, inp, w, stream)
+    configs = None
+    if not args.no_configs:
+        configs = bench_configs(ssm, dev, stream)
     ssd = None
     if not args.no_ssd:
         ssd = bench_ssd(ssm, dev, stream)
@@ -306,6 +310,7 @@ def bench_ours(args, rank, world, local):
         "clocks": clocks.summary(),
         "backward": backward,
         "ssd": ssd,
+        "other_configs": configs,
         "decode": decode,
         "discretisation_variants": variants,
         "e2e": e2e,
@@ -379,12 +384,71 @@ def bench_decode(ssm, dev, stream, reps: int = 5):
     peak, kind = measured_peaks()
     us = graph_ms * 1e3 / w.steps
     gbs = per_step / (us * 1e-6) / 1e9
+    # each step with L2 flushed before it (a write larger than L2 between
+    # steps, outside the events): the state then comes from DRAM every step
+    flush = torch.empty(64 << 20, device=dev, dtype=torch.float32)   # 256 MB > 126 MB L2
+    state.copy_(state0)
+    cold = []
+    for s_ in range(w.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ssm.ssm_step(state, inp["u"][s_], inp["delta"][s_], inp["dt_bias"], inp["A"],
+                     inp["B"][s_], inp["C"][s_], inp["Dskip"], inp["z"][s_], ys[s_])
+        e1.record()
+        e1.synchronize()
+        cold.append(e0.elapsed_time(e1))
+    cold_us = sorted(cold)[len(cold) // 2] * 1e3
     return {"workload": w.name, "steps": w.steps, "bytes_per_step": per_step,
             "us_per_step_graph": us, "us_per_step_launches": plain_ms * 1e3 / w.steps,
+            "us_per_step_l2_flushed": cold_us,
+            "gbs_l2_flushed": per_step / (cold_us * 1e-6) / 1e9,
             "elements_per_s": w.batch * w.D / (us * 1e-6), "gbs": gbs,
             "hbm_frac": gbs / peak, "peak_source": kind, "kernel_launches": w.steps,
             "note": "best of %d; the 84 MB state can stay resident in the 126 MB L2 across "
                     "steps, so GB/s is algorithmic bytes / time, not DRAM traffic" % reps}
+
+
+def bench_configs(ssm, dev, stream, reps: int = 20):
+    """The other scan configurations: the tiny fp32 case (time-varying and
+    time-invariant) and the Mamba-130M layer, each the median of `reps` calls
+    back to back and the median of `reps` calls with L2 flushed before each
+    (a 256 MB write outside the events), after 5 warm-up calls."""
+    import torch
+    from selective_state_space_113_b300 import workloads as wl
+    flush = torch.empty(64 << 20, device=dev, dtype=torch.float32)
+    out = {}
+    for w in (wl.TINY_F32, wl.TINY_F32_LTI, wl.MAMBA_130M):
+        inp = wl.make_scan_inputs(w, device=dev)
+        y = torch.empty_like(inp["u"])
+        h = torch.empty((w.batch, w.D, w.N), device=dev)
+
+        def call():
+            ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                             inp["Dskip"], inp["z"], y, h, stream=stream)
+        for _ in range(5):
+            call()
+        res = {}
+        for tag, cold in (("ms_back_to_back", False), ("ms_l2_flushed", True)):
+            # all calls enqueued before one synchronize, so that the GPU never
+            # waits for the host between them
+            ev = []
+            for _ in range(reps):
+                if cold:
+                    with torch.cuda.stream(stream):
+                        flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                ev.append((e0, e1))
+            stream.synchronize()
+            ts = sorted(a.elapsed_time(b) for a, b in ev)
+            res[tag] = ts[len(ts) // 2]
+        res["elements_per_s"] = w.elements / (res["ms_l2_flushed"] * 1e-3)
+        res["hbm_gbs_l2_flushed"] = algorithmic_bytes(w) / (res["ms_l2_flushed"] * 1e-3) / 1e9
+        out[w.name] = res
+    return out
 
 
 def bench_variants(ssm, inp, w, stream, reps: int = 5):
@@ -581,9 +645,17 @@ def cpu_baseline(inp, w):
     channels = min(w.D, max(64, int(20 * 3.5e6 / (w.batch * w.L))))
     channels = max(n, channels - channels % n)
     elems, secs = _oracle_sample(inp, w, channels, n)
+    # one core on a sample of the Mamba-130M layer, for scale
+    from selective_state_space_113_b300 import workloads as wl
+    w1 = wl.MAMBA_130M
+    inp1 = wl.make_scan_inputs(w1, device="cpu")
+    e1, s1 = _oracle_sample(inp1, w1, 64, 1)
     return {"value": elems / secs, "unit": "elements/s", "cores": n, "kind": "oracle",
             "sample": f"all {w.batch}x{w.L} steps of the first {channels} of {w.D} channels "
-                      f"({elems} elements, {secs:.1f} s wall, float64)"}
+                      f"({elems} elements, {secs:.1f} s wall, float64)",
+            "single_core_mamba130m": {"value": e1 / s1, "unit": "elements/s",
+                                      "sample": f"all {w1.batch}x{w1.L} steps of 64 of {w1.D} "
+                                                f"channels ({e1} elements, {s1:.1f} s)"}}
 
 
 def bench_reference(args, rank, world):
