@@ -13,15 +13,18 @@
 // (chunks of Q = 64 steps, cum_t = A sum_{r<=t in chunk} dt_r):
 //   y_chunk = (Lmask o C B^T) X + diag(exp(cum)) C H_in + Dskip X,
 //     Lmask[t, s] = exp(cum_t - cum_s) dt_s  for s <= t, 0 above the diagonal
-//   H_out = exp(cum_end) H_in + (B o w)^T X,   w_s = exp(cum_end - cum_s) dt_s
+//   H_out = exp(cum_end) H_in + B^T (w o X),   w_s = exp(cum_end - cum_s) dt_s
 // with H the N x P state of the head.  One CTA (4 warps) owns one (b, h) and
 // walks its chunks in order, the fp32 state in registers (warp w holds state
 // rows (N/4)w .. (N/4)(w+1)-1 as mma accumulators).  The four products run on the
 // tensor cores as bf16 x bf16 -> fp32 m16n8k16 mma: C B^T (K = N), the masked
 // scores times X (K = Q, causal: warp w, which owns steps 16w..16w+15, needs
-// only the first w+1 key tiles), C H_in (K = N) and (B o w)^T X (K = Q).  The
-// masked scores, B o w and H_in are rounded to bf16 for their products
-// (relative 2^-9); every sum is fp32.
+// only the first w+1 key tiles), C H_in (K = N) and B^T (w o X) (K = Q; the
+// B^T fragments come straight from the B tile by transposing ldmatrix).  The
+// masked scores, w o X and H_in are rounded to bf16 for their products
+// (relative 2^-9); every sum is fp32.  The scores are formed two key tiles at
+// a time, so that a CTA needs few enough registers (and, with no transposed
+// copy of B, little enough shared memory) for three CTAs to share an SM.
 #pragma once
 
 #include "common.cuh"
@@ -53,21 +56,44 @@ __device__ __forceinline__ uint32_t ld32(const bf16* p) {
     return *reinterpret_cast<const uint32_t*>(p);
 }
 
+// Four 8x8 bf16 tiles from shared memory, transposed: lane i gives the
+// address of row i % 8 of tile i / 8 (16 contiguous bytes, 16-byte aligned);
+// lane l receives (row 2(l%4), column l/4) and (row 2(l%4)+1, column l/4) of
+// each tile.  Read from a [k][m] array this is the A fragment of a
+// [m][k] = [k][m]^T operand.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const bf16* row_addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(ptx::smem_u32(row_addr)));
+}
+
+// Splits a, b into bf16 pairs hi + lo (hi = bf16(v), lo = bf16(v - hi)), so
+// that hi + lo carries about 16 significant bits: a product with an exact
+// bf16 operand taken as hi x + lo x keeps that accuracy.
+__device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+constexpr int PH = 32;   // channels of the head per CTA (two CTAs per head)
+
 // Shared-memory layout; every row is padded by 8 elements so that the eight
 // rows a fragment load touches fall in different banks.
 template <int N>
 struct Smem {
     static constexpr int NP = N + 8, QP = Q + 8;
-    bf16 Xt[P][QP];    // x of the chunk, transposed: [p][s]
-    bf16 Bs[Q][NP];    // B rows: [s][n]
-    bf16 Cs[Q][NP];    // C rows: [t][n]
-    bf16 Bwt[N][QP];   // (B o w) transposed: [n][s]
-    bf16 Ht[P][NP];    // the state entering the chunk, transposed: [p][n]
+    bf16 Xt[PH][QP];                // x of the chunk, transposed: [p][s]
+    bf16 Xwh[PH][QP], Xwl[PH][QP];  // w o x, transposed, as hi + lo bf16 parts
+    bf16 Bs[Q][NP];                 // B rows: [s][n]
+    bf16 Cs[Q][NP];                 // C rows: [t][n]
+    bf16 Hh[PH][NP], Hl[PH][NP];    // the state entering the chunk, [p][n], hi + lo
     float dts[Q], cum[Q], w[Q], ecum[Q];
 };
 
 template <int N>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 3)
 ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                  const float* __restrict__ dt_bias, const float* __restrict__ A,
                  const bf16* __restrict__ Bm, const bf16* __restrict__ Cm,
@@ -77,37 +103,38 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
     Smem<N>& sm = *reinterpret_cast<Smem<N>*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tq = lane & 3;
-    const long long b = blockIdx.x / H, hh = blockIdx.x % H;
+    const long long hb = blockIdx.x / (P / PH);
+    const int pbase = (int)(blockIdx.x % (P / PH)) * PH;   // this CTA's channels of the head
+    const long long b = hb / H, hh = hb % H;
     const float a = A[hh];
     const float kb2 = dt_bias ? dt_bias[hh] * kLog2e : 0.0f;
     const float dsk = Dskip ? Dskip[hh] : 0.0f;
-    constexpr int MT = 2;          // state m-tiles per warp (32 rows)
-    constexpr int NT = P / 8;      // n-tiles over p
-    float Hs[MT][NT][4];           // state rows RW*warp + 16*mt + {g, g+8}, cols 8*nt + 2tq + {0,1}
     static_assert(N == 64 || N == 128, "state size");
+    constexpr int NT = PH / 8;     // n-tiles over the CTA's channels
     constexpr int RW = N / 4;      // state rows per warp
-    static_assert(RW == 16 * MT || RW == 16, "rows per warp");
-    constexpr int MTW = RW / 16;   // m-tiles per warp actually used (1 for N = 64)
+    constexpr int MTW = RW / 16;   // state m-tiles per warp
+    float Hs[MTW][NT][4];          // state rows RW*warp + 16*mt + {g, g+8}, cols 8*nt + 2tq + {0,1}
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) Hs[mt][nt][i] = 0.0f;
-    // Ht starts at zero
-    for (int i = tid; i < P * (N + 8); i += THREADS)
-        (&sm.Ht[0][0])[i] = __float2bfloat16_rn(0.0f);
+    for (int i = tid; i < PH * (N + 8); i += THREADS) {
+        (&sm.Hh[0][0])[i] = __float2bfloat16_rn(0.0f);
+        (&sm.Hl[0][0])[i] = __float2bfloat16_rn(0.0f);
+    }
 
     const long long nchunks = (L + Q - 1) / Q;
     for (long long c = 0; c < nchunks; ++c) {
         const long long t0 = c * Q;
         const int nv = (int)(L - t0 < Q ? L - t0 : Q);
         // ---- loads: x (transposed), B, C, dt
-        for (int i = tid; i < Q * (P / 8); i += THREADS) {
-            const int s = i / (P / 8), p8 = (i % (P / 8)) * 8;
+        for (int i = tid; i < Q * (PH / 8); i += THREADS) {
+            const int s = i / (PH / 8), p8 = (i % (PH / 8)) * 8;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (s < nv)
-                v = *reinterpret_cast<const uint4*>(x + ((b * L + t0 + s) * H + hh) * P + p8);
+                v = *reinterpret_cast<const uint4*>(x + ((b * L + t0 + s) * H + hh) * P + pbase + p8);
             const bf16* e = reinterpret_cast<const bf16*>(&v);
 #pragma unroll
             for (int k = 0; k < 8; ++k) sm.Xt[p8 + k][s] = e[k];
@@ -134,14 +161,14 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
         // ---- cumulative decay (warp 0: a scan over 64 steps, two per lane)
         if (warp == 0) {
             const float d0 = sm.dts[2 * lane] * a, d1 = sm.dts[2 * lane + 1] * a;
-            float s = d0 + d1;
+            float sc = d0 + d1;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const float v = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += v;
+                const float v = __shfl_up_sync(0xffffffffu, sc, o);
+                if (lane >= o) sc += v;
             }
-            const float c1 = s, c0 = s - d1;   // inclusive sums at steps 2*lane, 2*lane+1
-            const float cend = __shfl_sync(0xffffffffu, s, 31);
+            const float c1 = sc, c0 = sc - d1;   // inclusive sums at steps 2*lane, 2*lane+1
+            const float cend = __shfl_sync(0xffffffffu, sc, 31);
             sm.cum[2 * lane] = c0;
             sm.cum[2 * lane + 1] = c1;
             sm.ecum[2 * lane] = ptx::ex2(c0 * kLog2e);
@@ -150,10 +177,13 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
             sm.w[2 * lane + 1] = ptx::ex2((cend - c1) * kLog2e) * sm.dts[2 * lane + 1];
         }
         __syncthreads();
-        // ---- (B o w)^T
-        for (int i = tid; i < Q * N; i += THREADS) {
-            const int s = i / N, n = i % N;
-            sm.Bwt[n][s] = __float2bfloat16_rn(__bfloat162float(sm.Bs[s][n]) * sm.w[s]);
+        // ---- w o x, transposed, hi + lo
+        for (int i = tid; i < Q * PH; i += THREADS) {
+            const int pp = i / Q, s = i % Q;
+            const float v = __bfloat162float(sm.Xt[pp][s]) * sm.w[s];
+            const bf16 hi = __float2bfloat16_rn(v);
+            sm.Xwh[pp][s] = hi;
+            sm.Xwl[pp][s] = __float2bfloat16_rn(v - __bfloat162float(hi));
         }
         // ---- outputs of this warp's 16 steps: exp(cum_t) C_t H_in + masked scores X + D x
         {
@@ -163,7 +193,7 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) Y[nt][i] = 0.0f;
-            // C H_in (K = N)
+            // C H_in (K = N), H_in as hi + lo
 #pragma unroll
             for (int k0 = 0; k0 < N; k0 += 16) {
                 const uint32_t a0 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq]);
@@ -172,9 +202,10 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                 const uint32_t a3 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq + 8]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint32_t b0 = ld32(&sm.Ht[8 * nt + g][k0 + 2 * tq]);
-                    const uint32_t b1 = ld32(&sm.Ht[8 * nt + g][k0 + 2 * tq + 8]);
-                    mma16816(Y[nt], a0, a1, a2, a3, b0, b1);
+                    mma16816(Y[nt], a0, a1, a2, a3, ld32(&sm.Hh[8 * nt + g][k0 + 2 * tq]),
+                             ld32(&sm.Hh[8 * nt + g][k0 + 2 * tq + 8]));
+                    mma16816(Y[nt], a0, a1, a2, a3, ld32(&sm.Hl[8 * nt + g][k0 + 2 * tq]),
+                             ld32(&sm.Hl[8 * nt + g][k0 + 2 * tq + 8]));
                 }
             }
             const float e_lo = sm.ecum[r0 + g], e_hi = sm.ecum[r0 + g + 8];
@@ -185,55 +216,53 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                 Y[nt][2] *= e_hi;
                 Y[nt][3] *= e_hi;
             }
-            // scores S = C B^T for key tiles 0..2*warp+1 (keys s <= r0 + 15)
-            float S[8][4];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) S[j][i] = 0.0f;
-#pragma unroll
-            for (int k0 = 0; k0 < N; k0 += 16) {
-                const uint32_t a0 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq]);
-                const uint32_t a1 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq]);
-                const uint32_t a2 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq + 8]);
-                const uint32_t a3 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq + 8]);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (j <= 2 * warp + 1) {
-                        const uint32_t b0 = ld32(&sm.Bs[8 * j + g][k0 + 2 * tq]);
-                        const uint32_t b1 = ld32(&sm.Bs[8 * j + g][k0 + 2 * tq + 8]);
-                        mma16816(S[j], a0, a1, a2, a3, b0, b1);
-                    }
-                }
-            }
-            // mask and decay: S[t][s] *= exp(cum_t - cum_s) dt_s for s <= t, else 0
+            // scores S = C B^T, two key tiles (16 keys) at a time up to the
+            // diagonal; masked, decayed, split hi + lo and multiplied into X
             const int tlo = r0 + g, thi = r0 + g + 8;
             const float clo = sm.cum[tlo], chi = sm.cum[thi];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j <= 2 * warp + 1) {
-                    const int s0 = 8 * j + 2 * tq, s1 = s0 + 1;
-                    const float cs0 = sm.cum[s0], cs1 = sm.cum[s1];
-                    const float d0 = sm.dts[s0], d1 = sm.dts[s1];
-                    S[j][0] = s0 <= tlo ? S[j][0] * ptx::ex2((clo - cs0) * kLog2e) * d0 : 0.0f;
-                    S[j][1] = s1 <= tlo ? S[j][1] * ptx::ex2((clo - cs1) * kLog2e) * d1 : 0.0f;
-                    S[j][2] = s0 <= thi ? S[j][2] * ptx::ex2((chi - cs0) * kLog2e) * d0 : 0.0f;
-                    S[j][3] = s1 <= thi ? S[j][3] * ptx::ex2((chi - cs1) * kLog2e) * d1 : 0.0f;
-                }
-            }
-            // masked scores times X (K = keys, tiles of 16: 0..warp)
-#pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
                 if (kt <= warp) {
-                    const uint32_t a0 = pack_bf16(S[2 * kt][0], S[2 * kt][1]);
-                    const uint32_t a1 = pack_bf16(S[2 * kt][2], S[2 * kt][3]);
-                    const uint32_t a2 = pack_bf16(S[2 * kt + 1][0], S[2 * kt + 1][1]);
-                    const uint32_t a3 = pack_bf16(S[2 * kt + 1][2], S[2 * kt + 1][3]);
+                    float S[2][4];
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) S[jj][i] = 0.0f;
+#pragma unroll
+                    for (int k0 = 0; k0 < N; k0 += 16) {
+                        const uint32_t a0 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq]);
+                        const uint32_t a1 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq]);
+                        const uint32_t a2 = ld32(&sm.Cs[r0 + g][k0 + 2 * tq + 8]);
+                        const uint32_t a3 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq + 8]);
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int j = 2 * kt + jj;
+                            mma16816(S[jj], a0, a1, a2, a3, ld32(&sm.Bs[8 * j + g][k0 + 2 * tq]),
+                                     ld32(&sm.Bs[8 * j + g][k0 + 2 * tq + 8]));
+                        }
+                    }
+                    // S[t][s] *= exp(cum_t - cum_s) dt_s for s <= t, else 0
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int s0 = 16 * kt + 8 * jj + 2 * tq, s1 = s0 + 1;
+                        const float cs0 = sm.cum[s0], cs1 = sm.cum[s1];
+                        const float d0 = sm.dts[s0], d1 = sm.dts[s1];
+                        S[jj][0] = s0 <= tlo ? S[jj][0] * ptx::ex2((clo - cs0) * kLog2e) * d0 : 0.0f;
+                        S[jj][1] = s1 <= tlo ? S[jj][1] * ptx::ex2((clo - cs1) * kLog2e) * d1 : 0.0f;
+                        S[jj][2] = s0 <= thi ? S[jj][2] * ptx::ex2((chi - cs0) * kLog2e) * d0 : 0.0f;
+                        S[jj][3] = s1 <= thi ? S[jj][3] * ptx::ex2((chi - cs1) * kLog2e) * d1 : 0.0f;
+                    }
+                    uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+                    split_pack(S[0][0], S[0][1], h0, l0);
+                    split_pack(S[0][2], S[0][3], h1, l1);
+                    split_pack(S[1][0], S[1][1], h2, l2);
+                    split_pack(S[1][2], S[1][3], h3, l3);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const uint32_t b0 = ld32(&sm.Xt[8 * nt + g][16 * kt + 2 * tq]);
                         const uint32_t b1 = ld32(&sm.Xt[8 * nt + g][16 * kt + 2 * tq + 8]);
-                        mma16816(Y[nt], a0, a1, a2, a3, b0, b1);
+                        mma16816(Y[nt], h0, h1, h2, h3, b0, b1);
+                        mma16816(Y[nt], l0, l1, l2, l3, b0, b1);
                     }
                 }
             }
@@ -241,22 +270,24 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int p0 = 8 * nt + 2 * tq;
+                bf16* yrow = y + pbase + p0;
                 if (tlo < nv) {
                     const float x0 = __bfloat162float(sm.Xt[p0][tlo]), x1 = __bfloat162float(sm.Xt[p0 + 1][tlo]);
-                    *reinterpret_cast<__nv_bfloat162*>(y + ((b * L + t0 + tlo) * H + hh) * P + p0) =
+                    *reinterpret_cast<__nv_bfloat162*>(yrow + ((b * L + t0 + tlo) * H + hh) * P) =
                         __floats2bfloat162_rn(fmaf(dsk, x0, Y[nt][0]), fmaf(dsk, x1, Y[nt][1]));
                 }
                 if (thi < nv) {
                     const float x0 = __bfloat162float(sm.Xt[p0][thi]), x1 = __bfloat162float(sm.Xt[p0 + 1][thi]);
-                    *reinterpret_cast<__nv_bfloat162*>(y + ((b * L + t0 + thi) * H + hh) * P + p0) =
+                    *reinterpret_cast<__nv_bfloat162*>(yrow + ((b * L + t0 + thi) * H + hh) * P) =
                         __floats2bfloat162_rn(fmaf(dsk, x0, Y[nt][2]), fmaf(dsk, x1, Y[nt][3]));
                 }
             }
         }
-        __syncthreads();   // Ht and Bwt: all readers done / all writers done
-        // ---- the state: H <- exp(cum_end) H + (B o w)^T X   (K = Q)
+        __syncthreads();   // Hh/Hl: all readers done; Xwh/Xwl: all writers done
+        // ---- the state: H <- exp(cum_end) H + B^T (w o X)   (K = Q), w o X as hi + lo
         {
             const float dec = sm.ecum[Q - 1];
+            const int tile = lane >> 3, row = lane & 7;
 #pragma unroll
             for (int mt = 0; mt < MTW; ++mt) {
                 const int m0 = RW * warp + 16 * mt;
@@ -266,29 +297,35 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                     for (int i = 0; i < 4; ++i) Hs[mt][nt][i] *= dec;
 #pragma unroll
                 for (int k0 = 0; k0 < Q; k0 += 16) {
-                    const uint32_t a0 = ld32(&sm.Bwt[m0 + g][k0 + 2 * tq]);
-                    const uint32_t a1 = ld32(&sm.Bwt[m0 + g + 8][k0 + 2 * tq]);
-                    const uint32_t a2 = ld32(&sm.Bwt[m0 + g][k0 + 2 * tq + 8]);
-                    const uint32_t a3 = ld32(&sm.Bwt[m0 + g + 8][k0 + 2 * tq + 8]);
+                    // A = B^T rows m0.., keys k0..: tiles Bs[k0 + 8 (i/16) ..][m0 + 8 ((i/8)&1)]
+                    uint32_t af[4];
+                    ldsm_x4_trans(af, &sm.Bs[k0 + 8 * (tile >> 1) + row][m0 + 8 * (tile & 1)]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const uint32_t b0 = ld32(&sm.Xt[8 * nt + g][k0 + 2 * tq]);
-                        const uint32_t b1 = ld32(&sm.Xt[8 * nt + g][k0 + 2 * tq + 8]);
-                        mma16816(Hs[mt][nt], a0, a1, a2, a3, b0, b1);
+                        mma16816(Hs[mt][nt], af[0], af[1], af[2], af[3],
+                                 ld32(&sm.Xwh[8 * nt + g][k0 + 2 * tq]),
+                                 ld32(&sm.Xwh[8 * nt + g][k0 + 2 * tq + 8]));
+                        mma16816(Hs[mt][nt], af[0], af[1], af[2], af[3],
+                                 ld32(&sm.Xwl[8 * nt + g][k0 + 2 * tq]),
+                                 ld32(&sm.Xwl[8 * nt + g][k0 + 2 * tq + 8]));
                     }
                 }
-                // the bf16 copy the next chunk reads, transposed to [p][n]
+                // the copy the next chunk reads, transposed to [p][n], hi + lo
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int p0 = 8 * nt + 2 * tq;
-                    sm.Ht[p0][m0 + g] = __float2bfloat16_rn(Hs[mt][nt][0]);
-                    sm.Ht[p0 + 1][m0 + g] = __float2bfloat16_rn(Hs[mt][nt][1]);
-                    sm.Ht[p0][m0 + g + 8] = __float2bfloat16_rn(Hs[mt][nt][2]);
-                    sm.Ht[p0 + 1][m0 + g + 8] = __float2bfloat16_rn(Hs[mt][nt][3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int pp = p0 + (i & 1), mm = m0 + g + 8 * (i >> 1);
+                        const float v = Hs[mt][nt][i];
+                        const bf16 hi = __float2bfloat16_rn(v);
+                        sm.Hh[pp][mm] = hi;
+                        sm.Hl[pp][mm] = __float2bfloat16_rn(v - __bfloat162float(hi));
+                    }
                 }
             }
         }
-        __syncthreads();   // Ht complete; the chunk's tiles are free
+        __syncthreads();   // Hh/Hl complete; the chunk's tiles are free
     }
     if (h_last) {
 #pragma unroll
@@ -296,7 +333,7 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
             const int m0 = RW * warp + 16 * mt;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int p0 = 8 * nt + 2 * tq;
+                const int p0 = pbase + 8 * nt + 2 * tq;
                 float* base = h_last + ((b * H + hh) * P) * N;
                 base[(long long)p0 * N + m0 + g] = Hs[mt][nt][0];
                 base[(long long)(p0 + 1) * N + m0 + g] = Hs[mt][nt][1];
@@ -355,8 +392,8 @@ inline cudaError_t launch_ssd_chunk(const bf16* x, const bf16* dt, const float* 
     cudaError_t e = cudaFuncSetAttribute(ssd_chunk_kernel<N>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    ssd_chunk_kernel<N><<<(unsigned)(batch * H), THREADS, smem, s>>>(x, dt, dt_bias, A, Bm, Cm,
-                                                                    Dskip, y, h_last, batch, L, H);
+    ssd_chunk_kernel<N><<<(unsigned)(batch * H * (P / PH)), THREADS, smem, s>>>(
+        x, dt, dt_bias, A, Bm, Cm, Dskip, y, h_last, batch, L, H);
     return cudaGetLastError();
 }
 

@@ -72,11 +72,15 @@ def test_ssd_nulls_and_empty():
 
 def test_ssd_mamba2_2p7b_sampled_heads():
     """The 4 x 4096 x (80 heads x 64) layer with N = 128 on the tensor-core
-    kernel; every output of three sampled heads against the oracle."""
+    kernel; every output of sampled heads against the oracle.  The sample
+    always holds the six most slowly decaying heads (smallest |A|), whose long
+    memories make the largest states and the most cancellation in y: rounding
+    the bf16 operands of the products once (without a low part) put y 4.6% off
+    on such a head."""
     w = wl.SSD_2P7B
     inp = wl.make_ssd_inputs(w, device=DEV)
     y, h = run_ssd(inp)
-    heads = [0, 37, w.H - 1]
+    heads = sorted(set(torch.argsort(inp["A"].abs())[:6].tolist()) | {0, 37, w.H - 1})
     idx = torch.tensor(heads, device=DEV)
     sub = dict(inp, x=inp["x"].index_select(2, idx), dt=inp["dt"].index_select(2, idx),
                dt_bias=inp["dt_bias"].index_select(0, idx), A=inp["A"].index_select(0, idx),
