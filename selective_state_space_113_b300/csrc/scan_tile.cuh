@@ -388,7 +388,9 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
         }
         const float dv = ld_elem(Dl + t * CB + col);
         const float v2 = fmaf(dv, kLog2e, cp.kb2);           // (delta + bias) log2(e)
-        const float dl = ptx::lg2(1.0f + ptx::ex2(v2));      // softplus / ln 2
+        // softplus / ln 2; the identity above v = 20 (v2 = 28.85), where the two
+        // agree to float32 and 2^v2 could overflow
+        const float dl = v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2));
         float g = 1.0f;
         if (MODE != kAggregate) {
             if constexpr (HASZ) {

@@ -115,3 +115,22 @@ def test_disc_rejects_unknown():
     inp = wl.make_scan_inputs(wl.TINY_F32, device=DEV, batch=1, L=4, D=8, seed=1)
     with pytest.raises(ssm.SsmError):
         run_disc(inp, 3)
+
+
+@pytest.mark.parametrize("disc", ["euler", "trapezoid"])
+def test_disc_huge_and_tiny_dt(disc):
+    """delta + bias far above 88 (where 2^(v log2 e) overflows float32) and far
+    below: dt must stay finite and follow the oracle, on geometric rows, an
+    A = 0 row and per-state rows.  With these input terms a huge dt makes the
+    state itself huge (dt B u), and the outputs of later steps would then be
+    small differences of huge terms, beyond float32; so the huge steps are
+    the last ones, where y and h_last are large themselves."""
+    inp = wl.make_scan_inputs(wl.TINY_F32, device=DEV, batch=2, L=64, D=32, seed=13)
+    inp["delta"][0, -1] = 1e4
+    inp["delta"][1, -1] = 300.0
+    inp["delta"][1, ::4] = -1e4
+    inp["A"][3] = 0.0
+    g = torch.Generator(device=DEV).manual_seed(2)
+    inp["A"][4:8] = -torch.rand((4, 16), generator=g, device=DEV) * 5
+    full_parity(inp, DISCS[disc], f"{disc} huge/tiny dt")
+

@@ -109,6 +109,8 @@ def test_edge_values():
     inp = wl.make_scan_inputs(wl.TINY_F32, device=DEV, batch=2, L=64, D=32, seed=9)
     inp["delta"][0, ::3, 8:] = 1e4
     inp["delta"][1, ::5, 8:] = -1e4
+    inp["delta"][0, 1::7, :8] = 1e4     # huge dt on the A = 0 and per-state channels too
+    inp["delta"][1, 2::9, :8] = 300.0
     inp["z"][0, 10:20] = 0.0
     inp["A"][3] = 0.0
     g = torch.Generator(device=DEV).manual_seed(1)
