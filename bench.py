@@ -411,14 +411,16 @@ def bench_decode(ssm, dev, stream, reps: int = 5):
 
 def bench_configs(ssm, dev, stream, reps: int = 20):
     """The other scan configurations: the tiny fp32 case (time-varying and
-    time-invariant) and the Mamba-130M layer, each the median of `reps` calls
-    back to back and the median of `reps` calls with L2 flushed before each
-    (a 256 MB write outside the events), after 5 warm-up calls."""
+    time-invariant), the Mamba-130M layer and the 1M-step sequence (the narrow
+    plan; 5 calls), each the median of `reps` calls back to back and the
+    median with L2 flushed before each (a 256 MB write outside the events),
+    after 5 warm-up calls."""
     import torch
     from selective_state_space_113_b300 import workloads as wl
     flush = torch.empty(64 << 20, device=dev, dtype=torch.float32)
     out = {}
-    for w in (wl.TINY_F32, wl.TINY_F32_LTI, wl.MAMBA_130M):
+    for w in (wl.TINY_F32, wl.TINY_F32_LTI, wl.MAMBA_130M, wl.LONG_SEQ):
+        n_reps = 5 if w is wl.LONG_SEQ else reps
         inp = wl.make_scan_inputs(w, device=dev)
         y = torch.empty_like(inp["u"])
         h = torch.empty((w.batch, w.D, w.N), device=dev)
@@ -433,7 +435,7 @@ def bench_configs(ssm, dev, stream, reps: int = 20):
             # all calls enqueued before one synchronize, so that the GPU never
             # waits for the host between them
             ev = []
-            for _ in range(reps):
+            for _ in range(n_reps):
                 if cold:
                     with torch.cuda.stream(stream):
                         flush.zero_()
