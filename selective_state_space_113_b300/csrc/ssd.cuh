@@ -79,6 +79,16 @@ __device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint3
 
 constexpr int PH = 32;   // channels of the head per CTA (two CTAs per head)
 
+// 16-byte asynchronous copy global -> shared; with valid false it reads
+// nothing and writes zeros (src-size 0).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Shared-memory layout; every row is padded by 8 elements so that the eight
 // rows a fragment load touches fall in different banks.
 template <int N>
@@ -126,37 +136,56 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
     }
 
     const long long nchunks = (L + Q - 1) / Q;
+    // Staging of a chunk: x transposed into Xt, B and C rows, dt after the
+    // softplus; rows past the sequence are zero.  Chunk 0 is staged here; a
+    // later chunk's C rows (by cp.async), x and dt (in registers) are fetched
+    // while the chunk before it updates its state, and its B rows after.
+    auto x_item = [&](int i, int& s, int& p8) {
+        s = i / (PH / 8);
+        p8 = (i % (PH / 8)) * 8;
+    };
+    auto load_x = [&](long long tc, int nvc, int i) {
+        int s, p8;
+        x_item(i, s, p8);
+        return s < nvc ? *reinterpret_cast<const uint4*>(x + ((b * L + tc + s) * H + hh) * P + pbase + p8)
+                       : make_uint4(0, 0, 0, 0);
+    };
+    auto store_x = [&](int i, const uint4& v) {
+        int s, p8;
+        x_item(i, s, p8);
+        const bf16* e = reinterpret_cast<const bf16*>(&v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sm.Xt[p8 + k][s] = e[k];
+    };
+    auto load_dt = [&](long long tc, int nvc) {
+        float d = 0.0f;
+        if (tid < nvc) {
+            const float v2 = fmaf(__bfloat162float(dtr[(b * L + tc + tid) * H + hh]), kLog2e, kb2);
+            d = (v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2))) * 0.6931471805599453f;
+        }
+        return d;
+    };
+    auto load_rows = [&](const bf16* src, bf16 (*dst)[N + 8], long long tc, int nvc) {
+        for (int i = tid; i < Q * (N / 8); i += THREADS) {
+            const int s = i / (N / 8), n8 = (i % (N / 8)) * 8;
+            *reinterpret_cast<uint4*>(&dst[s][n8]) =
+                s < nvc ? *reinterpret_cast<const uint4*>(src + (b * L + tc + s) * N + n8)
+                        : make_uint4(0, 0, 0, 0);
+        }
+    };
+    constexpr int XPT = Q * (PH / 8) / THREADS;   // x items per thread
+    static_assert(Q * (PH / 8) % THREADS == 0, "x staging");
+    {
+        const int nv0 = (int)(L < Q ? L : Q);
+#pragma unroll
+        for (int k = 0; k < XPT; ++k) store_x(tid + THREADS * k, load_x(0, nv0, tid + THREADS * k));
+        load_rows(Bm, sm.Bs, 0, nv0);
+        load_rows(Cm, sm.Cs, 0, nv0);
+        if (tid < Q) sm.dts[tid] = load_dt(0, nv0);
+    }
     for (long long c = 0; c < nchunks; ++c) {
         const long long t0 = c * Q;
         const int nv = (int)(L - t0 < Q ? L - t0 : Q);
-        // ---- loads: x (transposed), B, C, dt
-        for (int i = tid; i < Q * (PH / 8); i += THREADS) {
-            const int s = i / (PH / 8), p8 = (i % (PH / 8)) * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (s < nv)
-                v = *reinterpret_cast<const uint4*>(x + ((b * L + t0 + s) * H + hh) * P + pbase + p8);
-            const bf16* e = reinterpret_cast<const bf16*>(&v);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) sm.Xt[p8 + k][s] = e[k];
-        }
-        for (int i = tid; i < Q * (N / 8); i += THREADS) {
-            const int s = i / (N / 8), n8 = (i % (N / 8)) * 8;
-            uint4 vb = make_uint4(0, 0, 0, 0), vc = make_uint4(0, 0, 0, 0);
-            if (s < nv) {
-                vb = *reinterpret_cast<const uint4*>(Bm + (b * L + t0 + s) * N + n8);
-                vc = *reinterpret_cast<const uint4*>(Cm + (b * L + t0 + s) * N + n8);
-            }
-            *reinterpret_cast<uint4*>(&sm.Bs[s][n8]) = vb;
-            *reinterpret_cast<uint4*>(&sm.Cs[s][n8]) = vc;
-        }
-        if (tid < Q) {
-            float d = 0.0f;
-            if (tid < nv) {
-                const float v2 = fmaf(__bfloat162float(dtr[(b * L + t0 + tid) * H + hh]), kLog2e, kb2);
-                d = (v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2))) * 0.6931471805599453f;
-            }
-            sm.dts[tid] = d;
-        }
         __syncthreads();
         // ---- cumulative decay (warp 0: a scan over 64 steps, two per lane)
         if (warp == 0) {
@@ -283,7 +312,24 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                 }
             }
         }
-        __syncthreads();   // Hh/Hl: all readers done; Xwh/Xwl: all writers done
+        __syncthreads();   // Hh/Hl and the C tile: all readers done; Xwh/Xwl: all writers done
+        // ---- the next chunk's C rows (asynchronously), x and dt (in registers)
+        const bool more = c + 1 < nchunks;
+        const long long tn = t0 + Q;
+        const int nvn = more ? (int)(L - tn < Q ? L - tn : Q) : 0;
+        uint4 xr[XPT];
+        float dr = 0.0f;
+        if (more) {
+            for (int i = tid; i < Q * (N / 8); i += THREADS) {
+                const int s2 = i / (N / 8), n8 = (i % (N / 8)) * 8;
+                const bool ok = s2 < nvn;
+                cp_async16(&sm.Cs[s2][n8], Cm + (b * L + (ok ? tn + s2 : 0)) * N + n8, ok);
+            }
+            cp_async_commit();
+#pragma unroll
+            for (int k = 0; k < XPT; ++k) xr[k] = load_x(tn, nvn, tid + THREADS * k);
+            if (tid < Q) dr = load_dt(tn, nvn);
+        }
         // ---- the state: H <- exp(cum_end) H + B^T (w o X)   (K = Q), w o X as hi + lo
         {
             const float dec = sm.ecum[Q - 1];
@@ -325,7 +371,14 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                 }
             }
         }
-        __syncthreads();   // Hh/Hl complete; the chunk's tiles are free
+        __syncthreads();   // Hh/Hl complete; the B and x tiles are free
+        if (more) {
+#pragma unroll
+            for (int k = 0; k < XPT; ++k) store_x(tid + THREADS * k, xr[k]);
+            if (tid < Q) sm.dts[tid] = dr;
+            load_rows(Bm, sm.Bs, tn, nvn);
+            cp_async_wait_all();
+        }
     }
     if (h_last) {
 #pragma unroll
