@@ -96,9 +96,12 @@ struct Smem {
     static constexpr int NP = N + 8, QP = Q + 8;
     bf16 Xt[PH][QP];                // x of the chunk, transposed: [p][s]
     bf16 Xwh[PH][QP], Xwl[PH][QP];  // w o x, transposed, as hi + lo bf16 parts
-    bf16 Bs[Q][NP];                 // B rows: [s][n]
     bf16 Cs[Q][NP];                 // C rows: [t][n]
-    bf16 Hh[PH][NP], Hl[PH][NP];    // the state entering the chunk, [p][n], hi + lo
+    // Two buffers that take turns: one holds the chunk's B rows [s][n], the
+    // other the state entering it, [p][n] hi in rows 0..PH-1 and lo in rows
+    // PH..2PH-1.  While the state is updated, the next chunk's B rows stream
+    // into the (spent) state buffer; the new state then goes into the B one.
+    bf16 Pb[2][Q][NP];
     float dts[Q], cum[Q], w[Q], ecum[Q];
 };
 
@@ -130,10 +133,9 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) Hs[mt][nt][i] = 0.0f;
-    for (int i = tid; i < PH * (N + 8); i += THREADS) {
-        (&sm.Hh[0][0])[i] = __float2bfloat16_rn(0.0f);
-        (&sm.Hl[0][0])[i] = __float2bfloat16_rn(0.0f);
-    }
+    static_assert(Q == 2 * PH, "a state buffer (hi + lo) has the shape of a B tile");
+    int cb = 0;   // the buffer holding the current chunk's B rows; 1 - cb holds its state
+    for (int i = tid; i < Q * (N + 8); i += THREADS) (&sm.Pb[1][0][0])[i] = __float2bfloat16_rn(0.0f);
 
     const long long nchunks = (L + Q - 1) / Q;
     // Staging of a chunk: x transposed into Xt, B and C rows, dt after the
@@ -179,7 +181,7 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
         const int nv0 = (int)(L < Q ? L : Q);
 #pragma unroll
         for (int k = 0; k < XPT; ++k) store_x(tid + THREADS * k, load_x(0, nv0, tid + THREADS * k));
-        load_rows(Bm, sm.Bs, 0, nv0);
+        load_rows(Bm, sm.Pb[0], 0, nv0);
         load_rows(Cm, sm.Cs, 0, nv0);
         if (tid < Q) sm.dts[tid] = load_dt(0, nv0);
     }
@@ -231,10 +233,11 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                 const uint32_t a3 = ld32(&sm.Cs[r0 + g + 8][k0 + 2 * tq + 8]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    mma16816(Y[nt], a0, a1, a2, a3, ld32(&sm.Hh[8 * nt + g][k0 + 2 * tq]),
-                             ld32(&sm.Hh[8 * nt + g][k0 + 2 * tq + 8]));
-                    mma16816(Y[nt], a0, a1, a2, a3, ld32(&sm.Hl[8 * nt + g][k0 + 2 * tq]),
-                             ld32(&sm.Hl[8 * nt + g][k0 + 2 * tq + 8]));
+                    const bf16 (*Hb)[N + 8] = sm.Pb[1 - cb];
+                    mma16816(Y[nt], a0, a1, a2, a3, ld32(&Hb[8 * nt + g][k0 + 2 * tq]),
+                             ld32(&Hb[8 * nt + g][k0 + 2 * tq + 8]));
+                    mma16816(Y[nt], a0, a1, a2, a3, ld32(&Hb[PH + 8 * nt + g][k0 + 2 * tq]),
+                             ld32(&Hb[PH + 8 * nt + g][k0 + 2 * tq + 8]));
                 }
             }
             const float e_lo = sm.ecum[r0 + g], e_hi = sm.ecum[r0 + g + 8];
@@ -266,8 +269,8 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {
                             const int j = 2 * kt + jj;
-                            mma16816(S[jj], a0, a1, a2, a3, ld32(&sm.Bs[8 * j + g][k0 + 2 * tq]),
-                                     ld32(&sm.Bs[8 * j + g][k0 + 2 * tq + 8]));
+                            mma16816(S[jj], a0, a1, a2, a3, ld32(&sm.Pb[cb][8 * j + g][k0 + 2 * tq]),
+                                     ld32(&sm.Pb[cb][8 * j + g][k0 + 2 * tq + 8]));
                         }
                     }
                     // S[t][s] *= exp(cum_t - cum_s) dt_s for s <= t, else 0
@@ -312,8 +315,8 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                 }
             }
         }
-        __syncthreads();   // Hh/Hl and the C tile: all readers done; Xwh/Xwl: all writers done
-        // ---- the next chunk's C rows (asynchronously), x and dt (in registers)
+        __syncthreads();   // the state buffer and the C tile: all readers done; Xwh/Xwl written
+        // ---- the next chunk's B and C rows (asynchronously), x and dt (in registers)
         const bool more = c + 1 < nchunks;
         const long long tn = t0 + Q;
         const int nvn = more ? (int)(L - tn < Q ? L - tn : Q) : 0;
@@ -323,7 +326,9 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
             for (int i = tid; i < Q * (N / 8); i += THREADS) {
                 const int s2 = i / (N / 8), n8 = (i % (N / 8)) * 8;
                 const bool ok = s2 < nvn;
-                cp_async16(&sm.Cs[s2][n8], Cm + (b * L + (ok ? tn + s2 : 0)) * N + n8, ok);
+                const long long row = (b * L + (ok ? tn + s2 : 0)) * N + n8;
+                cp_async16(&sm.Cs[s2][n8], Cm + row, ok);
+                cp_async16(&sm.Pb[1 - cb][s2][n8], Bm + row, ok);
             }
             cp_async_commit();
 #pragma unroll
@@ -345,7 +350,7 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                 for (int k0 = 0; k0 < Q; k0 += 16) {
                     // A = B^T rows m0.., keys k0..: tiles Bs[k0 + 8 (i/16) ..][m0 + 8 ((i/8)&1)]
                     uint32_t af[4];
-                    ldsm_x4_trans(af, &sm.Bs[k0 + 8 * (tile >> 1) + row][m0 + 8 * (tile & 1)]);
+                    ldsm_x4_trans(af, &sm.Pb[cb][k0 + 8 * (tile >> 1) + row][m0 + 8 * (tile & 1)]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         mma16816(Hs[mt][nt], af[0], af[1], af[2], af[3],
@@ -356,7 +361,14 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                                  ld32(&sm.Xwl[8 * nt + g][k0 + 2 * tq + 8]));
                     }
                 }
-                // the copy the next chunk reads, transposed to [p][n], hi + lo
+            }
+        }
+        __syncthreads();   // every read of this chunk's B rows is done
+        // ---- the copy of the state the next chunk reads, [p][n] hi + lo, into the B buffer
+        {
+#pragma unroll
+            for (int mt = 0; mt < MTW; ++mt) {
+                const int m0 = RW * warp + 16 * mt;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int p0 = 8 * nt + 2 * tq;
@@ -365,20 +377,19 @@ ssd_chunk_kernel(const bf16* __restrict__ x, const bf16* __restrict__ dtr,
                         const int pp = p0 + (i & 1), mm = m0 + g + 8 * (i >> 1);
                         const float v = Hs[mt][nt][i];
                         const bf16 hi = __float2bfloat16_rn(v);
-                        sm.Hh[pp][mm] = hi;
-                        sm.Hl[pp][mm] = __float2bfloat16_rn(v - __bfloat162float(hi));
+                        sm.Pb[cb][pp][mm] = hi;
+                        sm.Pb[cb][PH + pp][mm] = __float2bfloat16_rn(v - __bfloat162float(hi));
                     }
                 }
             }
         }
-        __syncthreads();   // Hh/Hl complete; the B and x tiles are free
         if (more) {
 #pragma unroll
             for (int k = 0; k < XPT; ++k) store_x(tid + THREADS * k, xr[k]);
             if (tid < Q) sm.dts[tid] = dr;
-            load_rows(Bm, sm.Bs, tn, nvn);
             cp_async_wait_all();
         }
+        cb = 1 - cb;
     }
     if (h_last) {
 #pragma unroll
