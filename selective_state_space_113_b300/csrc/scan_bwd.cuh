@@ -184,14 +184,23 @@ adjoint_summary_kernel(const BwdParams p) {
     const long long G = gridDim.x;
     const long long nsum = p.nCB * p.batch * (p.P - 1);
     const long long r0 = blockIdx.x * nsum / G, r1 = (blockIdx.x + 1) * nsum / G;
+    // a CTA's units are consecutive and mostly share their channel block: its
+    // A rows and parameters are loaded again only when the block changes
+    long long cur_cb = -1;
+    long long d = 0;
+    bool valid = false;
+    float arow[NS];
+    Chan c{};
     for (long long i = r0; i < r1; ++i) {
         // skip unit 0 of every chain: index i counts units with k >= 1
         const long long cbb = i / (p.P - 1);
         const Unit w = unit_of(p, cbb * p.P + 1 + (i - cbb * (p.P - 1)));
-        const long long d = w.cb * CB + threadIdx.x;
-        const bool valid = d < p.D;
-        float arow[NS];
-        const Chan c = load_chan(p, d, valid, arow);
+        if (w.cb != cur_cb) {
+            cur_cb = w.cb;
+            d = w.cb * CB + threadIdx.x;
+            valid = d < p.D;
+            c = load_chan(p, d, valid, arow);
+        }
         __syncthreads();
         load_rows<T>(p, w, nullptr, nullptr, Cs, false);
         __syncthreads();
