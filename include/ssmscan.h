@@ -176,7 +176,9 @@ SSM_API int ssm_conv_scan_fwd(const void *x, const float *conv_w, const float *c
  *   ddt_bias, dDskip : [D] float32, written (sums over batch and steps);
  *                 NULL: not computed
  * Sizes as for ssm_scan_fwd.  With L == 0 or batch == 0 the sums are zero.
- * Takes a stream-ordered workspace (SSM_ERR_NOMEM if that fails): about
+ * N == 16 with u, delta, z, dy, B, C, A and du 16-byte aligned and
+ * D * sizeof(dtype) a multiple of 16 runs the unit kernels; anything else
+ * runs a one-thread-per-channel kernel.  Takes a stream-ordered workspace (SSM_ERR_NOMEM if that fails): about
  * 3.2 * batch * L * D * N bytes / 16 for N == 16 (the states entering every
  * 32-step unit, the adjoints leaving it and their summaries), plus
  * 128 * ceil(D / 128) * batch * L bytes of per-block dB/dC sums.  The sums

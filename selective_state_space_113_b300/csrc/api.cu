@@ -209,7 +209,7 @@ extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bi
     if (bd == 0 || L == 0) return SSM_OK;
     const int plan = ssm::tile::forced_plan();
     if (N == ssm::bwd::NS && plan != ssm::tile::kPlanGeneric &&
-        all_aligned16({u, delta, z, B, C, A, du}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
+        all_aligned16({u, delta, z, dy, B, C, A, du}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
         if (dtype == SSM_F32)
             return ssm::bwd::launch_scan_bwd16<float>(
                 static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,

@@ -177,13 +177,89 @@ __device__ __forceinline__ void load_rows(const BwdParams& p, const Unit& w, flo
 // ------------------------------------------------------------ phase 2
 // Adjoint summary of each unit k >= 1, walked backward from lam = 0:
 // adj[k] = {sum dl, Abar_{t0} lam_{t0}}.
+//
+// A CTA takes its units as a list of half-unit stages (the steps HS..TU-1 of
+// a unit, then 0..HS-1).  While one stage computes, the next one's delta, dy
+// and z rows are copied into the other shared buffer by cp.async and its C
+// rows come into registers, to be widened into the other C buffer when the
+// stage ends; the loads of a stage are thus in flight during a whole stage of
+// arithmetic, at no cost in registers.
+constexpr int HS = TU / 2;   // steps per stage
+
+template <typename T>
+struct AdjSmem {
+    T dv[2][HS][CB], dy[2][HS][CB], z[2][HS][CB];
+    float Cs[2][HS * NS];
+};
+
+// 16-byte global -> shared copy, zero-filled (nothing read) when !ok.
+__device__ __forceinline__ void cpa16(void* dst, const void* src, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
+                 "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// every group but the newest one complete (this thread's copies)
+__device__ __forceinline__ void cpa_wait_prior() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Unit of index i in the list of units with k >= 1.
+__device__ __forceinline__ Unit adj_unit(const BwdParams& p, long long i) {
+    const long long cbb = i / (p.P - 1);
+    return unit_of(p, cbb * p.P + 1 + (i - cbb * (p.P - 1)));
+}
+
+// Issues stage (w, h) into buffer s: its rows t0 + h*HS .. min(t1, +HS) - 1,
+// channels cb*CB .. +CB-1 (16-byte pieces past D or past the rows are
+// zero-filled; D is a multiple of the piece), and loads its C rows into cpre.
+template <typename T>
+__device__ __forceinline__ void adj_issue(const BwdParams& p, const Unit& w, int h,
+                                          AdjSmem<T>& sm, int s, float (&cpre)[2]) {
+    constexpr int EPP = 16 / (int)sizeof(T);   // elements per 16-byte piece
+    constexpr int CPR = CB / EPP;              // pieces per row
+    const long long ta = w.t0 + (long long)h * HS;
+    const long long rows = w.t1 - ta < HS ? w.t1 - ta : HS;
+    const long long d0 = w.cb * CB;
+    const long long base = (w.b * p.L + ta) * p.D + d0;
+    const T* dv = static_cast<const T*>(p.delta);
+    const T* dy = static_cast<const T*>(p.dy);
+    const T* z = static_cast<const T*>(p.z);
+    for (int q = threadIdx.x; q < HS * CPR; q += CB) {
+        const int r = q / CPR, c = q - r * CPR;
+        const bool ok = r < rows && d0 + c * EPP < p.D;
+        const long long off = ok ? base + r * p.D + c * EPP : 0;
+        cpa16(&sm.dv[s][r][c * EPP], dv + off, ok);
+        cpa16(&sm.dy[s][r][c * EPP], dy + off, ok);
+        if (z) cpa16(&sm.z[s][r][c * EPP], z + off, ok);
+    }
+    const T* Cg = static_cast<const T*>(p.Cm) + (w.b * p.L + ta) * NS;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int e = threadIdx.x + k * CB;
+        cpre[k] = e < rows * NS ? ldf(Cg + e) : 0.0f;
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(CB)
 adjoint_summary_kernel(const BwdParams p) {
-    __shared__ float Cs[TU * NS];
+    static_assert(HS * NS == 2 * CB, "two C values per thread and stage");
+    extern __shared__ __align__(16) unsigned char adj_smem_raw[];
+    AdjSmem<T>& sm = *reinterpret_cast<AdjSmem<T>*>(adj_smem_raw);
     const long long G = gridDim.x;
     const long long nsum = p.nCB * p.batch * (p.P - 1);
     const long long r0 = blockIdx.x * nsum / G, r1 = (blockIdx.x + 1) * nsum / G;
+    if (r0 >= r1) return;
+    const bool hasz = p.z != nullptr;
+    // stage being computed: unit i (w), half h, buffer s
+    long long i = r0;
+    Unit w = adj_unit(p, r0);
+    int h = (int)((w.t1 - w.t0 - 1) / HS);
+    int s = 0;
+    float cpre[2];
+    adj_issue<T>(p, w, h, sm, 0, cpre);
+    cpa_commit();
+    sm.Cs[0][threadIdx.x] = cpre[0];
+    sm.Cs[0][threadIdx.x + CB] = cpre[1];
     // a CTA's units are consecutive and mostly share their channel block: its
     // A rows and parameters are loaded again only when the block changes
     long long cur_cb = -1;
@@ -191,48 +267,47 @@ adjoint_summary_kernel(const BwdParams p) {
     bool valid = false;
     float arow[NS];
     Chan c{};
-    for (long long i = r0; i < r1; ++i) {
-        // skip unit 0 of every chain: index i counts units with k >= 1
-        const long long cbb = i / (p.P - 1);
-        const Unit w = unit_of(p, cbb * p.P + 1 + (i - cbb * (p.P - 1)));
+    float lam[NS];
+#pragma unroll
+    for (int n = 0; n < NS; ++n) lam[n] = 0.0f;
+    float S2 = 0.0f;
+    for (;;) {
+        // the next stage, issued before this one computes
+        long long ni = i;
+        Unit nw = w;
+        int nh = h - 1;
+        if (nh < 0) {
+            ni = i + 1;
+            if (ni < r1) {
+                nw = adj_unit(p, ni);
+                nh = (int)((nw.t1 - nw.t0 - 1) / HS);
+            }
+        }
+        const bool more = ni < r1;
+        if (more) adj_issue<T>(p, nw, nh, sm, s ^ 1, cpre);
+        cpa_commit();
         if (w.cb != cur_cb) {
             cur_cb = w.cb;
             d = w.cb * CB + threadIdx.x;
             valid = d < p.D;
             c = load_chan(p, d, valid, arow);
         }
+        cpa_wait_prior();
         __syncthreads();
-        load_rows<T>(p, w, nullptr, nullptr, Cs, false);
-        __syncthreads();
-        const T* dl_src = static_cast<const T*>(p.delta) + w.b * p.L * p.D + (valid ? d : 0);
-        const T* dy_src = static_cast<const T*>(p.dy) + w.b * p.L * p.D + (valid ? d : 0);
-        const T* z_src = p.z ? static_cast<const T*>(p.z) + w.b * p.L * p.D + (valid ? d : 0)
-                             : nullptr;
-        float lam[NS];
+        const long long ta = w.t0 + (long long)h * HS;
+        const int rows = (int)(w.t1 - ta < HS ? w.t1 - ta : HS);
 #pragma unroll
-        for (int n = 0; n < NS; ++n) lam[n] = 0.0f;
-        float S2 = 0.0f;
-        const int nsteps = (int)(w.t1 - w.t0);
-        for (int tb = ((nsteps - 1) / KS) * KS; tb >= 0; tb -= KS) {
-          // the sub-chunk's loads first, then its steps from the last
-          float dvj[KS], dyj[KS], zj[KS];
-#pragma unroll
-          for (int j = 0; j < KS; ++j) {
-            const long long t = w.t0 + tb + j;
-            const bool in = valid && tb + j < nsteps;
-            dvj[j] = in ? ldf(dl_src + t * p.D) : 0.0f;
-            dyj[j] = in ? ldf(dy_src + t * p.D) : 0.0f;
-            zj[j] = (in && z_src) ? ldf(z_src + t * p.D) : 0.0f;
-          }
-#pragma unroll
-          for (int j = KS - 1; j >= 0; --j) {
-            if (tb + j >= nsteps) continue;
+        for (int j = HS - 1; j >= 0; --j) {
+            if (j >= rows) continue;
             float g = 1.0f;
-            if (z_src) g = zj[j] * ptx::rcp(1.0f + ptx::ex2(-zj[j] * kLog2e));
-            const float ds = dyj[j] * g;
-            const float dl = softplus_l2(fmaf(dvj[j], kLog2e, c.kb2));
+            if (hasz) {
+                const float zj = ldf(&sm.z[s][j][threadIdx.x]);
+                g = zj * ptx::rcp(1.0f + ptx::ex2(-zj * kLog2e));
+            }
+            const float ds = ldf(&sm.dy[s][j][threadIdx.x]) * g;
+            const float dl = softplus_l2(fmaf(ldf(&sm.dv[s][j][threadIdx.x]), kLog2e, c.kb2));
             S2 += dl;
-            const float* Ct = Cs + (tb + j) * NS;
+            const float* Ct = sm.Cs[s] + j * NS;
             if (c.geo) {
                 const float e0 = em1_near0(dl * c.a0 * kLn2, ptx::ex2(dl * c.a0));
                 const float r = e0 + 1.0f;
@@ -256,14 +331,28 @@ adjoint_summary_kernel(const BwdParams p) {
                     lam[n] *= ptx::ex2(dl * arow[n]);
                 }
             }
-          }
         }
-        if (valid) {
-            float* o = p.adj + (w.k * p.batch * p.D + w.b * p.D + d) * (NS + 1);
-            o[0] = S2;
+        if (h == 0) {   // the unit is done
+            if (valid) {
+                float* o = p.adj + (w.k * p.batch * p.D + w.b * p.D + d) * (NS + 1);
+                o[0] = S2;
 #pragma unroll
-            for (int n = 0; n < NS; ++n) o[1 + n] = lam[n];
+                for (int n = 0; n < NS; ++n) o[1 + n] = lam[n];
+            }
+#pragma unroll
+            for (int n = 0; n < NS; ++n) lam[n] = 0.0f;
+            S2 = 0.0f;
         }
+        if (more) {
+            sm.Cs[s ^ 1][threadIdx.x] = cpre[0];
+            sm.Cs[s ^ 1][threadIdx.x + CB] = cpre[1];
+        }
+        __syncthreads();   // buffer s is free for the stage after next
+        if (!more) break;
+        i = ni;
+        w = nw;
+        h = nh;
+        s ^= 1;
     }
 }
 

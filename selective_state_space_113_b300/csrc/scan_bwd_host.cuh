@@ -24,7 +24,7 @@ inline cudaError_t resident(K kern, int threads, int smem, int* per_sm) {
 }
 
 // Returns an ssm_status_t.  Preconditions (checked by the caller): N == 16;
-// u, delta, z, B, C, A and du 16-byte aligned; D * sizeof(T) % 16 == 0;
+// u, delta, z, dy, B, C, A and du 16-byte aligned; D * sizeof(T) % 16 == 0;
 // batch*D > 0; L > 0; dz given when z is.
 template <typename T>
 int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const float* A,
@@ -41,7 +41,7 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
     if (prepare<T, (int)kAggregate, (int)kZOH>(sms, &wa) != cudaSuccess || wa < 1)
         return SSM_ERR_CUDA;
     int occ_sum = 0, occ_unit = 0;
-    if (resident(adjoint_summary_kernel<T>, CB, 0, &occ_sum) != cudaSuccess ||
+    if (resident(adjoint_summary_kernel<T>, CB, (int)sizeof(AdjSmem<T>), &occ_sum) != cudaSuccess ||
         resident(bwd_unit_kernel<T>, CB, (int)sizeof(BwdSmem), &occ_unit) != cudaSuccess ||
         occ_sum < 1 || occ_unit < 1)
         return SSM_ERR_CUDA;
@@ -135,7 +135,8 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
         if (P > 1) {
             const long long nsum = nCB * batch * (P - 1);
             const long long g = (long long)sms * occ_sum;
-            adjoint_summary_kernel<T><<<(unsigned)(nsum < g ? nsum : g), CB, 0, stream>>>(bp);
+            adjoint_summary_kernel<T><<<(unsigned)(nsum < g ? nsum : g), CB, sizeof(AdjSmem<T>),
+                                        stream>>>(bp);
             if (cudaGetLastError() != cudaSuccess) {
                 status = SSM_ERR_CUDA;
                 break;
