@@ -106,6 +106,25 @@ def test_bwd_general_A_and_nulls(monkeypatch, plan):
     compare(out, oracle_bwd(inp), 1e-4, "outputs left out")
 
 
+def _shifted(t):
+    """A copy of t whose data starts one element past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 16 != 0
+    return v
+
+
+@pytest.mark.parametrize("which", ["dy", "u", "z"])
+def test_bwd_unaligned_operand(which):
+    """An operand that is element-aligned but not 16-byte aligned sends the call
+    to the generic kernel (the fast kernels copy 16-byte pieces); the result
+    still follows the oracle."""
+    inp = inputs(2, 90, 64, 16, torch.bfloat16, 17)
+    inp[which] = _shifted(inp[which])
+    compare(run_bwd(inp), oracle_bwd(inp), parity.TOL[torch.bfloat16], f"unaligned {which}")
+
+
 @pytest.mark.parametrize("N", [7, 33])
 def test_bwd_other_state_sizes(N):
     inp = inputs(2, 40, 24, N, torch.float32, N)
