@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.ssm_abi_version() == 1
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = lib.ssm_status_string(code)
         assert s and s != b"unknown status"
     assert lib.ssm_status_string(12345) == b"unknown status"
@@ -92,3 +92,105 @@ def test_step_argument_validation(lib):
     assert step(lib, N=300) == -5
     assert step(lib, dtype=-1) == -3
     assert step(lib, state=FAKE + 2) == -4
+
+
+def disc(lib, code, batch=0, **kw):
+    a = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, y=FAKE)
+    a.update(kw)
+    return lib.ssm_scan_fwd_disc(a["u"], a["delta"], None, a["A"], a["B"], a["C"], None, None,
+                                 a["y"], None, batch, 4, 8, 16, 1, code, None)
+
+
+def test_disc_argument_validation(lib):
+    for code in (0, 1, 2):
+        assert disc(lib, code) == 0
+    assert disc(lib, 3) == -5
+    assert disc(lib, -1) == -5
+    assert disc(lib, 1, batch=1, u=None) == -1
+    assert disc(lib, 2, u=FAKE + 1) == -4
+
+
+def conv(lib, w=FAKE, b=None, act=1, batch=0, x=FAKE, D=8):
+    return lib.ssm_conv_scan_fwd(x, w, b, act, FAKE, None, FAKE, FAKE, FAKE, None, None, FAKE,
+                                 None, batch, 4, D, 16, 1, None)
+
+
+def test_conv_argument_validation(lib):
+    assert conv(lib) == 0
+    assert conv(lib, act=0) == 0
+    assert conv(lib, w=None) == -1            # the filter is required when D > 0
+    assert conv(lib, w=None, D=0) == 0
+    assert conv(lib, act=2) == -5
+    assert conv(lib, w=FAKE + 2) == -4        # float32 filter needs 4-byte alignment
+    assert conv(lib, b=FAKE + 1) == -4
+    assert conv(lib, batch=1, x=None) == -1
+
+
+BWD_ARGS = ("u", "delta", "dt_bias", "A", "B", "C", "Dskip", "z", "dy", "dh_last", "du", "ddelta",
+            "ddt_bias", "dA", "dB", "dC", "dDskip", "dz")
+
+
+def bwd(lib, batch=1, L=4, D=8, N=16, dtype=1, **kw):
+    a = {k: FAKE for k in BWD_ARGS}
+    for k in ("dt_bias", "Dskip", "z", "dh_last", "ddt_bias", "dB", "dC", "dDskip", "dz"):
+        a[k] = None
+    a.update(kw)
+    return lib.ssm_scan_bwd(*[a[k] for k in BWD_ARGS], batch, L, D, N, dtype, None)
+
+
+def test_bwd_argument_validation(lib):
+    """Only the rejections: a valid call clears the derivative sums with CUDA."""
+    for k in ("u", "delta", "dy", "du", "ddelta", "B", "C", "A", "dA"):
+        assert bwd(lib, **{k: None}) == -1, k
+    assert bwd(lib, z=FAKE) == -1                       # z given without dz
+    assert bwd(lib, batch=-1) == -2
+    assert bwd(lib, N=0) == -2
+    assert bwd(lib, N=257) == -5
+    assert bwd(lib, dtype=2) == -3
+    assert bwd(lib, batch=1 << 30, L=1 << 30, D=1) == -2   # index range of the workspace
+    assert bwd(lib, dy=FAKE + 1) == -4
+    assert bwd(lib, dz=FAKE + 1, z=FAKE) == -4
+    assert bwd(lib, dB=FAKE + 2) == -4
+    assert bwd(lib, dh_last=FAKE + 2) == -4
+
+
+def ssd(lib, batch=0, L=4, H=2, P=64, N=64, dtype=1, **kw):
+    a = dict(x=FAKE, dt=FAKE, dt_bias=None, A=FAKE, B=FAKE, C=FAKE, Dskip=None, y=FAKE,
+             h_last=None)
+    a.update(kw)
+    return lib.ssm_ssd_fwd(a["x"], a["dt"], a["dt_bias"], a["A"], a["B"], a["C"], a["Dskip"],
+                           a["y"], a["h_last"], batch, L, H, P, N, dtype, None)
+
+
+def test_ssd_argument_validation(lib):
+    assert ssd(lib) == 0                     # no channels: nothing to do
+    assert ssd(lib, A=None) == -1            # A has H elements even when batch == 0
+    for k in ("x", "dt", "B", "C", "y"):
+        assert ssd(lib, **{k: None}) == 0
+        assert ssd(lib, batch=1, **{k: None}) == -1, k
+    assert ssd(lib, P=0) == -2
+    assert ssd(lib, H=-1) == -2
+    assert ssd(lib, N=0) == -2
+    assert ssd(lib, N=257) == -5
+    assert ssd(lib, dtype=7) == -3
+    assert ssd(lib, batch=1 << 40, L=1 << 40) == -2
+    assert ssd(lib, x=FAKE + 1) == -4
+    assert ssd(lib, dt_bias=FAKE + 2) == -4
+
+
+def noalloc(lib, batch=0, L=4, D=8, h=None, **kw):
+    a = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, y=FAKE)
+    a.update(kw)
+    return lib.ssm_scan_fwd_noalloc(a["u"], a["delta"], None, a["A"], a["B"], a["C"], None, None,
+                                    a["y"], h, batch, L, D, 16, 1, None)
+
+
+def test_noalloc_argument_validation(lib):
+    assert noalloc(lib) == 0
+    assert noalloc(lib, A=None) == -1
+    assert noalloc(lib, batch=1, y=None) == -1
+    assert noalloc(lib, batch=-1) == -2
+    assert noalloc(lib, u=FAKE + 1) == -4
+    # a fast-path problem whose carried states (64 bytes per channel without
+    # h_last) cannot fit the fixed scratch is refused before any CUDA call
+    assert noalloc(lib, batch=1024, D=8192) == -9
