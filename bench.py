@@ -288,10 +288,10 @@ def bench_ours(args, rank, world, local):
     return {
         "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,1) u/delta/z/B/C, Mamba dt_bias init, A=-(n+1))",
         "config": {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.D, "N": w.N,
-                   "state": "fp32", "arith": "fp32",
+                   "io": "bf16", "state": "fp32", "arith": "fp32",
                    "l2": f"inputs {alg / 1e6:.0f} MB per step > 126 MB L2; no flush",
                    "parallelism": f"replicas x{world} (independent workloads per GPU)"},
         "hbm_gbs": achieved_gbs,
