@@ -124,6 +124,20 @@ def algorithmic_bytes(w) -> int:
 SCAN_KERNEL_SOURCES = ("scan_tile.cuh", "scan_tile_host.cuh", "ptx.cuh", "common.cuh")
 
 
+L2_MB = 126.0
+
+
+def bench_config(w, world: int) -> dict:
+    """The workload as both arms' lines name it."""
+    io = {"torch.bfloat16": "bf16", "torch.float32": "f32"}[str(w.dtype)]
+    mb = algorithmic_bytes(w) / 1e6
+    l2 = (f"inputs {mb:.0f} MB per step > 126 MB L2; no flush" if mb > L2_MB else
+          f"inputs {mb:.0f} MB per step fit the 126 MB L2; not flushed")
+    return {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.D, "N": w.N,
+            "io": io, "state": "fp32", "arith": "fp32", "l2": l2,
+            "parallelism": f"replicas x{world} (independent workloads per GPU)"}
+
+
 def csrc_digest() -> str:
     h = hashlib.sha256()
     for name in SCAN_KERNEL_SOURCES:
@@ -290,10 +304,7 @@ def bench_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,1) u/delta/z/B/C, Mamba dt_bias init, A=-(n+1))",
-        "config": {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.D, "N": w.N,
-                   "io": "bf16", "state": "fp32", "arith": "fp32",
-                   "l2": f"inputs {alg / 1e6:.0f} MB per step > 126 MB L2; no flush",
-                   "parallelism": f"replicas x{world} (independent workloads per GPU)"},
+        "config": bench_config(w, world),
         "hbm_gbs": achieved_gbs,
         "hbm_frac_measured": achieved_gbs / peak,
         "hbm_frac_nominal_8tbs": achieved_gbs / NOMINAL_HBM_GBS,
@@ -684,7 +695,7 @@ def bench_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "L": w.L, "D": w.D, "N": w.N},
+        "config": bench_config(w, world),
         "cpu_baseline": {"value": value, "unit": "elements/s", "cores": n, "kind": "oracle",
                          "sample": f"per step: all {w.batch}x{w.L} steps of {channels} of "
                                    f"{w.D} channels"},
