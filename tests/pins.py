@@ -666,20 +666,18 @@ def pin_bwd_homogeneity(lib):
         _close(got, want, 1e-10, 1e-10, f"homogeneity in {key}")
 
 
-def pin_bwd_matches_autograd(lib):
-    """All gradients against torch.autograd of a float64 torch statement of
-    the forward (the derivative is the library's, not a hand derivation)."""
-    rng = np.random.default_rng(13)
-    p = random_problem(rng, 2, 9, 3, 4)
+def _bwd_against_autograd(lib, batch, L, D, N, seed):
+    rng = np.random.default_rng(seed)
+    p = random_problem(rng, batch, L, D, N)
     dy = _f32(rng.standard_normal(p["u"].shape))
-    dh = _f32(rng.standard_normal((2, 3, 4)))
+    dh = _f32(rng.standard_normal((batch, D, N)))
     g = _bwd(lib, p, dy, dh)
     t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in p.items()}
     dt = torch.nn.functional.softplus(t["delta"] + t["dt_bias"])       # [b, L, D]
     a = t["A"]                                                          # [D, N]
-    h = torch.zeros((2, 3, 4), dtype=torch.float64)
+    h = torch.zeros((batch, D, N), dtype=torch.float64)
     ys = []
-    for step in range(p["u"].shape[1]):
+    for step in range(L):
         x = dt[:, step, :, None] * a                                    # [b, D, N]
         h = torch.exp(x) * h + torch.expm1(x) / a * t["B"][:, step, None, :] * t["u"][:, step, :, None]
         s = (h * t["C"][:, step, None, :]).sum(-1) + t["Dskip"] * t["u"][:, step]
@@ -689,7 +687,20 @@ def pin_bwd_matches_autograd(lib):
         (h * torch.tensor(dh, dtype=torch.float64)).sum()
     grads = torch.autograd.grad(loss, [t[k] for k in GRAD_OF])
     for key, gr in zip(GRAD_OF, grads):
-        _close(g[GRAD_OF[key]], gr.numpy(), 1e-9, 1e-9, f"autograd, {GRAD_OF[key]}")
+        _close(g[GRAD_OF[key]], gr.numpy(), 1e-9, 1e-9, f"autograd N={N}, {GRAD_OF[key]}")
+
+
+def pin_bwd_matches_autograd(lib):
+    """All gradients against torch.autograd of a float64 torch statement of
+    the forward (the derivative is the library's, not a hand derivation)."""
+    _bwd_against_autograd(lib, 2, 9, 3, 4, 13)
+
+
+def pin_bwd_largest_state(lib):
+    """The same comparison at the largest state size the library takes
+    (N = 256, D != N), where a state-index stride or a per-state buffer
+    mistake would show."""
+    _bwd_against_autograd(lib, 1, 6, 3, 256, 15)
 
 
 def pin_bwd_optional_inputs(lib):
@@ -708,7 +719,7 @@ def pin_bwd_optional_inputs(lib):
 
 
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_homogeneity, pin_bwd_matches_autograd,
-            pin_bwd_optional_inputs]
+            pin_bwd_largest_state, pin_bwd_optional_inputs]
 
 
 # ------------------------------------------------------ SSD (Mamba-2) pins
