@@ -2,10 +2,16 @@
 
 ``python -m selective_state_space_113_b300.build`` compiles the single
 translation unit ``csrc/api.cu`` (which includes every kernel file) into
-``selective_state_space_113_b300/libssmscan.so``.
+``selective_state_space_113_b300/libssmscan.so``.  A build is skipped when the
+library is current: when a stamp written by the last successful build (a
+SHA-256 of the nvcc flags and of every source's contents, kept in ``_build/``)
+matches, or, with no stamp, when no source is newer than the library.  So a
+checkout that only rewrites files, changing their times but not their
+contents, does not trigger the (several-minute) compile.
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -33,9 +39,36 @@ def sources() -> list[str]:
     return out
 
 
-def up_to_date(out: str = LIB) -> bool:
+def command(out: str = LIB, extra=()) -> list[str]:
+    return [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
+            "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+            "-Xptxas", "-warn-spills", *extra,
+            "-o", out, os.path.join(CSRC, "api.cu")]
+
+
+def digest(cmd: list[str]) -> str:
+    """SHA-256 of the compile flags (not the compiler's location) and of every
+    source file's relative path and contents."""
+    h = hashlib.sha256()
+    h.update("\0".join(cmd[1:]).encode())
+    for src in sources():
+        h.update(b"\0" + os.path.relpath(src, ROOT).encode() + b"\0")
+        with open(src, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def stamp_path(out: str = LIB) -> str:
+    return os.path.join(ROOT, "_build", os.path.basename(out) + ".stamp")
+
+
+def up_to_date(out: str = LIB, extra=()) -> bool:
     if not os.path.exists(out):
         return False
+    stamp = stamp_path(out)
+    if os.path.exists(stamp):
+        with open(stamp) as fh:
+            return fh.read().strip() == digest(command(out, extra))
     t = os.path.getmtime(out)
     return all(os.path.getmtime(s) <= t for s in sources())
 
@@ -44,13 +77,14 @@ def build(out: str = LIB, extra=(), verbose: bool = False, force: bool = False) 
     """Compile the library; returns its path.  ``extra`` adds nvcc flags."""
     if not force and not extra and up_to_date(out):
         return out
-    cmd = [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-           "-Xptxas", "-warn-spills", *extra,
-           "-o", out, os.path.join(CSRC, "api.cu")]
+    cmd = command(out, extra)
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
+    stamp = stamp_path(out)
+    os.makedirs(os.path.dirname(stamp), exist_ok=True)
+    with open(stamp, "w") as fh:
+        fh.write(digest(cmd) + "\n")
     return out
 
 
