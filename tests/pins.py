@@ -136,12 +136,10 @@ def pin_lti_convolution_with_skip_and_gate(lib):
             _close(y[b, :, d], want, 1e-10, 1e-12, f"LTI conv b={b} d={d}")
 
 
-def pin_bruteforce_unrolled(lib):
-    """Selective (time-varying) case by brute force: h_t = sum_{s<=t}
-    (prod_{r=s+1..t} Abar_r) Bbar_s B_s u_s, no recurrence; ZOH from scipy,
-    softplus from numpy, SiLU from scipy."""
-    rng = np.random.default_rng(5)
-    batch, L, D, N = 2, 12, 3, 4
+def bruteforce_check(lib, rng, batch, L, D, N):
+    """The oracle's scan on a random problem of the given shape against the
+    brute-force sum h_t = sum_{s<=t} (prod_{r=s+1..t} Abar_r) Bbar_s B_s u_s,
+    with no recurrence; ZOH from scipy, softplus from numpy, SiLU from scipy."""
     p = random_problem(rng, batch, L, D, N)
     y, h = scan(lib, p)
     for b in range(batch):
@@ -164,6 +162,11 @@ def pin_bruteforce_unrolled(lib):
                 * silu_ref(p["z"][b, :, d])
             _close(y[b, :, d], want, 1e-10, 1e-12, f"unrolled y b={b} d={d}")
             _close(h[b, d], hs[-1], 1e-10, 1e-12, f"unrolled h_last b={b} d={d}")
+
+
+def pin_bruteforce_unrolled(lib):
+    """Selective (time-varying) case by brute force (see bruteforce_check)."""
+    bruteforce_check(lib, np.random.default_rng(5), 2, 12, 3, 4)
 
 
 def pin_continuous_time_ode(lib):
@@ -666,7 +669,7 @@ def pin_bwd_homogeneity(lib):
         _close(got, want, 1e-10, 1e-10, f"homogeneity in {key}")
 
 
-def _bwd_against_autograd(lib, batch, L, D, N, seed):
+def bwd_against_autograd(lib, batch, L, D, N, seed):
     rng = np.random.default_rng(seed)
     p = random_problem(rng, batch, L, D, N)
     dy = _f32(rng.standard_normal(p["u"].shape))
@@ -693,14 +696,14 @@ def _bwd_against_autograd(lib, batch, L, D, N, seed):
 def pin_bwd_matches_autograd(lib):
     """All gradients against torch.autograd of a float64 torch statement of
     the forward (the derivative is the library's, not a hand derivation)."""
-    _bwd_against_autograd(lib, 2, 9, 3, 4, 13)
+    bwd_against_autograd(lib, 2, 9, 3, 4, 13)
 
 
 def pin_bwd_largest_state(lib):
     """The same comparison at the largest state size the library takes
     (N = 256, D != N), where a state-index stride or a per-state buffer
     mistake would show."""
-    _bwd_against_autograd(lib, 1, 6, 3, 256, 15)
+    bwd_against_autograd(lib, 1, 6, 3, 256, 15)
 
 
 def pin_bwd_optional_inputs(lib):
