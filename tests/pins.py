@@ -545,26 +545,30 @@ def _conv(lib, p, w, cb, act):
                                 p["z"], dtype=oracle.F32, lib=lib)
 
 
-def pin_conv_against_numpy(lib):
+def conv_numpy_check(lib, rng, batch, L, D, N):
     """With B = 0 the state stays 0 and y = Dskip u: with Dskip = 1 and no gate
     y is the convolution output itself, checked against numpy.convolve (causal,
     width 4, w[d, 3] on the current input) plus bias, and SiLU via scipy's
     logistic function for act = 1."""
-    rng = np.random.default_rng(60)
-    p = random_problem(rng, 2, 30, 5, 4, gate=False)
+    p = random_problem(rng, batch, L, D, N, gate=False)
     p["B"] = _f32(np.zeros_like(p["B"]))
-    p["Dskip"] = _f32(np.ones(5))
-    w = rng.standard_normal((5, 4))
-    cb = rng.standard_normal(5)
+    p["Dskip"] = _f32(np.ones(D))
+    w = rng.standard_normal((D, 4))
+    cb = rng.standard_normal(D)
     for act in (0, 1):
         y, _ = _conv(lib, p, w, cb, act)
         x = np.float64(p["u"])
         wf, cbf = np.float64(np.float32(w)), np.float64(np.float32(cb))
-        for b in range(2):
-            for d in range(5):
-                v = np.convolve(x[b, :, d], wf[d][::-1])[:30] + cbf[d]
+        for b in range(batch):
+            for d in range(D):
+                v = np.convolve(x[b, :, d], wf[d][::-1])[:L] + cbf[d]
                 want = v * scipy.special.expit(v) if act else v
                 _close(y[b, :, d], want, 1e-12, 1e-13, f"conv act={act} b={b} d={d}")
+
+
+def pin_conv_against_numpy(lib):
+    """The convolution against numpy.convolve (see conv_numpy_check)."""
+    conv_numpy_check(lib, np.random.default_rng(60), 2, 30, 5, 4)
 
 
 def pin_conv_identity_is_the_scan(lib):
@@ -741,13 +745,12 @@ def _ssd_run(ssd, lib, p):
     return ssd(p["x"], p["dt"], p["dt_bias"], p["A"], p["B"], p["C"], p["Dskip"], lib=lib)
 
 
-def pin_ssd_masked_matmul(lib, ssd=oracle.ssd_fwd):
+def ssd_masked_matmul_check(lib, rng, ssd=oracle.ssd_fwd, **shape):
     """The pages' duality statement written out: per head, y = (L o C B^T) X
     with the decay mask L[t, s] = exp(a sum_{r=s+1..t} dt_r) dt_s for s <= t
     (0 above the diagonal), plus D x; the final state is
     sum_s exp(a sum_{r>s} dt_r) dt_s B_s^T x_s.  numpy matmuls, float64."""
-    rng = np.random.default_rng(21)
-    p = _ssd_problem(rng)
+    p = _ssd_problem(rng, **shape)
     y, h = _ssd_run(ssd, lib, p)
     batch, L, H, P = p["x"].shape
     for b in range(batch):
@@ -763,6 +766,11 @@ def pin_ssd_masked_matmul(lib, ssd=oracle.ssd_fwd):
             wlast = np.exp(cum[-1] - cum) * dt                                     # [s]
             hw = (p["B"][b].astype(np.float64) * wlast[:, None]).T @ xh          # [N, P]
             _close(h[b, hh], hw.T, 1e-10, 1e-10, f"SSD final state b={b} h={hh}")
+
+
+def pin_ssd_masked_matmul(lib, ssd=oracle.ssd_fwd):
+    """The duality statement as masked matrix products (see ssd_masked_matmul_check)."""
+    ssd_masked_matmul_check(lib, np.random.default_rng(21), ssd)
 
 
 def pin_ssd_chunked_form(lib, ssd=oracle.ssd_fwd):

@@ -1,6 +1,8 @@
 """The oracle over random small shapes, including the degenerate ones
-(L = 1, N = 1, D = 1, batch = 1): the forward against brute-force unrolling
-and the backward against torch.autograd (CPU only)."""
+(L = 1, N = 1, D = 1, batch = 1): the forward and its Euler and trapezoid
+variants against brute-force unrolling, the backward against torch.autograd,
+the SSD form against its masked matrix products and the convolution against
+numpy.convolve (CPU only)."""
 import numpy as np
 import pytest
 from hypothesis import given, settings
@@ -69,3 +71,19 @@ def test_variants_against_unrolling(lib, disc, batch, L, D, N, seed):
     want_y, want_h = _variant_unrolled(p, disc)
     pins._close(y, want_y, 1e-10, 1e-12, f"disc {disc} y")
     pins._close(h, want_h, 1e-10, 1e-12, f"disc {disc} h_last")
+
+
+@settings(max_examples=25, deadline=None)
+@given(batch=st.integers(1, 2), L=st.integers(1, 20), H=st.integers(1, 3), P=st.integers(1, 5),
+       N=st.integers(1, 9), seed=st.integers(0, 2**31 - 1))
+def test_ssd_against_masked_matmul(lib, batch, L, H, P, N, seed):
+    pins.ssd_masked_matmul_check(lib, np.random.default_rng(seed), batch=batch, L=L, H=H, P=P,
+                                 N=N)
+
+
+@settings(max_examples=25, deadline=None)
+@given(batch=st.integers(1, 2), L=st.integers(1, 12), D=st.integers(1, 5), N=st.integers(1, 4),
+       seed=st.integers(0, 2**31 - 1))
+def test_conv_against_numpy(lib, batch, L, D, N, seed):
+    """Including sequences shorter than the width-4 filter."""
+    pins.conv_numpy_check(lib, np.random.default_rng(seed), batch, L, D, N)
