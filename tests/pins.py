@@ -398,11 +398,9 @@ def pin_bf16_decode(lib):
     _close(ysb, ysf, 0, 0, "bf16 step y")
 
 
-def pin_step_matches_library_pipeline(lib):
+def step_pipeline_check(lib, rng, batch, D, N):
     """One decode step from a random state, every stage from a library
     routine: softplus (torch), ZOH (scipy), SiLU (torch)."""
-    rng = np.random.default_rng(17)
-    batch, D, N = 2, 3, 4
     A = _f32(-(0.2 + 2 * rng.random((D, N))))
     dt_bias = _f32(rng.standard_normal(D) - 1)
     u, delta, z = (_f32(rng.standard_normal((batch, D))) for _ in range(3))
@@ -424,6 +422,11 @@ def pin_step_matches_library_pipeline(lib):
                             + float(Dskip[d]) * float(u[b, d])) * silu[b, d]
     _close(st1, want_s, 1e-12, 1e-14, "library step state")
     _close(y1, want_y, 1e-12, 1e-14, "library step y")
+
+
+def pin_step_matches_library_pipeline(lib):
+    """One decode step against library routines (see step_pipeline_check)."""
+    step_pipeline_check(lib, np.random.default_rng(17), 2, 3, 4)
 
 
 ALL_PINS = [

@@ -1,8 +1,8 @@
 """The oracle over random small shapes, including the degenerate ones
 (L = 1, N = 1, D = 1, batch = 1): the forward and its Euler and trapezoid
 variants against brute-force unrolling, the backward against torch.autograd,
-the SSD form against its masked matrix products and the convolution against
-numpy.convolve (CPU only)."""
+the SSD form against its masked matrix products, the convolution against
+numpy.convolve and the decode step against library routines (CPU only)."""
 import numpy as np
 import pytest
 from hypothesis import given, settings
@@ -87,3 +87,10 @@ def test_ssd_against_masked_matmul(lib, batch, L, H, P, N, seed):
 def test_conv_against_numpy(lib, batch, L, D, N, seed):
     """Including sequences shorter than the width-4 filter."""
     pins.conv_numpy_check(lib, np.random.default_rng(seed), batch, L, D, N)
+
+
+@settings(max_examples=30, deadline=None)
+@given(batch=st.integers(1, 3), D=st.integers(1, 6), N=st.integers(1, 12),
+       seed=st.integers(0, 2**31 - 1))
+def test_step_against_library_pipeline(lib, batch, D, N, seed):
+    pins.step_pipeline_check(lib, np.random.default_rng(seed), batch, D, N)
