@@ -101,13 +101,39 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def measured_peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(p):
+def _find_key(d, key):
+    """The first positive number stored under ``key`` anywhere in a JSON value."""
+    if isinstance(d, dict):
+        v = d.get(key)
+        if isinstance(v, (int, float)) and not isinstance(v, bool) and v > 0:
+            return float(v)
+        items = d.values()
+    elif isinstance(d, list):
+        items = d
+    else:
+        return None
+    for v in items:
+        got = _find_key(v, key)
+        if got is not None:
+            return got
+    return None
+
+
+def measured_peaks(path=None):
+    """HBM copy bandwidth (GB/s) from MEASURED_PEAKS.json ("measured"), else
+    the stated fallback; a file that cannot be read or holds no positive
+    ``hbm_gbs`` falls back too, and the kind says so."""
+    p = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(p):
+        return FALLBACK_HBM_GBS, "fallback"
+    try:
         with open(p) as f:
-            d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+            v = _find_key(json.load(f), "hbm_gbs")
+    except (OSError, ValueError):
+        v = None
+    if v is None:
+        return FALLBACK_HBM_GBS, "fallback (MEASURED_PEAKS.json has no usable hbm_gbs)"
+    return v, "measured"
 
 
 def algorithmic_bytes(w) -> int:

@@ -44,3 +44,21 @@ def test_launches_per_call_matches_the_plan_choice():
     assert bench.launches_per_call(wl.MAMBA_2P8B) == 1     # 4 x 40 = 160 chains
     assert bench.launches_per_call(wl.MAMBA_130M) == 1     # 8 x 12 = 96 chains
     assert bench.launches_per_call(wl.LONG_SEQ) == 3       # 1 x 12 = 12 chains
+
+
+def test_measured_peaks_reader(tmp_path):
+    """The HBM peak comes from MEASURED_PEAKS.json when it holds a positive
+    hbm_gbs (at any depth); a missing, malformed or incomplete file falls
+    back to the stated figure and says so."""
+    import json
+    p = tmp_path / "MEASURED_PEAKS.json"
+    assert bench.measured_peaks(str(p)) == (bench.FALLBACK_HBM_GBS, "fallback")
+    p.write_text(json.dumps({"hbm_gbs": 6506.3, "bf16_tflops": 1800.0}))
+    assert bench.measured_peaks(str(p)) == (6506.3, "measured")
+    p.write_text(json.dumps({"gpu": "B300", "peaks": [{"hbm_gbs": 6400.5}]}))
+    assert bench.measured_peaks(str(p)) == (6400.5, "measured")
+    for bad in ("{not json", json.dumps({"hbm_gbs": "fast"}), json.dumps({"hbm_gbs": 0}),
+                json.dumps({"bf16_tflops": 1800.0})):
+        p.write_text(bad)
+        v, kind = bench.measured_peaks(str(p))
+        assert v == bench.FALLBACK_HBM_GBS and kind.startswith("fallback (")
