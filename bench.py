@@ -33,12 +33,16 @@ sys.path.insert(0, ROOT)
 METRIC = "selective-scan fwd elements/s (B·L·D) and achieved HBM GB/s vs B300 peak"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
-# The scan is bound by fp32 FMA issue, not HBM: 4 FMA lane-ops per (element,
-# state) -- the exp(dt A)-1 recurrence over n, the two multiply-adds of the
-# state update and the readout -- i.e. 64 per element at N = 16, against
-# 148 SMs x 128 FMA lanes per clock (measured) x 2.032 GHz (maximum SM clock).
+# Work per element of the scan at N = 16, counted by unit.  fp32 multiply-adds:
+# 4 per (element, state) -- the decay's exp(dt A) - 1 (the kernel forms it by
+# a multiply-add recurrence over n in place of 15 of the 16 exponentials), the
+# two of the state update h + e (h + B u / A), and the readout -- 64 in all.
+# Special-function results: 5 (softplus: 2^x and log2; exp(dt A[d,0]); the
+# SiLU gate: 2^x and 1/x); 20 with the 16 exponentials of the zero-order hold
+# taken one by one as written.
 FMA_PER_ELEMENT_N16 = 64
-ALU_PEAK_TFLOPS = 148 * 128 * 2.032e9 * 2 / 1e12
+SFU_PER_ELEMENT = 5
+SFU_PER_ELEMENT_AS_WRITTEN = 20
 
 
 def parse():
@@ -172,16 +176,42 @@ def csrc_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """ncu DRAM bytes per launch recorded under profiles/, if the kernel
-    sources have not changed since (else None)."""
+def recorded_metric(key: str):
+    """A per-launch figure ``key: <number> csrc_sha256: <digest>`` recorded
+    under profiles/ from an ncu capture, if the scan kernel's sources have not
+    changed since it was taken (else (None, None))."""
     dig = csrc_digest()
+    pat = re.compile(re.escape(key) + r":\s*([0-9.eE+]+)\s+csrc_sha256:\s*([0-9a-f]+)")
     for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for line in open(f):
-            m = re.match(r"traffic_bytes_per_launch:\s*(\d+)\s+csrc_sha256:\s*([0-9a-f]+)", line)
+            m = pat.match(line.strip())
             if m and m.group(2) == dig:
-                return int(m.group(1)), os.path.basename(f)
+                return float(m.group(1)), os.path.basename(f)
     return None, None
+
+
+def recorded_traffic():
+    """ncu DRAM bytes (read + write) per launch of the scan kernel."""
+    v, src = recorded_metric("traffic_bytes_per_launch")
+    return (int(v) if v is not None else None), src
+
+
+def scan_ceilings(rates: dict, hbm_gbs: float, bytes_per_element: float,
+                  warp_inst_per_element) -> dict:
+    """Elements/s each unit allows the scan: HBM at the measured copy
+    bandwidth, the FMA pipes, the special-function unit and instruction issue
+    at the rates measured in this process (``rates`` from ssm_unit_ceilings);
+    issue only when the kernel's instruction count per element is recorded."""
+    c = {"hbm": hbm_gbs * 1e9 / bytes_per_element,
+         "fma": rates["fma_per_s"] / FMA_PER_ELEMENT_N16,
+         "sfu": rates["ex2_per_s"] / SFU_PER_ELEMENT,
+         "issue": (rates["warp_inst_per_s"] / warp_inst_per_element
+                   if warp_inst_per_element else None)}
+    binding = min((k for k in c if c[k]), key=lambda k: c[k])
+    c["sfu_as_written"] = rates["ex2_per_s"] / SFU_PER_ELEMENT_AS_WRITTEN
+    c["binding"] = binding
+    c["unit"] = "elements/s"
+    return c
 
 
 class ClockSampler:
@@ -266,6 +296,8 @@ def bench_ours(args, rank, world, local):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    # unit rates of this GPU, measured before (not inside) the timed region
+    rates = ssm.ssm_unit_ceilings(reps=5, stream=stream)
     for _ in range(args.warmup):
         call()
     barrier()
@@ -295,7 +327,14 @@ def bench_ours(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     achieved_gbs = alg / avg_launch_s / 1e9
     achieved_tflops = 2 * FMA_PER_ELEMENT_N16 * w.elements / avg_launch_s / 1e12
+    fma_peak_tflops = 2 * rates["fma_per_s"] / 1e12
     traffic, traffic_src = recorded_traffic()
+    inst_pe, inst_src = recorded_metric("warp_inst_per_element")
+    ceilings = scan_ceilings(rates, peak, alg / w.elements, inst_pe)
+    ceilings["achieved"] = w.elements / avg_launch_s
+    ceilings["warp_inst_per_element"] = inst_pe
+    ceilings["warp_inst_per_element_source"] = inst_src
+    ceilings["measured_rates"] = rates
 
     variants = None
     if not args.no_variants:
@@ -334,16 +373,22 @@ def bench_ours(args, rank, world, local):
         "hbm_gbs": achieved_gbs,
         "hbm_frac_measured": achieved_gbs / peak,
         "hbm_frac_nominal_8tbs": achieved_gbs / NOMINAL_HBM_GBS,
-        "roofline": {"bound": "alu", "achieved": achieved_tflops, "peak": ALU_PEAK_TFLOPS,
-                     "unit": "TFLOP/s", "frac": achieved_tflops / ALU_PEAK_TFLOPS,
-                     "peak_source": "derived: 148 SMs x 128 fp32 FMA lanes/clk x 2.032 GHz x 2",
-                     "algorithmic_flops_per_launch": 2 * FMA_PER_ELEMENT_N16 * w.elements,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "traffic": traffic,
+                     "peak_source": peak_kind + " HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": alg,
                      "avg_launch_ms": avg_launch_s * 1e3,
                      "median_launch_ms": launch_ms[len(launch_ms) // 2],
-                     "traffic": traffic, "traffic_source": traffic_src},
-        "hbm_roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": achieved_gbs / peak, "peak_source": peak_kind},
+                     "traffic_source": traffic_src,
+                     "frac_of_nominal_8tbs": achieved_gbs / NOMINAL_HBM_GBS},
+        "alu_roofline": {"bound": "alu", "achieved": achieved_tflops, "peak": fma_peak_tflops,
+                         "unit": "TFLOP/s", "frac": achieved_tflops / fma_peak_tflops,
+                         "peak_source": "measured in this run: ssm_unit_ceilings, packed fp32 "
+                                        "multiply-add stream on all SMs",
+                         "flops_per_element": 2 * FMA_PER_ELEMENT_N16,
+                         "counted": "4 fp32 multiply-adds per (element, state): exp(dt A)-1, the "
+                                    "two of the state update, the readout"},
+        "ceilings": ceilings,
         "clocks": clocks.summary(),
         "backward": backward,
         "ssd": ssd,
@@ -689,12 +734,23 @@ def cpu_baseline(inp, w):
     w1 = wl.MAMBA_130M
     inp1 = wl.make_scan_inputs(w1, device="cpu")
     e1, s1 = _oracle_sample(inp1, w1, 64, 1)
+    # the long sequence (1 x 1,048,576 x 1536): every step of a 2n-channel
+    # slice drawn with that workload's recipe (the oracle's time depends on
+    # the sizes, not on which channels)
+    w3 = wl.LONG_SEQ
+    ch3 = 2 * n
+    inp3 = wl.make_scan_inputs(w3, device="cpu", D=ch3)
+    e3, s3 = _oracle_sample(inp3, w3, ch3, n)
     return {"value": elems / secs, "unit": "elements/s", "cores": n, "kind": "oracle",
             "sample": f"all {w.batch}x{w.L} steps of the first {channels} of {w.D} channels "
                       f"({elems} elements, {secs:.1f} s wall, float64)",
             "single_core_mamba130m": {"value": e1 / s1, "unit": "elements/s",
                                       "sample": f"all {w1.batch}x{w1.L} steps of 64 of {w1.D} "
-                                                f"channels ({e1} elements, {s1:.1f} s)"}}
+                                                f"channels ({e1} elements, {s1:.1f} s)"},
+            "longseq": {"value": e3 / s3, "unit": "elements/s", "cores": n,
+                        "sample": f"all {w3.L} steps of {ch3} of {w3.D} channels ({e3} "
+                                  f"elements, {s3:.1f} s wall, float64)",
+                        "full_workload_s_at_this_rate": w3.elements / (e3 / s3)}}
 
 
 def bench_reference(args, rank, world):

@@ -62,3 +62,33 @@ def test_measured_peaks_reader(tmp_path):
         p.write_text(bad)
         v, kind = bench.measured_peaks(str(p))
         assert v == bench.FALLBACK_HBM_GBS and kind.startswith("fallback (")
+
+
+def test_scan_ceilings_pick_the_binding_unit():
+    """Each unit's ceiling is its measured rate over the work per element;
+    the binding one is the smallest of those that are known."""
+    rates = {"fma_per_s": 3.84e13, "ex2_per_s": 9.6e12, "warp_inst_per_s": 1.2e12}
+    c = bench.scan_ceilings(rates, 6500.0, 8.0, 2.0)
+    assert c["hbm"] == 6500.0e9 / 8.0
+    assert c["fma"] == 3.84e13 / 64
+    assert c["sfu"] == 9.6e12 / 5 and c["sfu_as_written"] == 9.6e12 / 20
+    assert c["issue"] == 1.2e12 / 2.0
+    assert c["binding"] == "fma"
+    c = bench.scan_ceilings(rates, 6500.0, 8.0, None)      # no recorded instruction count
+    assert c["issue"] is None and c["binding"] == "fma"
+    c = bench.scan_ceilings(rates, 6500.0, 8.0, 4.0)
+    assert c["binding"] == "issue"
+
+
+def test_recorded_metric_needs_the_current_kernel_digest(tmp_path, monkeypatch):
+    """A figure recorded under profiles/ is used only while the scan kernel's
+    sources still have the digest written beside it."""
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    dig = bench.csrc_digest()
+    (prof / "a.md").write_text(f"traffic_bytes_per_launch: 654404608 csrc_sha256: {dig}\n"
+                               f"warp_inst_per_element: 1.75 csrc_sha256: 0000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "csrc_digest", lambda: dig)
+    assert bench.recorded_traffic() == (654404608, "a.md")
+    assert bench.recorded_metric("warp_inst_per_element") == (None, None)
