@@ -256,13 +256,23 @@ SSM_API int ssm_step(float *state, const void *u, const void *delta,
  * kernel, which needs no scratch.  Nothing here calls cudaMalloc, cudaFree
  * or any allocating routine.
  *
+ * The chained plan keeps one 128-channel block of one batch entry on one CTA
+ * at a time, so a problem with fewer such blocks (batch * ceil(D/128)) than
+ * resident CTAs (one per SM) runs on that fraction of the GPU: the 1 x 1M x
+ * 1536 long sequence, 12 blocks, uses 12 SMs here, where ssm_scan_fwd splits
+ * the sequence over the whole GPU with a stream-ordered workspace of about
+ * (P-1)*batch*D*68 + P*batch*D*64 bytes for P sequence pieces.
+ *
  *   - Limit: 256 + 4 * batch * ceil(D/32) bytes (rounded up to 256), plus
  *     64 * batch * D bytes when h_last is NULL, must fit in
  *     SSM_NOALLOC_SCRATCH_BYTES; otherwise SSM_ERR_SCRATCH is returned before
  *     anything is enqueued.  (batch 4, D 5120 needs 2.8 KB with h_last and
  *     1.3 MB without.)
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - The first call in a device's context looks up the array's device
+ *     address with that device current, and the first call on a device also
+ *     sets the kernel's shared-memory attribute and queries its occupancy
+ *     (both once per device).  Make that first call before any stream
+ *     capture.
  *   - All calls share the one array, and it keeps the last call's contents
  *     (each call clears the parts that must start at zero).  Calls whose
  *     work overlaps on the GPU -- on different streams, or from different
@@ -288,6 +298,22 @@ SSM_API const char *ssm_status_string(int status);
 
 /* Library ABI version (this header describes version 1). */
 SSM_API int ssm_abi_version(void);
+
+/*
+ * ssm_unit_ceilings -- measures, on the current device, the rates of the
+ * three execution units that bound the scan kernels, so that a benchmark can
+ * set its throughput beside ceilings measured on the same GPU in the same
+ * process.  The pages have no counterpart; this is measurement support.
+ *   out[0]  fp32 multiply-adds per second (packed f32x2 stream, all SMs)
+ *   out[1]  2^x results of the special-function unit per second (all SMs)
+ *   out[2]  warp instructions issued per second (scalar multiply-add
+ *           stream, all SMs)
+ * Each rate is the best of `reps` (>= 1) launches timed with CUDA events on
+ * `stream`; the call synchronises `stream` and allocates nothing.  Returns
+ * SSM_ERR_NULL for out == NULL, SSM_ERR_SIZE for reps < 1, SSM_ERR_CUDA if a
+ * launch or event failed.
+ */
+SSM_API int ssm_unit_ceilings(double *out, int reps, void *stream);
 
 #ifdef __cplusplus
 }

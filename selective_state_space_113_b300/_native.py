@@ -22,7 +22,7 @@ STATUS = {0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_SIZE", -3: "SSM_ERR_DTYP
           -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT", -9: "SSM_ERR_SCRATCH"}
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd",
            "ssm_ssd_fwd", "ssm_scan_fwd_noalloc", "ssm_step",
-           "ssm_device_status", "ssm_status_string", "ssm_abi_version")
+           "ssm_device_status", "ssm_status_string", "ssm_abi_version", "ssm_unit_ceilings")
 SSM_DISC_ZOH, SSM_DISC_EULER, SSM_DISC_TRAPEZOID = 0, 1, 2
 
 
@@ -57,6 +57,8 @@ def _load() -> ctypes.CDLL:
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_status_string.argtypes = [ci]
     lib.ssm_abi_version.restype = ci
+    lib.ssm_unit_ceilings.restype = ci
+    lib.ssm_unit_ceilings.argtypes = [ctypes.POINTER(ctypes.c_double), ci, vp]
     if lib.ssm_abi_version() != 1:
         raise ImportError("libssmscan ABI version mismatch")
     return lib
@@ -182,3 +184,11 @@ def ssm_device_status(stream=None) -> int:
 
 def ssm_abi_version() -> int:
     return lib.ssm_abi_version()
+
+
+def ssm_unit_ceilings(reps: int = 5, stream=None) -> dict:
+    """Measured unit rates of the current GPU (all SMs): fp32 multiply-adds/s
+    (packed), special-function 2^x results/s, warp instructions issued/s."""
+    out = (ctypes.c_double * 3)()
+    _check(lib.ssm_unit_ceilings(out, int(reps), _stream(stream)), "ssm_unit_ceilings")
+    return {"fma_per_s": out[0], "ex2_per_s": out[1], "warp_inst_per_s": out[2]}

@@ -10,7 +10,9 @@
 #include <cstring>
 #include <mutex>
 
+#include "ceilings.cuh"
 #include "common.cuh"
+#include "faults.cuh"
 #include "scan_tile_host.cuh"
 #include "scan_bwd_generic.cuh"
 #include "scan_bwd_host.cuh"
@@ -151,6 +153,7 @@ extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bi
                             const float* Dskip, const void* z, void* y, float* h_last,
                             int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
                             void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_scan_fwd");
     return scan_impl(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
                      SSM_DISC_ZOH, stream_);
 }
@@ -160,6 +163,7 @@ extern "C" int ssm_scan_fwd_disc(const void* u, const void* delta, const float* 
                                  const float* Dskip, const void* z, void* y, float* h_last,
                                  int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
                                  int disc, void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_scan_fwd_disc");
     return scan_impl(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
                      disc, stream_);
 }
@@ -170,6 +174,7 @@ extern "C" int ssm_conv_scan_fwd(const void* x, const float* conv_w, const float
                                  const float* Dskip, const void* z, void* y, float* h_last,
                                  int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
                                  void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_conv_scan_fwd");
     if (D > 0 && !conv_w) return SSM_ERR_NULL;
     return scan_impl(x, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
                      SSM_DISC_ZOH, stream_, ConvArgs{D > 0 ? conv_w : nullptr, conv_b, act});
@@ -181,6 +186,7 @@ extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bi
                             void* ddelta, float* ddt_bias, float* dA, float* dB, float* dC,
                             float* dDskip, void* dz, int64_t batch, int64_t L, int64_t D,
                             int64_t N, int dtype, void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_scan_bwd");
     if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
@@ -226,7 +232,7 @@ extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bi
     }
     float* scratch = nullptr;
     const size_t bytes = sizeof(float) * ssm::bwdg::bwd_generic_scratch_floats(batch, L, D, N);
-    if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), bytes, stream) != cudaSuccess) {
+    if (ssm::fault::malloc_async(reinterpret_cast<void**>(&scratch), bytes, stream) != cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_NOMEM;
     }
@@ -253,6 +259,7 @@ extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, 
                            const void* B, const void* C, const float* Dskip, void* y,
                            float* h_last, int64_t batch, int64_t L, int64_t H, int64_t P,
                            int64_t N, int dtype, void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_ssd_fwd");
     if (batch < 0 || L < 0 || H < 0 || P < 1 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
@@ -299,6 +306,7 @@ extern "C" int ssm_step(float* state, const void* u, const void* delta, const fl
                         const float* A, const void* B, const void* C, const float* Dskip,
                         const void* z, void* y, int64_t batch, int64_t D, int64_t N, int dtype,
                         void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_step");
     if (batch < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
@@ -374,6 +382,20 @@ extern "C" const char* ssm_status_string(int status) {
 
 extern "C" int ssm_abi_version(void) { return 1; }
 
+extern "C" int ssm_unit_ceilings(double* out, int reps, void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_unit_ceilings");
+    if (!out) return SSM_ERR_NULL;
+    if (reps < 1) return SSM_ERR_SIZE;
+    if (ssm::fault::launch_refused()) return SSM_ERR_CUDA;
+    double r[3] = {0.0, 0.0, 0.0};
+    if (ssm::ceil::measure(r, reps, static_cast<cudaStream_t>(stream_)) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    for (int i = 0; i < 3; ++i) out[i] = r[i];
+    return SSM_OK;
+}
+
 // ---------------------------------------------------------------------------
 // ssm_scan_fwd_noalloc: the selective scan for callers that must not allocate
 // device memory while they run (for example a serving loop whose memory is
@@ -395,23 +417,57 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 constexpr int kMaxDevices = 128;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+// Per device: the context the address was looked up in, and the address.
+struct NoallocSlot {
+    CUcontext ctx;
+    void* ptr;
+};
+NoallocSlot g_noalloc_slot[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (the first call on a device does it, with that device current).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent from the driver, found once through the runtime (the
+// library does not link libcuda).
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    });
+    return fn;
+}
+
+// Device address of g_noalloc_scratch in the current device's current
+// context.  It is looked up with that device current the first time a call
+// runs in that context (the first call on a device, and again after the
+// context was destroyed and another one made current), so an address is never
+// reused from a context that is gone.
 int noalloc_scratch_ptr(unsigned char** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSM_ERR_CUDA;
+    CtxGetCurrentFn get_ctx = ctx_get_current();
+    if (!get_ctx) return SSM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return SSM_ERR_CUDA;
+    NoallocSlot& slot = g_noalloc_slot[dev];
+    if (!ctx || slot.ctx != ctx || !slot.ptr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
             return SSM_ERR_CUDA;
         }
-        g_noalloc_ptr[dev] = p;
+        // The lookup makes the device's primary context current if none was.
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return SSM_ERR_CUDA;
+        slot.ctx = ctx;
+        slot.ptr = p;
     }
-    *out = static_cast<unsigned char*>(g_noalloc_ptr[dev]);
+    *out = static_cast<unsigned char*>(slot.ptr);
     return SSM_OK;
 }
 
@@ -439,7 +495,9 @@ int launch_noalloc(const T* u, const T* delta, const float* dt_bias, const float
     Params p;
     if (!setup<T>(maps, &p, u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D))
         return SSM_ERR_CUDA;
-    p.G = chained_grid<T>(p.nchains, workers, L, 0);
+    // SSM_CHUNK_T (development and tests) cuts chains into pieces of about
+    // that many steps, as it does for ssm_scan_fwd's chained plan.
+    p.G = chained_grid<T>(p.nchains, workers, L, env_ll("SSM_CHUNK_T", 0));
     const size_t head = header_bytes(batch, D);
     // The array keeps the previous call's contents: reset the tickets, the
     // abort word and the sub-block flags, which must start at zero.
@@ -459,6 +517,7 @@ extern "C" int ssm_scan_fwd_noalloc(const void* u, const void* delta, const floa
                                     const float* Dskip, const void* z, void* y, float* h_last,
                                     int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
                                     void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_scan_fwd_noalloc");
     if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;

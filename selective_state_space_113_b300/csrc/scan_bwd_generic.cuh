@@ -10,6 +10,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "faults.cuh"
 
 namespace ssm {
 namespace bwdg {
@@ -162,6 +163,7 @@ static cudaError_t launch_scan_bwd_generic(const T* u, const T* delta, const flo
                                                           dy, dh_last, du, ddelta, ddt_bias, dA,  \
                                                           dB, dC, dDskip, dz, ck, hist, batch, L, \
                                                           D, N)
+    if (fault::launch_refused()) return cudaErrorLaunchFailure;
     if (N <= 16) SSM_BWDG(16);
     else if (N <= 32) SSM_BWDG(32);
     else if (N <= 64) SSM_BWDG(64);

@@ -63,7 +63,7 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
     off = round256(off + (size_t)nCB * batch * L * 32 * 4);
 
     unsigned char* ws = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), off, stream) != cudaSuccess) {
+    if (fault::malloc_async(reinterpret_cast<void**>(&ws), off, stream) != cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_NOMEM;
     }
@@ -95,6 +95,10 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
             p.total_units = p.nchains * (P - 1);
             if (launch_mode<T, (int)kAggregate, (int)kZOH>(p.total_units < wa ? p.total_units : wa,
                                                           maps, p, stream) != cudaSuccess) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
+            if (fault::launch_refused()) {
                 status = SSM_ERR_CUDA;
                 break;
             }
@@ -131,6 +135,10 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
         bp.P = P;
         bp.nCB = nCB;
         bp.units = nCB * batch * P;
+        if (fault::launch_refused()) {
+            status = SSM_ERR_CUDA;
+            break;
+        }
         // 2. adjoint summaries of units 1..P-1, then the adjoint entering each unit
         if (P > 1) {
             const long long nsum = nCB * batch * (P - 1);

@@ -16,6 +16,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "faults.cuh"
 
 namespace ssm {
 
@@ -108,6 +109,7 @@ static cudaError_t launch_scan_generic_n(const T* u, const T* delta, const float
     const int64_t channels = batch * D;
     const int threads = 128;
     const int64_t blocks = (channels + threads - 1) / threads;
+    if (fault::launch_refused()) return cudaErrorLaunchFailure;
     scan_generic_kernel<T, NMAX><<<(unsigned)blocks, threads, 0, stream>>>(
         u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, h_last, batch, L, D, N, disc, conv_w, conv_b,
         act);

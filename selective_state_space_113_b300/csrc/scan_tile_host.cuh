@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/ssmscan.h"
+#include "faults.cuh"
 #include "scan_tile.cuh"
 
 namespace ssm {
@@ -136,6 +137,7 @@ inline size_t header_bytes(long long batch, long long D) {
 template <typename T, int MODE, int DISC, bool CONV = false>
 inline cudaError_t launch_mode(long long grid, const CUtensorMap* maps, const Params& p,
                                cudaStream_t s) {
+    if (fault::launch_refused()) return cudaErrorLaunchFailure;
     scan_tile_kernel<T, MODE, DISC, CONV><<<(unsigned)grid, THREADS, Cfg<T>::kSmemBytes, s>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
     return cudaGetLastError();
@@ -240,7 +242,7 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
         bytes += (size_t)p.P * nch * NS * 4;
     }
     unsigned char* ws = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream) != cudaSuccess) {
+    if (fault::malloc_async(reinterpret_cast<void**>(&ws), bytes, stream) != cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_NOMEM;
     }
@@ -268,6 +270,10 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
                 break;
             }
             const long long threads = nch * NS;
+            if (fault::launch_refused()) {
+                status = SSM_ERR_CUDA;
+                break;
+            }
             carry_kernel<<<(unsigned)cdiv(threads, 256), 256, 0, stream>>>(
                 p.agg, A, reinterpret_cast<float*>(ws + off_hin), batch, D, p.P);
             if (cudaGetLastError() != cudaSuccess) {

@@ -28,6 +28,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "faults.cuh"
 #include "ptx.cuh"
 
 namespace ssm {
@@ -456,6 +457,7 @@ inline cudaError_t launch_ssd_chunk(const bf16* x, const bf16* dt, const float* 
     cudaError_t e = cudaFuncSetAttribute(ssd_chunk_kernel<N>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (fault::launch_refused()) return cudaErrorLaunchFailure;
     ssd_chunk_kernel<N><<<(unsigned)(batch * H * (P / PH)), THREADS, smem, s>>>(
         x, dt, dt_bias, A, Bm, Cm, Dskip, y, h_last, batch, L, H);
     return cudaGetLastError();
@@ -472,6 +474,7 @@ inline cudaError_t launch_ssd_generic(const T* x, const T* dt, const float* dt_b
 #define SSM_SSDG(NM)                                                                            \
     ssd_generic_kernel<T, NM><<<blocks, 128, 0, s>>>(x, dt, dt_bias, A, Bm, Cm, Dskip, y, h_last, \
                                                      batch, L, H, P, N)
+    if (fault::launch_refused()) return cudaErrorLaunchFailure;
     if (N <= 16) SSM_SSDG(16);
     else if (N <= 64) SSM_SSDG(64);
     else if (N <= 128) SSM_SSDG(128);

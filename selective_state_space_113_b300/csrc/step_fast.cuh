@@ -14,6 +14,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "faults.cuh"
 #include "ptx.cuh"
 
 namespace ssm {
@@ -131,6 +132,7 @@ static cudaError_t launch_step16(float* state, const T* u, const T* delta, const
     const int J = (e && e[0] == '1') ? 1 : (e && e[0] == '4') ? 4 : 2;
     const long long Dh = (D + J - 1) / J;
     const dim3 grid((unsigned)((4 * Dh + THREADS - 1) / THREADS), (unsigned)batch);
+    if (fault::launch_refused()) return cudaErrorLaunchFailure;
     if (J == 4)
         step16_kernel<T, 4><<<grid, THREADS, 0, stream>>>(state, u, delta, dt_bias, A, Bm, Cm,
                                                           Dskip, z, y, (int)D, (int)Dh);

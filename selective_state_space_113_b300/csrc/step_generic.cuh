@@ -5,6 +5,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "faults.cuh"
 
 namespace ssm {
 
@@ -47,6 +48,7 @@ static cudaError_t launch_step_generic(float* state, const T* u, const T* delta,
     const int64_t channels = batch * D;
     const int threads = 128;
     const int64_t blocks = (channels + threads - 1) / threads;
+    if (fault::launch_refused()) return cudaErrorLaunchFailure;
     step_generic_kernel<T><<<(unsigned)blocks, threads, 0, stream>>>(
         state, u, delta, dt_bias, A, Bm, Cm, Dskip, z, y, batch, D, N);
     return cudaGetLastError();

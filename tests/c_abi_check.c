@@ -61,6 +61,11 @@ int main(void) {
     expect(ssm_scan_fwd_noalloc(FAKE, FAKE, NULL, FAKEF, FAKE, FAKE, NULL, NULL, FAKE, NULL, 0, 4,
                                 8, 16, SSM_BF16, NULL),
            SSM_OK, "no-alloc, no channels");
+    {
+        double rates[3];
+        expect(ssm_unit_ceilings(NULL, 1, NULL), SSM_ERR_NULL, "ceilings, out NULL");
+        expect(ssm_unit_ceilings(rates, 0, NULL), SSM_ERR_SIZE, "ceilings, reps 0");
+    }
     printf(fails ? "c abi check: %d failures\n" : "c abi check: ok\n", fails);
     return fails != 0;
 }

@@ -194,3 +194,9 @@ def test_noalloc_argument_validation(lib):
     # a fast-path problem whose carried states (64 bytes per channel without
     # h_last) cannot fit the fixed scratch is refused before any CUDA call
     assert noalloc(lib, batch=1024, D=8192) == -9
+
+
+def test_ceilings_argument_validation(lib):
+    buf = (ctypes.c_double * 3)()
+    assert lib.ssm_unit_ceilings(None, 1, None) == -1
+    assert lib.ssm_unit_ceilings(buf, 0, None) == -2
