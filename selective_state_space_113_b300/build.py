@@ -40,9 +40,11 @@ def sources() -> list[str]:
 
 
 def command(out: str = LIB, extra=()) -> list[str]:
+    # --split-compile 0: the optimiser runs on all host CPUs at once (the
+    # single translation unit otherwise takes several minutes)
     return [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
             "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-            "-Xptxas", "-warn-spills", *extra,
+            "-Xptxas", "-warn-spills", "--split-compile", "0", *extra,
             "-o", out, os.path.join(CSRC, "api.cu")]
 
 

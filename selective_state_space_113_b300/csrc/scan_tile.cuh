@@ -86,8 +86,18 @@ constexpr int NS = 16;              // state size handled here
 constexpr int CW = 32;              // channels per consumer warp (one per lane)
 constexpr int NCW = 4;              // consumer warps per CTA
 constexpr int CB = CW * NCW;        // channels per CTA tile
-constexpr int S = 4;                // stages in the shared-memory ring
-constexpr int KP = 8;               // steps per prologue chunk
+#ifndef SSM_TILE_STAGES
+#define SSM_TILE_STAGES 4
+#endif
+#ifndef SSM_TILE_KP
+#define SSM_TILE_KP 8
+#endif
+#ifndef SSM_TILE_NPB
+#define SSM_TILE_NPB 2
+#endif
+constexpr int S = SSM_TILE_STAGES;  // stages in the shared-memory ring
+constexpr int KP = SSM_TILE_KP;     // steps per prologue chunk
+constexpr int NPB = SSM_TILE_NPB;   // prologue buffers per helper/consumer pair
 constexpr int NWARPS = 2 * NCW + 1; // consumers, helpers, TMA warp
 constexpr int THREADS = 32 * NWARPS;
 constexpr int kTmaWarp = 2 * NCW;
@@ -173,17 +183,17 @@ struct Cfg {
     static constexpr int offState = offPar + kPar;
     static constexpr int offPrev = offState + kState;
     static constexpr int kStage = offPrev + kPrev;
-    // Prologue ring of one helper/consumer pair: 2 buffers x KP steps x
+    // Prologue ring of one helper/consumer pair: NPB buffers x KP steps x
     // 32 lanes x float4.
     static constexpr int kProBuf = KP * CW * 16;
-    static constexpr int kPro = 2 * kProBuf;
+    static constexpr int kPro = NPB * kProBuf;
     static constexpr int offPro = S * kStage;
     // y tiles of one consumer: 2 buffers of [TC][32] elements.
     static constexpr int kY = TC * CW * es;
     static constexpr int offY = offPro + NCW * kPro;
     static constexpr int offMeta = offY + NCW * 2 * kY;
     static constexpr int offBar = offMeta + S * (int)sizeof(Meta);
-    static constexpr int kNumBars = 3 * S + 4 * NCW;
+    static constexpr int kNumBars = 3 * S + 2 * NPB * NCW;
     static constexpr int kBytes = offBar + kNumBars * 8;
     static constexpr int kSmemBytes = kBytes + 1024;   // + slack to align the base
     static constexpr int kRowsPerHelper = TC / NCW;
@@ -572,8 +582,8 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::offBar);
     uint64_t* convd = full + S;
     uint64_t* empty = convd + S;
-    uint64_t* pfull = empty + S;          // [NCW][2]
-    uint64_t* pempty = pfull + 2 * NCW;   // [NCW][2]
+    uint64_t* pfull = empty + S;            // [NCW][NPB]
+    uint64_t* pempty = pfull + NPB * NCW;   // [NCW][NPB]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -582,7 +592,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             ptx::mbar_init(&convd[s], NCW);
             ptx::mbar_init(&empty[s], NCW);
         }
-        for (int i = 0; i < 2 * NCW; ++i) {
+        for (int i = 0; i < NPB * NCW; ++i) {
             ptx::mbar_init(&pfull[i], 1);
             ptx::mbar_init(&pempty[i], 1);
         }
@@ -760,8 +770,8 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             }
             const int nchunks = (m.nvalid + KP - 1) / KP;
             for (int c = 0; c < nchunks; ++c, ++q) {
-                const int buf = (int)(q & 1);
-                if (q >= 2 && !bwait(&pempty[2 * hi + buf], (uint32_t)(((q / 2) - 1) & 1), p)) {
+                const int buf = (int)(q % NPB);
+                if (q >= NPB && !bwait(&pempty[NPB * hi + buf], (uint32_t)(((q / NPB) - 1) & 1), p)) {
                     failed = true;
                     break;
                 }
@@ -773,7 +783,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                     prologue_chunk<T, MODE, DISC, false, CONV>(st, c * KP, CW * hi + lane, cp, geo,
                                                                out, cs, p.act);
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&pfull[2 * hi + buf]);
+                if (lane == 0) ptx::mbar_arrive(&pfull[NPB * hi + buf]);
             }
         }
         if (failed && lane == 0) raise_failure(p);
@@ -848,8 +858,8 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
         }
         const int nchunks = (m.nvalid + KP - 1) / KP;
         for (int c = 0; c < nchunks; ++c, ++q) {
-            const int buf = (int)(q & 1);
-            if (!bwait(&pfull[2 * w + buf], (uint32_t)((q / 2) & 1), p)) {
+            const int buf = (int)(q % NPB);
+            if (!bwait(&pfull[NPB * w + buf], (uint32_t)((q / NPB) & 1), p)) {
                 failed = true;
                 break;
             }
@@ -865,7 +875,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                 steps_general<T, MODE, DISC>(st, c * KP, cnt, pv, Arow, H, P, S2, ytile, lane);
             }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&pempty[2 * w + buf]);
+            if (lane == 0) ptx::mbar_arrive(&pempty[NPB * w + buf]);
         }
         if (failed) break;
         if (MODE != kAggregate && block_live) {

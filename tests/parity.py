@@ -85,3 +85,20 @@ def sample_channels(batch: int, D: int, count: int, seed: int = 0):
     while len(chans) < min(count, batch * D):
         chans.add((int(rng.integers(batch)), int(rng.integers(D))))
     return sorted(chans)
+
+
+def chain_channels(batch: int, D: int, per_chain: int = 3, block: int = 128, seed: int = 0):
+    """Channels that touch every 128-channel chain of the fast kernel: for each
+    (batch entry, channel block), its first and last channel plus
+    ``per_chain - 2`` others drawn from the block.  A chain is cut only along
+    the sequence, so each CTA's static range of chain-major stages starts
+    and ends in chains whose first and last channels are all in the sample."""
+    rng = np.random.default_rng(seed)
+    chans = set()
+    for b in range(batch):
+        for c0 in range(0, D, block):
+            c1 = min(c0 + block, D) - 1
+            chans.update({(b, c0), (b, c1)})
+            for _ in range(max(0, per_chain - 2)):
+                chans.add((b, int(rng.integers(c0, c1 + 1))))
+    return sorted(chans)

@@ -125,8 +125,10 @@ def test_bwd_unaligned_operand(which):
     compare(run_bwd(inp), oracle_bwd(inp), parity.TOL[torch.bfloat16], f"unaligned {which}")
 
 
-@pytest.mark.parametrize("N", [7, 33])
+@pytest.mark.parametrize("N", [7, 20, 33, 100])
 def test_bwd_other_state_sizes(N):
+    """The generic backward's four instantiations: N <= 16, <= 32, <= 64 and
+    <= 256."""
     inp = inputs(2, 40, 24, N, torch.float32, N)
     compare(run_bwd(inp), oracle_bwd(inp), 1e-4, f"N={N}")
 

@@ -26,10 +26,11 @@ def full_parity(inp, what):
     parity.check(parity.to_f64(h), h_ref, tol, what + " h_last")
 
 
-def sampled_parity(inp, what, count, threads=8):
+def sampled_parity(inp, what, count=None, threads=8, chans=None):
     y, h = run_gpu(inp)
     batch, L, D = inp["u"].shape
-    chans = parity.sample_channels(batch, D, count)
+    if chans is None:
+        chans = parity.sample_channels(batch, D, count)
     ref = parity.oracle_scan_channels(inp, chans, threads=threads)
     tol = parity.TOL[inp["u"].dtype]
     idx_b = torch.tensor([c[0] for c in chans], device=DEV)
@@ -64,17 +65,36 @@ def test_state_sizes(N):
 
 
 def test_mamba130m_full_size_sampled():
-    sampled_parity(wl.make_scan_inputs(wl.MAMBA_130M, device=DEV), "mamba130m", 64)
+    """Every one of the 96 chains (8 x 12 blocks of 128 channels): its first
+    and last channel and one more."""
+    w = wl.MAMBA_130M
+    chans = parity.chain_channels(w.batch, w.D, per_chain=3, seed=1)
+    assert len({(b, d // 128) for b, d in chans}) == 96
+    sampled_parity(wl.make_scan_inputs(w, device=DEV), "mamba130m", chans=chans, threads=16)
 
 
 def test_mamba2p8b_full_size_sampled():
-    sampled_parity(wl.make_scan_inputs(wl.MAMBA_2P8B, device=DEV), "mamba2.8b", 48)
+    """Every one of the 160 chains (4 x 40 blocks of 128 channels), at the
+    bench's launch configuration: first, last and one more channel each."""
+    w = wl.MAMBA_2P8B
+    chans = parity.chain_channels(w.batch, w.D, per_chain=3, seed=2)
+    assert len({(b, d // 128) for b, d in chans}) == 160
+    sampled_parity(wl.make_scan_inputs(w, device=DEV), "mamba2.8b", chans=chans, threads=16)
 
 
 @pytest.mark.slow
 def test_longseq_full_size_sampled():
-    inp = wl.make_scan_inputs(wl.LONG_SEQ, device=DEV)
-    sampled_parity(inp, "longseq", 8, threads=8)
+    """64 channels spanning all 12 chains of the 1 x 1,048,576 x 1536
+    sequence (each chain's first and last channel and 3-4 more), through
+    the narrow plan's three launches."""
+    w = wl.LONG_SEQ
+    chans = parity.chain_channels(w.batch, w.D, per_chain=5, seed=3)
+    rng = np.random.default_rng(4)
+    while len(chans) < 64:
+        chans = sorted(set(chans) | {(0, int(rng.integers(w.D)))})
+    assert len({d // 128 for _, d in chans}) == 12
+    inp = wl.make_scan_inputs(w, device=DEV)
+    sampled_parity(inp, "longseq", chans=chans, threads=16)
 
 
 def test_optional_inputs_null():
