@@ -618,8 +618,9 @@ def bench_ssd(ssm, dev, stream, reps: int = 5):
     """ssm_ssd_fwd (the Mamba-2 form) on a Mamba-2 2.7B-shaped layer (4 x 4096,
     80 heads of 64, N = 128, bf16): one tensor-core launch per call, timed
     like the headline.  Algorithmic FLOPs are those of the chunked form's four
-    dense products per 64-step chunk (C B^T, scores X, C H, (B w)^T X), with
-    no credit for the causal half the kernel skips."""
+    dense products per 128-step chunk (C B^T, masked scores X, C H, B^T (w x)),
+    counted once (the hi + lo operand split, which doubles three of them, is
+    not credited)."""
     import torch
     from selective_state_space_113_b300 import workloads as wl
     w = wl.SSD_2P7B
@@ -641,7 +642,7 @@ def bench_ssd(ssm, dev, stream, reps: int = 5):
         e1.synchronize()
         ms = e0.elapsed_time(e1)
         best = ms if best is None or ms < best else best
-    Q = 64
+    Q = 128   # the kernel's chunk length
     chunks = w.batch * w.H * ((w.L + Q - 1) // Q)
     flops = chunks * 2 * (Q * Q * w.N + Q * Q * w.P + 2 * Q * w.N * w.P)
     nbytes = 2 * w.elements * 2 + w.batch * w.L * w.H * 2 + 2 * w.batch * w.L * w.N * 2 \
@@ -649,7 +650,8 @@ def bench_ssd(ssm, dev, stream, reps: int = 5):
     return {"workload": w.name, "ms": best, "elements_per_s": w.elements / (best * 1e-3),
             "algorithmic_flops": flops, "tflops": flops / (best * 1e-3) / 1e12,
             "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (best * 1e-3) / 1e9,
-            "tensor_path": "mma.sync m16n8k16 bf16 -> fp32",
+            "tensor_path": "tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM), TMA 128B-swizzled "
+                           "operand tiles",
             "note": "best of %d; one launch per call" % reps}
 
 

@@ -18,6 +18,7 @@
 #include "scan_bwd_host.cuh"
 #include "scan_generic.cuh"
 #include "ssd.cuh"
+#include "ssd_tc.cuh"
 #include "step_fast.cuh"
 #include "step_generic.cuh"
 
@@ -277,17 +278,15 @@ extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, 
         if (h_last) return from_cuda(cudaMemsetAsync(h_last, 0, sizeof(float) * bhpn, stream));
         return SSM_OK;
     }
-    const bool tc = dtype == SSM_BF16 && P == ssm::ssd::P && (N == 64 || N == 128) &&
+    const bool tc = dtype == SSM_BF16 && P == ssm::ssdtc::P && (N == 64 || N == 128) &&
                     all_aligned16({x, B, C, y}) && ssm::tile::forced_plan() != ssm::tile::kPlanGeneric;
     cudaError_t e;
     if (tc) {
-        const bf16 *xb = static_cast<const bf16*>(x), *db = static_cast<const bf16*>(dt),
-                   *Bb = static_cast<const bf16*>(B), *Cb = static_cast<const bf16*>(C);
-        bf16* yb = static_cast<bf16*>(y);
-        e = N == 64 ? ssm::ssd::launch_ssd_chunk<64>(xb, db, dt_bias, A, Bb, Cb, Dskip, yb, h_last,
-                                                    batch, L, H, stream)
-                    : ssm::ssd::launch_ssd_chunk<128>(xb, db, dt_bias, A, Bb, Cb, Dskip, yb,
-                                                     h_last, batch, L, H, stream);
+        e = ssm::ssdtc::launch_ssd_tc(
+            static_cast<const bf16*>(x), static_cast<const bf16*>(dt), dt_bias, A,
+            static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip, static_cast<bf16*>(y),
+            h_last, batch, L, H, (int)N,
+            (unsigned long long)ssm::tile::env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL), stream);
     } else if (dtype == SSM_F32) {
         e = ssm::ssd::launch_ssd_generic<float>(
             static_cast<const float*>(x), static_cast<const float*>(dt), dt_bias, A,

@@ -1,7 +1,7 @@
 """GPU parity of ssm_ssd_fwd (the Mamba-2 SSD form: scalar A per head, head
 dimension P, Euler input term) against the float64 oracle through the C ABI:
-the tensor-core chunked kernel (bf16, P = 64, N = 64 or 128) on shapes with
-ragged last chunks, the one-thread-per-channel kernel for the rest, and the
+the tcgen05 chunked kernel (bf16, P = 64, N = 64 or 128, 128-step chunks)
+on shapes with exact and ragged last chunks, the one-thread-per-channel kernel for the rest, and the
 Mamba-2 2.7B-shaped layer on sampled heads."""
 import numpy as np
 import pytest
@@ -39,6 +39,9 @@ SHAPES = [  # (batch, L, H, P, N, dtype, plan)
     (1, 200, 2, 64, 128, torch.bfloat16, None),     # ragged last chunk
     (2, 130, 4, 64, 128, torch.bfloat16, None),
     (1, 1, 2, 64, 64, torch.bfloat16, None),
+    (1, 128, 2, 64, 128, torch.bfloat16, None),     # exactly one 128-step chunk
+    (1, 129, 2, 64, 64, torch.bfloat16, None),      # a one-step second chunk
+    (2, 383, 3, 64, 128, torch.bfloat16, None),     # three chunks, ragged
     (2, 70, 2, 64, 128, torch.bfloat16, "generic"),
     (2, 50, 3, 32, 16, torch.float32, None),        # one thread per channel
     (1, 70, 2, 64, 128, torch.float32, None),
