@@ -21,16 +21,24 @@
 // slices.  C, B and X are exact bf16 inputs; the masked scores, w o X and the
 // entering state are not, so each is split into bf16 hi + lo parts
 // (hi = bf16(v), lo = bf16(v - hi)) and multiplied twice, every sum in fp32.
+// The masked scores go back into TMEM (packed bf16 pairs, the A operand of
+// Yi); C, B and X are double-buffered, so a chunk's loads and its S overlap
+// the previous chunk's epilogue.
 //
 // One CTA owns one (b, h) and walks its chunks in order.  Five warps:
-//   warp 4      control: TMA loads of a chunk's C, B (K-major, two 64-wide
-//               regions each) and X (its 128 steps x 64 channels), and the
-//               MMAs, one elected thread;
-//   warps 0..3  epilogue, thread i on TMEM lane i (row i of every product):
-//               the step sizes and cumulative decay (a block scan), w o X, the
-//               masked scores, the outputs, and the state, which it keeps in
-//               registers (thread n holds row n of H) and rewrites after each
-//               chunk as the next chunk's hi + lo operand.
+//   warp 8      control: TMA loads of a chunk's C, B (K-major, two 64-wide
+//               regions each) and X (its 128 steps x 64 channels) into one of
+//               two buffers, and the MMAs, one elected thread, each group
+//               issued as soon as what it reads is ready; the whole warp
+//               computes the next chunk's step sizes and cumulative decay
+//               (from dt values prefetched a chunk ahead) while the tensor
+//               cores work on the current one;
+//   warps 0..7  epilogue, two warps per TMEM lane quadrant (warp e serves
+//               lanes 32 (e % 4) .. +31, i.e. rows of every product, and one
+//               half of its columns): w o X, the masked scores, the outputs,
+//               and the state, which it keeps in registers (thread n holds
+//               half of row n of H) and rewrites after each chunk as the next
+//               chunk's hi + lo operand.
 // N = 64 runs the same code with the state padded to 128 by zeros (C and B
 // regions 64..127 stay zero, so those rows of H stay zero).
 // Every wait is bounded; a wait that gives up records the error, leaves the
@@ -49,43 +57,44 @@ namespace ssdtc {
 constexpr int Q = 128;           // steps per chunk
 constexpr int P = 64;            // channels per head
 constexpr int NP = 128;          // state rows as the kernel holds them (N padded to 128)
-constexpr int THREADS = 160;     // four epilogue warps, one control warp
-constexpr int kCtl = 4;          // the control warp
+constexpr int kEpWarps = 8;      // two per TMEM lane quadrant, each half the columns
+constexpr int THREADS = 32 * (kEpWarps + 1);
+constexpr int kCtl = kEpWarps;   // the control warp
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory: every operand tile is 1024-byte aligned, rows of 128 bytes,
 // 8-row atoms of 1 KB, 16-byte chunks swizzled by the row's index mod 8.
 struct Layout {
-    static constexpr int kC = 0;              // C: 2 regions [128 t][64 n], 16 KB each
-    static constexpr int kB = 32768;          // B: 2 regions [128 s][64 n]
-    static constexpr int kX = 65536;          // X: [128 s][64 p]
-    static constexpr int kSh = 81920;         // masked scores, hi: 2 regions [128 t][64 s]
-    static constexpr int kSl = 114688;        //                lo
-    static constexpr int kWh = 147456;        // w o X, hi: [128 s][64 p]
-    static constexpr int kWl = 163840;        //        lo
-    static constexpr int kHh = 180224;        // entering state, hi: [128 n][64 p]
-    static constexpr int kHl = 196608;        //                 lo
-    static constexpr int kCum = 212992;       // cum_t log2(e), [Q] float
+    // input buffer i at kIn + i * kInBytes: C (2 regions [128 t][64 n], 16 KB
+    // each), B (2 regions [128 s][64 n]), X ([128 s][64 p])
+    static constexpr int kInBytes = 81920;
+    static constexpr int kC = 0, kB = 32768, kX = 65536;   // offsets inside a buffer
+    static constexpr int kWh = 2 * kInBytes;  // w o X, hi: [128 s][64 p]
+    static constexpr int kWl = kWh + 16384;   //        lo
+    static constexpr int kHh = kWl + 16384;   // entering state, hi: [128 n][64 p]
+    static constexpr int kHl = kHh + 16384;   //                 lo
+    static constexpr int kCum = kHl + 16384;  // cum_t log2(e), [Q] float
     static constexpr int kDt = kCum + 512;    // dt_t, [Q] float
-    static constexpr int kWarpSum = kDt + 512;    // block scan: warp totals, [2][4] float
-    static constexpr int kBar = kWarpSum + 64;    // mbarriers
-    static constexpr int kNumBars = 8;
+    static constexpr int kBar = kDt + 512;    // mbarriers
+    static constexpr int kNumBars = 11;
     static constexpr int kTmem = kBar + 8 * kNumBars;   // TMEM base address (written by alloc)
     static constexpr int kBytes = kTmem + 16;
     static constexpr int kSmemBytes = kBytes + 1024;    // + slack to align the base
 };
 static_assert(Layout::kSmemBytes <= 227 * 1024, "CTA shared memory");
 
-// TMEM columns of the accumulators (fp32, lane = row).
+// TMEM columns: the fp32 accumulators (lane = row), then the masked scores
+// as the A operand of Yi (packed bf16 pairs, s = 2c and 2c+1 in column c).
 constexpr uint32_t kColS = 0, kColYx = 128, kColYi = 192, kColG = 256;
+constexpr uint32_t kColSh = 320, kColSl = 384;
 constexpr uint32_t kTmemCols = 512;
 
-// kInFull: a chunk's C, B, X landed; kInFree: the epilogue is done with them;
-// kMma1 / kMma2: S and C H, then the masked product and G, completed;
-// kEpReady: the masked scores and w o X are written; kHReady: the entering
-// state's copy is written; kScan / kCum: the epilogue warps' block scan totals
-// and cumulative decays are written (the epilogue's own rendezvous).
-enum Bar : int { kInFull = 0, kInFree, kMma1, kEpReady, kMma2, kHReady, kScan, kCum };
+// kInFull[2] / kInFree[2]: a buffer's C, B, X landed / the epilogue is done
+// with them; kMmaS, kMmaYx, kMmaYi, kMmaG: S, C H, the masked product, G
+// completed; kEpReady: the masked scores and w o X are written; kHReady: the
+// entering state's copy is written; kCum: the cumulative decays are written.
+enum Bar : int { kInFull = 0, kInFree = 2, kMmaS = 4, kMmaYx, kEpReady, kMmaYi, kMmaG, kHReady,
+                 kCum };
 
 struct Args {
     const bf16* x;
@@ -166,6 +175,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// A-from-TMEM product: [d_tmem] (+)= [a_tmem] x (shared-memory operand b).
+__device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                       int accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, without waiting:
+// the values are valid after a later tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+          "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]),
+          "=f"(v[13]), "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]),
+          "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]),
+          "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]),
+          "=f"(v[31])
+        : "r"(taddr));
+}
+
 // hi = bf16(v), lo = bf16(v - hi), for a pair, packed.
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -214,7 +259,6 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Layout::kTmem);
     float* cum = reinterpret_cast<float*>(sm + Layout::kCum);
     float* dts = reinterpret_cast<float*>(sm + Layout::kDt);
-    float* wsum = reinterpret_cast<float*>(sm + Layout::kWarpSum);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long bh = blockIdx.x;
     const long long b = bh / a.H, hh = bh % a.H;
@@ -223,14 +267,17 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
 
     // ---- set-up: barriers, zeroed state operand and padding regions, TMEM
     if (tid == 0) {
-        ptx::mbar_init(&bar[kInFull], 1);
-        ptx::mbar_init(&bar[kInFree], 4);
-        ptx::mbar_init(&bar[kMma1], 1);
-        ptx::mbar_init(&bar[kEpReady], 4);
-        ptx::mbar_init(&bar[kMma2], 1);
-        ptx::mbar_init(&bar[kHReady], 4);
-        ptx::mbar_init(&bar[kScan], 4);
-        ptx::mbar_init(&bar[kCum], 4);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&bar[kInFull + i], 1);
+            ptx::mbar_init(&bar[kInFree + i], kEpWarps);
+        }
+        ptx::mbar_init(&bar[kMmaS], 1);
+        ptx::mbar_init(&bar[kMmaYx], 1);
+        ptx::mbar_init(&bar[kEpReady], kEpWarps);
+        ptx::mbar_init(&bar[kMmaYi], 1);
+        ptx::mbar_init(&bar[kMmaG], 1);
+        ptx::mbar_init(&bar[kHReady], kEpWarps);
+        ptx::mbar_init(&bar[kCum], 1);
         ptx::fence_mbar_init();
     }
     {
@@ -238,8 +285,10 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         for (int i = tid; i < 2 * 16384 / 16; i += THREADS) {
             reinterpret_cast<uint4*>(sm + Layout::kHh)[i] = z;   // kHh and kHl are adjacent
             if (!two_regions) {
-                reinterpret_cast<uint4*>(sm + Layout::kC + 16384)[i % 1024] = z;
-                reinterpret_cast<uint4*>(sm + Layout::kB + 16384)[i % 1024] = z;
+                const int j = i % 1024, buf = i / 1024;
+                unsigned char* in = sm + buf * Layout::kInBytes;
+                reinterpret_cast<uint4*>(in + Layout::kC + 16384)[j] = z;
+                reinterpret_cast<uint4*>(in + Layout::kB + 16384)[j] = z;
             }
         }
     }
@@ -259,225 +308,309 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
 
     if (warp == kCtl) {
         // ------------------------------------------------------------- control
-        if (lane == 0) {
+        // Lane 0 issues the loads and the products; the whole warp waits and
+        // computes the step sizes and the cumulative decay of each chunk.
+        const bool leader = lane == 0;
+        if (leader) {
             ptx::prefetch_tensormap(&tmX);
             ptx::prefetch_tensormap(&tmB);
             ptx::prefetch_tensormap(&tmC);
-            const uint32_t in_bytes = (two_regions ? 4 : 2) * 16384 + 16384;
-            const uint32_t sC = ptx::smem_u32(sm + Layout::kC), sB = ptx::smem_u32(sm + Layout::kB);
-            const uint32_t sX = ptx::smem_u32(sm + Layout::kX);
-            const uint32_t sSh = ptx::smem_u32(sm + Layout::kSh), sSl = ptx::smem_u32(sm + Layout::kSl);
-            const uint32_t sWh = ptx::smem_u32(sm + Layout::kWh), sWl = ptx::smem_u32(sm + Layout::kWl);
-            const uint32_t sHh = ptx::smem_u32(sm + Layout::kHh), sHl = ptx::smem_u32(sm + Layout::kHl);
-            constexpr uint32_t idS = idesc(128, 128, 0, 0), idY = idesc(128, 64, 0, 1),
-                               idG = idesc(128, 64, 1, 1);
-            for (long long c = 0; c < nchunks && !failed; ++c) {
-                const uint32_t ph = (uint32_t)(c & 1);
-                if (c > 0 && !bwait(&bar[kInFree], ph ^ 1u, a.wait_ns)) { failed = true; break; }
-                ptx::mbar_arrive_expect_tx(&bar[kInFull], in_bytes);
-                const int t0 = (int)(c * Q);
-                ptx::tma_load_3d(sm + Layout::kC, &tmC, &bar[kInFull], 0, t0, (int)b);
-                ptx::tma_load_3d(sm + Layout::kB, &tmB, &bar[kInFull], 0, t0, (int)b);
-                if (two_regions) {
-                    ptx::tma_load_3d(sm + Layout::kC + 16384, &tmC, &bar[kInFull], 64, t0, (int)b);
-                    ptx::tma_load_3d(sm + Layout::kB + 16384, &tmB, &bar[kInFull], 64, t0, (int)b);
-                }
-                ptx::tma_load_4d(sm + Layout::kX, &tmX, &bar[kInFull], 0, (int)hh, t0, (int)b);
-                if (!bwait(&bar[kInFull], ph, a.wait_ns) || !bwait(&bar[kHReady], ph, a.wait_ns)) {
-                    failed = true;
-                    break;
-                }
-                fence_after_sync();
-                // S = C B^T and Yx = C H (hi, then lo)
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
-                    mma(tmem + kColS, sdesc(sC + ko, 16, 1024), sdesc(sB + ko, 16, 1024), idS, k > 0);
-                }
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
-                    mma(tmem + kColYx, sdesc(sC + ko, 16, 1024), sdesc(sHh + k * 2048, 16384, 1024), idY, k > 0);
-                }
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
-                    mma(tmem + kColYx, sdesc(sC + ko, 16, 1024), sdesc(sHl + k * 2048, 16384, 1024), idY, 1);
-                }
-                mma_commit(&bar[kMma1]);
-                if (!bwait(&bar[kEpReady], ph, a.wait_ns)) { failed = true; break; }
-                fence_after_sync();
-                // Yi = (masked S) X and G = B^T (w o X), each hi then lo
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t sS = part ? sSl : sSh, sW = part ? sWl : sWh;
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
-                        mma(tmem + kColYi, sdesc(sS + ko, 16, 1024), sdesc(sX + k * 2048, 16384, 1024), idY,
-                            part > 0 || k > 0);
-                        mma(tmem + kColG, sdesc(sB + k * 2048, 16384, 1024), sdesc(sW + k * 2048, 16384, 1024),
-                            idG, part > 0 || k > 0);
-                    }
-                }
-                mma_commit(&bar[kMma2]);
-            }
-            if (failed) atomicOr(&g_error_word, kErrTimeout);
-            // Leave no copy or product in flight (bounded): the last chunk's
-            // loads and MMAs have completed once its kMma2 phase has.
-            if (nchunks > 0 && !failed)
-                bwait(&bar[kMma2], (uint32_t)((nchunks - 1) & 1), a.wait_ns);
         }
+        const uint32_t in_bytes = (two_regions ? 4 : 2) * 16384 + 16384;
+        const uint32_t s0 = ptx::smem_u32(sm);
+        const uint32_t sWh = s0 + Layout::kWh, sWl = s0 + Layout::kWl;
+        const uint32_t sHh = s0 + Layout::kHh, sHl = s0 + Layout::kHl;
+        constexpr uint32_t idS = idesc(128, 128, 0, 0), idY = idesc(128, 64, 0, 1),
+                           idG = idesc(128, 64, 1, 1);
+        const float A = a.A[hh];
+        const float kb2 = a.dt_bias ? a.dt_bias[hh] * kLog2e : 0.0f;
+        auto load = [&](long long c) {   // chunk c into buffer c % 2
+            const int i = (int)(c & 1);
+            unsigned char* in = sm + i * Layout::kInBytes;
+            uint64_t* full = &bar[kInFull + i];
+            const int t0 = (int)(c * Q);
+            ptx::mbar_arrive_expect_tx(full, in_bytes);
+            ptx::tma_load_3d(in + Layout::kC, &tmC, full, 0, t0, (int)b);
+            ptx::tma_load_3d(in + Layout::kB, &tmB, full, 0, t0, (int)b);
+            if (two_regions) {
+                ptx::tma_load_3d(in + Layout::kC + 16384, &tmC, full, 64, t0, (int)b);
+                ptx::tma_load_3d(in + Layout::kB + 16384, &tmB, full, 64, t0, (int)b);
+            }
+            ptx::tma_load_4d(in + Layout::kX, &tmX, full, 0, (int)hh, t0, (int)b);
+        };
+        auto issue_s = [&](long long c) {   // S = C B^T
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
+                mma(tmem + kColS, sdesc(in + Layout::kC + ko, 16, 1024),
+                    sdesc(in + Layout::kB + ko, 16, 1024), idS, k > 0);
+            }
+            mma_commit(&bar[kMmaS]);
+        };
+        auto issue_yx = [&](long long c) {   // Yx = C H, H as hi then lo
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            for (int part = 0; part < 2; ++part)
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
+                    mma(tmem + kColYx, sdesc(in + Layout::kC + ko, 16, 1024),
+                        sdesc((part ? sHl : sHh) + k * 2048, 16384, 1024), idY, part > 0 || k > 0);
+                }
+            mma_commit(&bar[kMmaYx]);
+        };
+        auto issue_2 = [&](long long c) {   // G = B^T (w o X), then Yi = (masked S) X
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            for (int part = 0; part < 2; ++part)
+                for (int k = 0; k < 8; ++k)
+                    mma(tmem + kColG, sdesc(in + Layout::kB + k * 2048, 16384, 1024),
+                        sdesc((part ? sWl : sWh) + k * 2048, 16384, 1024), idG, part > 0 || k > 0);
+            mma_commit(&bar[kMmaG]);
+            for (int part = 0; part < 2; ++part)
+                for (int k = 0; k < 8; ++k)
+                    mma_ta(tmem + kColYi, tmem + (part ? kColSl : kColSh) + 8 * k,
+                           sdesc(in + Layout::kX + k * 2048, 16384, 1024), idY, part > 0 || k > 0);
+            mma_commit(&bar[kMmaYi]);
+        };
+        auto wait = [&](int which, long long k) {   // k-th completion of a barrier, whole warp
+            return __all_sync(0xffffffffu, bwait(&bar[which], (uint32_t)(k & 1), a.wait_ns));
+        };
+        // raw dt of the steps 4 lane .. 4 lane + 3 of a chunk (a chunk ahead)
+        float raw[4];
+        auto load_dt = [&](long long c) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const long long t = c * Q + 4 * lane + j;
+                raw[j] = t < a.L ? __bfloat162float(a.dt[(b * a.L + t) * a.H + hh]) : 0.0f;
+            }
+        };
+        // step sizes and cumulative decay of chunk c into the shared copy (its
+        // previous readers, the masked scores of chunk c - 1, are done)
+        auto scan = [&](long long c) {
+            const int nv = (int)(a.L - c * Q < Q ? a.L - c * Q : Q);
+            float d[4], cl[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float v2 = fmaf(raw[j], kLog2e, kb2);
+                const float sp = (v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2))) * 0.6931471805599453f;
+                d[j] = 4 * lane + j < nv ? sp : 0.0f;
+                cl[j] = (j ? cl[j - 1] : 0.0f) + A * d[j];
+            }
+            float inc = cl[3];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            const float ex = inc - cl[3];
+            *reinterpret_cast<float4*>(cum + 4 * lane) =
+                make_float4((cl[0] + ex) * kLog2e, (cl[1] + ex) * kLog2e, (cl[2] + ex) * kLog2e,
+                            (cl[3] + ex) * kLog2e);
+            *reinterpret_cast<float4*>(dts + 4 * lane) = make_float4(d[0], d[1], d[2], d[3]);
+            __syncwarp();
+            if (leader) ptx::mbar_arrive(&bar[kCum]);
+        };
+        // prologue: chunk 0's decay, the first two chunks' loads, chunk 0's S and C H
+        load_dt(0);
+        scan(0);
+        if (nchunks > 1) load_dt(1);
+        if (leader) {
+            load(0);
+            if (nchunks > 1) load(1);
+        }
+        if (!wait(kInFull, 0)) failed = true;
+        if (!failed) {
+            fence_after_sync();
+            if (leader) issue_s(0);
+            if (!wait(kHReady, 0)) failed = true;
+        }
+        if (!failed) {
+            fence_after_sync();
+            if (leader) issue_yx(0);
+        }
+        for (long long c = 0; c < nchunks && !failed; ++c) {
+            // the masked scores of chunk c are in TMEM, w o X in shared memory
+            if (!wait(kEpReady, c)) { failed = true; break; }
+            fence_after_sync();
+            if (leader) issue_2(c);
+            if (c + 1 < nchunks) {
+                scan(c + 1);
+                if (c + 2 < nchunks) load_dt(c + 2);
+                // chunk c+1's S (S of chunk c has been read by the epilogue)
+                if (!wait(kInFull + (int)((c + 1) & 1), (c + 1) >> 1)) { failed = true; break; }
+                fence_after_sync();
+                if (leader) issue_s(c + 1);
+            }
+            if (c + 1 < nchunks) {
+                // The epilogue is done with chunk c: its outputs have read Yx
+                // (which chunk c+1's C H overwrites) and buffer c % 2 is free.
+                if (!wait(kInFree + (int)(c & 1), c >> 1)) { failed = true; break; }
+                if (leader && c + 2 < nchunks) load(c + 2);
+                if (!wait(kHReady, c + 1)) { failed = true; break; }
+                fence_after_sync();
+                if (leader) issue_yx(c + 1);
+            }
+        }
+        if (failed && leader) atomicOr(&g_error_word, kErrTimeout);
+        // Leave no copy or product in flight (bounded): every load was
+        // waited for before its MMAs, and the last chunk's Yi, the last
+        // product issued, completes after all of them.
+        if (nchunks > 0 && !failed) wait(kMmaYi, nchunks - 1);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int row = 32 * warp + lane;   // TMEM lane; step t, or state row n
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-        const float A = a.A[hh];
-        const float kb2 = a.dt_bias ? a.dt_bias[hh] * kLog2e : 0.0f;
+        const int quad = warp & 3, hf = warp >> 2;   // TMEM lane quadrant; column half
+        const int row = 32 * quad + lane;            // step t, or state row n
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
         const float dsk = a.Dskip ? a.Dskip[hh] : 0.0f;
-        float Hs[P];   // row `row` of the state (zero for rows >= N)
+        float Hs[32];   // columns 32 hf .. 32 hf + 31 of row `row` of the state
 #pragma unroll
-        for (int p = 0; p < P; ++p) Hs[p] = 0.0f;
+        for (int j = 0; j < 32; ++j) Hs[j] = 0.0f;
+        // The state after chunk c - 1: H <- exp(cum_end) H + G (row n = row,
+        // this warp's 32 columns), then its hi + lo copy for chunk c's C H
+        // (the previous copy was read by chunk c - 1's Yx, which completed).
+        auto state_update = [&](long long c, float dend) -> bool {
+            if (!wwait(&bar[kMmaG], (uint32_t)(c & 1), a.wait_ns) ||
+                !wwait(&bar[kMmaYx], (uint32_t)(c & 1), a.wait_ns))
+                return false;
+            fence_after_sync();
+            float g[32];
+            tmem_ld32(lane_addr + kColG + 32 * hf, g);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) Hs[j] = fmaf(dend, Hs[j], g[j]);
+            store_split32(sm + Layout::kHh, sm + Layout::kHl, row, 4 * hf, Hs);
+            ptx::fence_proxy_async_shared();
+            fence_before_sync();
+            warp_arrive(&bar[kHReady], lane);
+            return true;
+        };
+        // The outputs of chunk c, step t = row, this warp's 32 columns:
+        // Yi + exp(cum_t) Yx + Dskip x; then chunk c's buffer is free.
+        auto outputs = [&](long long c, float ecum) -> bool {
+            if (!wwait(&bar[kMmaYi], (uint32_t)(c & 1), a.wait_ns)) return false;
+            fence_after_sync();
+            const unsigned char* X = sm + (c & 1) * Layout::kInBytes + Layout::kX;
+            const int nv = (int)(a.L - c * Q < Q ? a.L - c * Q : Q);
+            float yi[32], yx[32];
+            tmem_ld32_nowait(lane_addr + kColYi + 32 * hf, yi);
+            tmem_ld32_nowait(lane_addr + kColYx + 32 * hf, yx);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            bf16* yrow = a.y + ((b * a.L + c * Q + row) * a.H + hh) * P + 32 * hf;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(row, 4 * hf + cc));
+                const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+                uint4 o;
+                uint32_t* op = &o.x;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __bfloat1622float2(x2[q]);
+                    const int j = 8 * cc + 2 * q;
+                    const __nv_bfloat162 r2 = __floats2bfloat162_rn(
+                        fmaf(dsk, f.x, fmaf(ecum, yx[j], yi[j])),
+                        fmaf(dsk, f.y, fmaf(ecum, yx[j + 1], yi[j + 1])));
+                    op[q] = *reinterpret_cast<const uint32_t*>(&r2);
+                }
+                if (row < nv) *reinterpret_cast<uint4*>(yrow + 8 * cc) = o;
+            }
+            // X (read above and by Yi) and B (read by G) are free for chunk c + 2
+            fence_before_sync();
+            warp_arrive(&bar[kInFree + (int)(c & 1)], lane);
+            return true;
+        };
         // the zero entering state is in place
         fence_before_sync();
         warp_arrive(&bar[kHReady], lane);
+        float ecum_prev = 0.0f, dend_prev = 0.0f;
         for (long long c = 0; c < nchunks && !failed; ++c) {
             const uint32_t ph = (uint32_t)(c & 1);
-            const long long t0 = c * Q;
-            const int nv = (int)(a.L - t0 < Q ? a.L - t0 : Q);
-            // step size and the cumulative decay (inclusive block scan of A dt)
-            float dtv = 0.0f;
-            if (row < nv) {
-                const float v2 = fmaf(__bfloat162float(a.dt[(b * a.L + t0 + row) * a.H + hh]), kLog2e, kb2);
-                dtv = (v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2))) * 0.6931471805599453f;
+            const unsigned char* X = sm + (c & 1) * Layout::kInBytes + Layout::kX;
+            // the previous chunk's state (its G ran first) lets chunk c's C H go
+            if (c > 0 && !state_update(c - 1, dend_prev)) { failed = true; break; }
+            // this row's cumulative decay (log2 units) and step size, and the chunk's total
+            if (!wwait(&bar[kCum], ph, a.wait_ns)) { failed = true; break; }
+            const float ct = cum[row], dt_t = dts[row], cend2 = cum[Q - 1];
+            const float ecum = ptx::ex2(ct);                 // exp(cum_t)
+            const float wt = ptx::ex2(cend2 - ct) * dt_t;    // w_t
+            const float dend = ptx::ex2(cend2);              // exp(cum_end)
+            if (!wwait(&bar[kInFull + (int)(c & 1)], (uint32_t)((c >> 1) & 1), a.wait_ns)) {
+                failed = true;
+                break;
             }
-            float sc = A * dtv;
+            // w o X, row s = row, this warp's 32 columns, split hi + lo (the
+            // previous chunk's G, which read them, completed: state_update)
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float v = __shfl_up_sync(0xffffffffu, sc, o);
-                if (lane >= o) sc += v;
-            }
-            // warp totals (double-buffered by chunk parity), then the prefix.
-            // The previous chunk's cum / dts are no longer read: every warp
-            // finished its masked scores before kMma2, which this warp passed.
-            if (lane == 31) wsum[4 * ph + warp] = sc;
-            warp_arrive(&bar[kScan], lane);
-            if (!wwait(&bar[kScan], ph, a.wait_ns)) { failed = true; break; }
-            for (int w2 = 0; w2 < warp; ++w2) sc += wsum[4 * ph + w2];
-            const float cend = wsum[4 * ph] + wsum[4 * ph + 1] + wsum[4 * ph + 2] + wsum[4 * ph + 3];
-            const float ct = sc * kLog2e;
-            cum[row] = ct;
-            dts[row] = dtv;
-            const float ecum = ptx::ex2(ct);                       // exp(cum_t)
-            const float wt = ptx::ex2((cend - sc) * kLog2e) * dtv;  // w_t
-            const float dend = ptx::ex2(cend * kLog2e);            // exp(cum_end)
-            warp_arrive(&bar[kCum], lane);
-            if (!wwait(&bar[kInFull], ph, a.wait_ns)) { failed = true; break; }
-            // w o X, row s = row, split hi + lo
-            {
-                const unsigned char* X = sm + Layout::kX;
+            for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(row, cc));
+                const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+                uint4 h, l;
+                uint32_t* hp = &h.x;
+                uint32_t* lp = &l.x;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(row, cc));
-                    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
-                    uint4 h, l;
-                    uint32_t* hp = &h.x;
-                    uint32_t* lp = &l.x;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 f = __bfloat1622float2(x2[q]);
-                        split2(wt * f.x, wt * f.y, hp[q], lp[q]);
-                    }
-                    *reinterpret_cast<uint4*>(sm + Layout::kWh + sw128(row, cc)) = h;
-                    *reinterpret_cast<uint4*>(sm + Layout::kWl + sw128(row, cc)) = l;
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __bfloat1622float2(x2[q]);
+                    split2(wt * f.x, wt * f.y, hp[q], lp[q]);
                 }
+                *reinterpret_cast<uint4*>(sm + Layout::kWh + sw128(row, cc)) = h;
+                *reinterpret_cast<uint4*>(sm + Layout::kWl + sw128(row, cc)) = l;
             }
-            // masked scores of row t = row: S[t,s] exp(cum_t - cum_s) dt_s, s <= t
-            if (!wwait(&bar[kMma1], ph, a.wait_ns) || !wwait(&bar[kCum], ph, a.wait_ns)) {
+            // the previous chunk's outputs (its Yi ran after G)
+            if (c > 0 && !outputs(c - 1, ecum_prev)) { failed = true; break; }
+            // masked scores of row t = row, pieces hf and hf + 2 (32 columns
+            // each): S[t,s] exp(cum_t - cum_s) dt_s for s <= t, into TMEM as
+            // packed bf16 hi and lo (the previous chunk's Yi, which read them,
+            // completed: outputs)
+            if (!wwait(&bar[kMmaS], ph, a.wait_ns)) {
                 failed = true;
                 break;
             }
             fence_after_sync();
-#pragma unroll 1
-            for (int piece = 0; piece < 4; ++piece) {
-                float v[32];
-                if (piece <= warp) {   // some s of the piece are <= t (warp-uniform)
-                    tmem_ld32(lane_addr + kColS + 32 * piece, v);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int s = 32 * piece + j;
-                        v[j] = s <= row ? v[j] * ptx::ex2(ct - cum[s]) * dts[s] : 0.0f;
+            for (int k = 0; k < 2; ++k) {
+                const int piece = hf + 2 * k;
+                uint32_t hi[16], lo[16];
+                if (piece <= quad) {   // some s of the piece are <= t (warp-uniform)
+                    float v[32];
+                    tmem_ld32(lane_addr + kColS + 32 * piece, v);
+                    const float4* cum4 = reinterpret_cast<const float4*>(cum + 32 * piece);
+                    const float4* dt4 = reinterpret_cast<const float4*>(dts + 32 * piece);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 cq = cum4[j4], dq = dt4[j4];
+                        const float cs[4] = {cq.x, cq.y, cq.z, cq.w}, ds[4] = {dq.x, dq.y, dq.z, dq.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 4 * j4 + e, s_ = 32 * piece + j;
+                            v[j] = s_ <= row ? v[j] * ptx::ex2(ct - cs[e]) * ds[e] : 0.0f;
+                        }
                     }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) split2(v[2 * j], v[2 * j + 1], hi[j], lo[j]);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                    for (int j = 0; j < 16; ++j) hi[j] = lo[j] = 0u;
                 }
-                // columns s = 32 piece + 0..31: region s / 64, chunks (s % 64) / 8
-                const int region = piece >> 1, c0 = (piece & 1) * 4;
-                store_split32(sm + Layout::kSh + region * 16384, sm + Layout::kSl + region * 16384, row,
-                              c0, v);
+                tmem_st16(lane_addr + kColSh + 16 * piece, hi);
+                tmem_st16(lane_addr + kColSl + 16 * piece, lo);
             }
-            ptx::fence_proxy_async_shared();
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            ptx::fence_proxy_async_shared();   // w o X, for the tensor cores
             fence_before_sync();
             warp_arrive(&bar[kEpReady], lane);
-            // outputs of step t = row: Yi + exp(cum_t) Yx + Dskip x
-            if (!wwait(&bar[kMma2], ph, a.wait_ns)) { failed = true; break; }
-            fence_after_sync();
-            {
-                const unsigned char* X = sm + Layout::kX;
-                bf16* yrow = a.y + ((b * a.L + t0 + row) * a.H + hh) * P;
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float yi[32], yx[32];
-                    tmem_ld32(lane_addr + kColYi + 32 * half, yi);
-                    tmem_ld32(lane_addr + kColYx + 32 * half, yx);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(row, 4 * half + cc));
-                        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
-                        uint4 o;
-                        uint32_t* op = &o.x;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 f = __bfloat1622float2(x2[q]);
-                            const int j = 8 * cc + 2 * q;
-                            const __nv_bfloat162 r2 = __floats2bfloat162_rn(
-                                fmaf(dsk, f.x, fmaf(ecum, yx[j], yi[j])),
-                                fmaf(dsk, f.y, fmaf(ecum, yx[j + 1], yi[j + 1])));
-                            op[q] = *reinterpret_cast<const uint32_t*>(&r2);
-                        }
-                        if (row < nv)
-                            *reinterpret_cast<uint4*>(yrow + 32 * half + 8 * cc) = o;
-                    }
-                }
-            }
-            // X and the products' inputs are free for the next chunk
-            fence_before_sync();
-            warp_arrive(&bar[kInFree], lane);
-            // the state: H <- exp(cum_end) H + G (row n = row), then its hi + lo
-            // copy for the next chunk's C H
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float g[32];
-                tmem_ld32(lane_addr + kColG + 32 * half, g);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) Hs[32 * half + j] = fmaf(dend, Hs[32 * half + j], g[j]);
-            }
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = Hs[32 * half + j];
-                store_split32(sm + Layout::kHh, sm + Layout::kHl, row, 4 * half, v);
-            }
-            ptx::fence_proxy_async_shared();
-            fence_before_sync();
-            warp_arrive(&bar[kHReady], lane);
+            ecum_prev = ecum;
+            dend_prev = dend;
+        }
+        // the last chunk's state and outputs
+        if (!failed && nchunks > 0) {
+            if (!state_update(nchunks - 1, dend_prev) || !outputs(nchunks - 1, ecum_prev))
+                failed = true;
         }
         if (failed && lane == 0) atomicOr(&g_error_word, kErrTimeout);
         if (!failed && a.h_last && row < a.N) {
             float* base = a.h_last + (b * a.H + hh) * P * (long long)a.N + row;
 #pragma unroll
-            for (int p = 0; p < P; ++p) base[(long long)p * a.N] = Hs[p];
+            for (int j = 0; j < 32; ++j) base[(long long)(32 * hf + j) * a.N] = Hs[j];
         }
     }
-    // ---- tear-down: every TMEM read and MMA is done before the columns go
+    // ---- tear-down: every TMEM access and MMA is done before the columns go
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
