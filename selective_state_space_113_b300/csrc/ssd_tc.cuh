@@ -527,30 +527,40 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             if (c > 0 && !state_update(c - 1, dend_prev)) { failed = true; break; }
             // this row's cumulative decay (log2 units) and step size, and the chunk's total
             if (!wwait(&bar[kCum], ph, a.wait_ns)) { failed = true; break; }
-            const float ct = cum[row], dt_t = dts[row], cend2 = cum[Q - 1];
+            const float ct = cum[row], cend2 = cum[Q - 1];
             const float ecum = ptx::ex2(ct);                 // exp(cum_t)
-            const float wt = ptx::ex2(cend2 - ct) * dt_t;    // w_t
             const float dend = ptx::ex2(cend2);              // exp(cum_end)
             if (!wwait(&bar[kInFull + (int)(c & 1)], (uint32_t)((c >> 1) & 1), a.wait_ns)) {
                 failed = true;
                 break;
             }
-            // w o X, row s = row, this warp's 32 columns, split hi + lo (the
-            // previous chunk's G, which read them, completed: state_update)
+            // w o X, split hi + lo (the previous chunk's G, which read them,
+            // completed: state_update).  The causal mask gives the warps of
+            // lane quadrants 2 and 3 the most score columns, so the warps of
+            // quadrants 0 and 1 form all of w o X: warp e < 4 (quad 0 or 1,
+            // column half hf) takes rows s = 32 (e & 1) + lane and s + 64 of
+            // its column half, with the w_s of those rows from the shared copy.
+            if (quad < 2) {
 #pragma unroll
-            for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(row, cc));
-                const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
-                uint4 h, l;
-                uint32_t* hp = &h.x;
-                uint32_t* lp = &l.x;
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int s_ = 32 * quad + 64 * rr + lane;
+                    const float ws = ptx::ex2(cend2 - cum[s_]) * dts[s_];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 f = __bfloat1622float2(x2[q]);
-                    split2(wt * f.x, wt * f.y, hp[q], lp[q]);
+                    for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
+                        const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(s_, cc));
+                        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+                        uint4 h, l;
+                        uint32_t* hp = &h.x;
+                        uint32_t* lp = &l.x;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = __bfloat1622float2(x2[q]);
+                            split2(ws * f.x, ws * f.y, hp[q], lp[q]);
+                        }
+                        *reinterpret_cast<uint4*>(sm + Layout::kWh + sw128(s_, cc)) = h;
+                        *reinterpret_cast<uint4*>(sm + Layout::kWl + sw128(s_, cc)) = l;
+                    }
                 }
-                *reinterpret_cast<uint4*>(sm + Layout::kWh + sw128(row, cc)) = h;
-                *reinterpret_cast<uint4*>(sm + Layout::kWl + sw128(row, cc)) = l;
             }
             // the previous chunk's outputs (its Yi ran after G)
             if (c > 0 && !outputs(c - 1, ecum_prev)) { failed = true; break; }
