@@ -466,29 +466,45 @@ def bench_decode(ssm, dev, stream, reps: int = 5):
     peak, kind = measured_peaks()
     us = graph_ms * 1e3 / w.steps
     gbs = per_step / (us * 1e-6) / 1e9
-    # each step with L2 flushed before it (a write larger than L2 between
-    # steps, outside the events): the state then comes from DRAM every step
-    flush = torch.empty(64 << 20, device=dev, dtype=torch.float32)   # 256 MB > 126 MB L2
-    state.copy_(state0)
-    cold = []
-    for s_ in range(w.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        ssm.ssm_step(state, inp["u"][s_], inp["delta"][s_], inp["dt_bias"], inp["A"],
-                     inp["B"][s_], inp["C"][s_], inp["Dskip"], inp["z"][s_], ys[s_])
-        e1.record()
-        e1.synchronize()
-        cold.append(e0.elapsed_time(e1))
-    cold_us = sorted(cold)[len(cold) // 2] * 1e3
+    # each step with L2 flushed before it, outside the events: a 256 MB
+    # buffer (> 126 MB L2) is written and then read back, so the state comes
+    # from DRAM and L2 holds only clean lines of the buffer.  A flush that
+    # only writes leaves up to 126 MB of the buffer's dirty lines in L2, whose
+    # write-back then lands inside the timed step; that figure is reported
+    # beside it.
+    flush = torch.empty(64 << 20, device=dev, dtype=torch.float32)
+
+    def cold(read_back: bool):
+        state.copy_(state0)
+        times = []
+        for s_ in range(w.steps):
+            flush.zero_()
+            if read_back:
+                flush.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ssm.ssm_step(state, inp["u"][s_], inp["delta"][s_], inp["dt_bias"], inp["A"],
+                         inp["B"][s_], inp["C"][s_], inp["Dskip"], inp["z"][s_], ys[s_])
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return sorted(times)[len(times) // 2] * 1e3
+
+    cold_us = cold(True)
+    cold_w_us = cold(False)
     return {"workload": w.name, "steps": w.steps, "bytes_per_step": per_step,
             "us_per_step_graph": us, "us_per_step_launches": plain_ms * 1e3 / w.steps,
             "us_per_step_l2_flushed": cold_us,
             "gbs_l2_flushed": per_step / (cold_us * 1e-6) / 1e9,
+            "hbm_frac_l2_flushed": per_step / (cold_us * 1e-6) / 1e9 / peak,
+            "us_per_step_l2_write_flushed": cold_w_us,
             "elements_per_s": w.batch * w.D / (us * 1e-6), "gbs": gbs,
             "hbm_frac": gbs / peak, "peak_source": kind, "kernel_launches": w.steps,
-            "note": "best of %d; the 84 MB state can stay resident in the 126 MB L2 across "
-                    "steps, so GB/s is algorithmic bytes / time, not DRAM traffic" % reps}
+            "note": "graph: best of %d replays of the 64 steps (the 84 MB state can stay "
+                    "resident in the 126 MB L2 across steps, so GB/s there is algorithmic "
+                    "bytes / time, not DRAM traffic); l2_flushed: median step after a "
+                    "256 MB write + read-back flush; l2_write_flushed: after a write-only "
+                    "flush, which adds the write-back of its dirty lines" % reps}
 
 
 def bench_configs(ssm, dev, stream, reps: int = 20):

@@ -322,7 +322,30 @@ extern "C" int ssm_step(float* state, const void* u, const void* delta, const fl
     cudaError_t e;
     if (N == ssm::stepk::NS && all_aligned16({state, A}) && D <= ssm::stepk::kMaxD &&
         batch <= ssm::stepk::kMaxBatch && !std::getenv("SSM_FORCE_GENERIC_STEP")) {
-        // Fast path: four threads per channel, one float4 of state each.
+        // Tiled path: persistent CTAs, tensor copies of 128-channel x 4-entry
+        // tiles (needs D % 8 == 0 and 16-byte aligned rows).
+        // SSM_STEP_KERNEL=threads selects the one-pass kernel below instead.
+        const char* kname = std::getenv("SSM_STEP_KERNEL");
+        if (D % 8 == 0 && all_aligned16({u, delta, z, B, C}) &&
+            ((D + ssm::stepk::kTileTC - 1) / ssm::stepk::kTileTC) *
+                    ((batch + ssm::stepk::kTileNB - 1) / ssm::stepk::kTileNB) < INT32_MAX &&
+            !(kname && std::strcmp(kname, "threads") == 0)) {
+            const unsigned long long wait_ns =
+                (unsigned long long)ssm::tile::env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL);
+            if (dtype == SSM_F32)
+                e = ssm::stepk::launch_step16_tiled<float>(
+                    state, static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias,
+                    A, static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
+                    static_cast<const float*>(z), static_cast<float*>(y), batch, D, wait_ns,
+                    stream);
+            else
+                e = ssm::stepk::launch_step16_tiled<bf16>(
+                    state, static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias,
+                    A, static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
+                    static_cast<const bf16*>(z), static_cast<bf16*>(y), batch, D, wait_ns, stream);
+            return from_cuda(e);
+        }
+        // One-pass path: four threads per channel, one float4 of state each.
         if (dtype == SSM_F32)
             e = ssm::stepk::launch_step16<float>(
                 state, static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,

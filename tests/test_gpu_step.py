@@ -60,14 +60,26 @@ def check_steps(inp, steps, chans, what):
 
 
 def test_decode_full_size_64_steps_sampled():
-    """The 256 x 5120 decode, 64 steps: 320 channels, with both channels of
-    the pair each thread group handles (d and d + D/2) and every batch row's
+    """The 256 x 5120 decode, 64 steps: 320 channels, d and d + D/2 (the pair
+    one thread group of the one-pass kernel handles) with every batch row's
     first and last channel among them."""
     inp = wl.make_step_inputs(wl.DECODE, device=DEV)
     half = wl.DECODE.D // 2
     base = parity.sample_channels(wl.DECODE.batch, half, 160, seed=5)
     chans = sorted({c for b, d in base for c in ((b, d), (b, d + half))})
     check_steps(inp, wl.DECODE.steps, chans, "decode")
+
+
+def test_decode_full_size_tiled_matches_one_pass(monkeypatch):
+    """At 256 x 5120, the tiled kernel (what the benchmark times) and the
+    one-pass kernel agree over 4 steps: the state to 2e-6 relative (they
+    round the B_bar coefficient differently) and y to one bf16 unit."""
+    inp = wl.make_step_inputs(wl.DECODE, device=DEV)
+    st, y = gpu_steps(inp, 4)
+    monkeypatch.setenv("SSM_STEP_KERNEL", "threads")
+    st_ref, y_ref = gpu_steps(inp, 4)
+    parity.check(parity.to_f64(st), parity.to_f64(st_ref), 2e-6, "tiled vs one-pass state")
+    parity.check(parity.to_f64(y), parity.to_f64(y_ref), 8e-3, "tiled vs one-pass y")
 
 
 @pytest.mark.parametrize("N", [1, 5, 16, 32, 256])
@@ -117,6 +129,7 @@ def test_fast_step_matches_generic(monkeypatch, dtype, per_group):
     w = wl.StepWorkload("small", 3, 203, 16, 4, dtype, 11)
     inp = wl.make_step_inputs(w, device=DEV)
     monkeypatch.delenv("SSM_FORCE_GENERIC_STEP", raising=False)
+    monkeypatch.setenv("SSM_STEP_KERNEL", "threads")
     monkeypatch.setenv("SSM_STEP_J", per_group)
     st_fast, y_fast = gpu_steps(inp, 4)
     monkeypatch.setenv("SSM_FORCE_GENERIC_STEP", "1")
@@ -124,3 +137,49 @@ def test_fast_step_matches_generic(monkeypatch, dtype, per_group):
     tol = parity.TOL[dtype]
     parity.check(parity.to_f64(st_fast), parity.to_f64(st_gen), 1e-5, "fast vs generic state")
     parity.check(parity.to_f64(y_fast), parity.to_f64(y_gen), tol, "fast vs generic y")
+
+
+TILED_CASES = [  # (batch, D, steps): D % 8 == 0 takes the tiled kernel (128 channels x 4 entries)
+    (3, 200, 3),     # a full and a ragged (72-channel) block; 3 of a tile's 4 entries
+    (64, 1024, 2),   # 128 tiles: CTAs cross channel blocks
+    (1, 8, 2),       # one 8-channel, 1-entry tile
+    (5, 136, 2),     # 4 + 1 entries, 128 + 8 channels
+    (9, 384, 2),
+]
+
+
+@pytest.mark.parametrize("batch,D,steps", TILED_CASES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_tiled_step_matches_oracle_and_one_pass(monkeypatch, batch, D, steps, dtype):
+    """The tiled decode kernel (persistent CTAs, tensor copies of whole
+    tiles, out-of-range channels and entries read as zeros and not stored)
+    against the oracle on every channel, and against the one-pass kernel."""
+    w = wl.StepWorkload("small", batch, D, 16, steps, dtype, 200 + D)
+    inp = wl.make_step_inputs(w, device=DEV)
+    monkeypatch.delenv("SSM_FORCE_GENERIC_STEP", raising=False)
+    monkeypatch.delenv("SSM_STEP_KERNEL", raising=False)
+    chans = [(b, d) for b in range(batch) for d in range(D)]
+    if len(chans) > 600:
+        chans = parity.sample_channels(batch, D, 600, seed=D)
+    check_steps(inp, steps, chans, f"tiled {batch}x{D} {dtype}")
+    assert ssm.ssm_device_status() == 0
+    st, y = gpu_steps(inp, steps)
+    monkeypatch.setenv("SSM_STEP_KERNEL", "threads")
+    st_ref, y_ref = gpu_steps(inp, steps)
+    parity.check(parity.to_f64(st), parity.to_f64(st_ref), 2e-6, "tiled vs one-pass state")
+    parity.check(parity.to_f64(y), parity.to_f64(y_ref), parity.TOL[dtype], "tiled vs one-pass y")
+
+
+def test_tiled_step_optional_null_and_zero_A():
+    """z, D and dt_bias absent (the z copy is skipped, the others read as
+    zero), and A with zero entries, where B_bar = dt B (the limit the oracle
+    takes)."""
+    w = wl.StepWorkload("small", 4, 256, 16, 2, torch.bfloat16, 17)
+    chans = [(b, d) for b in range(4) for d in range(0, 256, 3)]
+    for drop in ("z", "Dskip", "dt_bias"):
+        inp = wl.make_step_inputs(w, device=DEV)
+        inp[drop] = None
+        check_steps(inp, 2, chans, f"tiled {drop}=NULL")
+    inp = wl.make_step_inputs(w, device=DEV)
+    inp["A"][::3, ::2] = 0.0
+    check_steps(inp, 2, chans, "tiled A with zeros")
