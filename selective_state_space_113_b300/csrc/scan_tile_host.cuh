@@ -11,48 +11,23 @@
 #include "../../include/ssmscan.h"
 #include "faults.cuh"
 #include "scan_tile.cuh"
+#include "tma_host.cuh"
 
 namespace ssm {
 namespace tile {
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver, found once through the runtime (no
-// link-time dependency on libcuda).
-inline EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// Rank-3 map over a row-major [batch, L, inner] tensor, box {box_inner, box_t, 1}.
+// Rank-3 map over a row-major [batch, L, inner] tensor, box {box_inner, box_t, 1}
+// (through the encode cache: a caller that reuses its buffers encodes once).
 template <typename T>
 inline bool make_map(CUtensorMap* m, const void* base, long long inner, long long L,
                      long long batch, unsigned box_inner, unsigned box_t) {
-    EncodeTiledFn fn = encode_tiled();
-    if (!fn) return false;
     const cuuint64_t es = sizeof(T);
     const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)L, (cuuint64_t)batch};
     const cuuint64_t strides[2] = {(cuuint64_t)inner * es, (cuuint64_t)inner * (cuuint64_t)L * es};
     const cuuint32_t box[3] = {box_inner, box_t, 1u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return tma::cached_map(m, dt, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 inline long long env_ll(const char* name, long long dflt) {

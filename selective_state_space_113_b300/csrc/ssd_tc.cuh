@@ -25,7 +25,7 @@
 // Yi); C, B and X are double-buffered, so a chunk's loads and its S overlap
 // the previous chunk's epilogue.
 //
-// One CTA owns one (b, h) and walks its chunks in order.  Five warps:
+// One CTA owns one (b, h) and walks its chunks in order.  Nine warps:
 //   warp 8      control: TMA loads of a chunk's C, B (K-major, two 64-wide
 //               regions each) and X (its 128 steps x 64 channels) into one of
 //               two buffers, and the MMAs, one elected thread, each group
@@ -654,9 +654,9 @@ inline cudaError_t launch_ssd_tc(const bf16* x, const bf16* dt, const float* dt_
     const cuuint64_t sBC[2] = {(cuuint64_t)N * es, (cuuint64_t)L * N * es};
     const cuuint32_t bBC[3] = {64u, (cuuint32_t)Q, 1u};
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!tma::make_map(&mX, bf, 4, x, dX, sX, bX, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tma::make_map(&mB, bf, 3, Bm, dBC, sBC, bBC, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tma::make_map(&mC, bf, 3, Cm, dBC, sBC, bBC, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!tma::cached_map(&mX, bf, 4, x, dX, sX, bX, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tma::cached_map(&mB, bf, 3, Bm, dBC, sBC, bBC, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tma::cached_map(&mC, bf, 3, Cm, dBC, sBC, bBC, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     Args a;
     a.x = x;

@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 #include "faults.cuh"
@@ -369,7 +370,10 @@ step16_tiled_kernel(const __grid_constant__ StepMaps maps, float* __restrict__ s
                 y[row0 + ch] = from_f32<T>(acc);
             }
         }
-        // every value read from the stage has been used: hand it back
+        // every value read from the stage has been used, and the new state
+        // written into it is ordered before the copy engine's next writes
+        // there: hand it back
+        ptx::fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(freed + s);
     }
@@ -395,7 +399,7 @@ static cudaError_t launch_step16_tiled(float* state, const T* u, const T* delta,
         const cuuint64_t dims[3] = {NS, (cuuint64_t)D, (cuuint64_t)batch};
         const cuuint64_t strides[2] = {NS * 4, (cuuint64_t)D * NS * 4};
         const cuuint32_t box[3] = {NS, TC, NB};
-        if (!tma::make_map(&m.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, state, dims, strides, box,
+        if (!tma::cached_map(&m.state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, state, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     }
@@ -403,9 +407,9 @@ static cudaError_t launch_step16_tiled(float* state, const T* u, const T* delta,
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)batch, 1};
         const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)D * es * (cuuint64_t)batch};
         const cuuint32_t box[3] = {TC, NB, 1};
-        if (!tma::make_map(&m.u, dt, 3, u, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !tma::make_map(&m.delta, dt, 3, delta, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            (z && !tma::make_map(&m.z, dt, 3, z, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        if (!tma::cached_map(&m.u, dt, 3, u, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !tma::cached_map(&m.delta, dt, 3, delta, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            (z && !tma::cached_map(&m.z, dt, 3, z, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)))
             return cudaErrorInvalidValue;
         if (!z) m.z = m.u;   // not read
     }
@@ -413,16 +417,31 @@ static cudaError_t launch_step16_tiled(float* state, const T* u, const T* delta,
         const cuuint64_t dims[3] = {NS, (cuuint64_t)batch, 1};
         const cuuint64_t strides[2] = {NS * es, NS * es * (cuuint64_t)batch};
         const cuuint32_t box[3] = {NS, NB, 1};
-        if (!tma::make_map(&m.B, dt, 3, Bm, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !tma::make_map(&m.C, dt, 3, Cm, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (!tma::cached_map(&m.B, dt, 3, Bm, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !tma::cached_map(&m.C, dt, 3, Cm, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
+    // per device, once: the kernel's shared-memory limit and the SM count
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static int sms_of[kMaxDev] = {};
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDev) {
+        std::lock_guard<std::mutex> lock(mu);
+        sms = sms_of[dev];
+    }
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDev) {
+            std::lock_guard<std::mutex> lock(mu);
+            sms_of[dev] = sms;
+        }
+    }
     const long long tiles = ((D + TC - 1) / TC) * ((batch + NB - 1) / NB);
     const long long grid = tiles < sms ? tiles : sms;
     if (fault::launch_refused()) return cudaErrorLaunchFailure;
