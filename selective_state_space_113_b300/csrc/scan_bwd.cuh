@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tmem.cuh"
 
 namespace ssm {
 namespace bwd {
@@ -51,7 +52,7 @@ constexpr int NS = 16;
 constexpr int CB = 128;       // channels per CTA, one per thread
 constexpr int NW = CB / 32;   // warps per CTA
 constexpr int TU = 32;        // steps per unit (the checkpoint interval)
-constexpr int KS = 8;         // steps per recomputed sub-chunk
+constexpr int KS = 4;         // steps per recomputed sub-chunk
 constexpr int NSUB = TU / KS;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -201,6 +202,8 @@ __device__ __forceinline__ void cpa16(void* dst, const void* src, bool ok) {
 __device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // every group but the newest one complete (this thread's copies)
 __device__ __forceinline__ void cpa_wait_prior() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// every group of this thread complete
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Unit of index i in the list of units with k >= 1.
 __device__ __forceinline__ Unit adj_unit(const BwdParams& p, long long i) {
@@ -418,12 +421,39 @@ __device__ __forceinline__ float warp_reduce32(float (&v)[32], int lane) {
     return v[0];
 }
 
+template <typename T>
 struct BwdSmem {
-    float4 starts[NSUB][NS / 4][CB];   // state at each sub-chunk start
-    float4 hist[KS][NS / 4][CB];       // h_t of the current sub-chunk
+    T in[4][TU][CB];                   // u, delta, z, dy of the unit
+    float4 hist[KS][NS / 4][CB];       // h_t of the sub-chunk walked back
     float red[KS][NW][32];             // per-warp dB/dC sums
     float Bs[TU * NS], Bp[TU * NS], Cs[TU * NS];
+    uint32_t tmem;                     // TMEM base: the state at each sub-chunk start
 };
+
+// The unit's u, delta, z and dy (rows t0 .. t1 - 1, channels cb*CB .. +CB-1)
+// into shared memory, 16-byte pieces by cp.async (zero-filled, nothing read,
+// past D or past the unit's end; D is a multiple of the piece).
+template <typename T>
+__device__ __forceinline__ void bwd_issue(const BwdParams& p, const Unit& w, BwdSmem<T>& sm) {
+    constexpr int EPP = 16 / (int)sizeof(T);   // elements per 16-byte piece
+    constexpr int CPR = CB / EPP;              // pieces per row
+    const long long rows = w.t1 - w.t0;
+    const long long d0 = w.cb * CB;
+    const long long base = (w.b * p.L + w.t0) * p.D + d0;
+    const T* src[4] = {static_cast<const T*>(p.u), static_cast<const T*>(p.delta),
+                       static_cast<const T*>(p.z), static_cast<const T*>(p.dy)};
+    for (int q = threadIdx.x; q < TU * CPR; q += CB) {
+        const int r = q / CPR, c = q - r * CPR;
+        const bool ok = r < rows && d0 + c * EPP < p.D;
+        const long long off = ok ? base + r * p.D + c * EPP : 0;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+            if (src[a]) cpa16(&sm.in[a][r][c * EPP], src[a] + off, ok);
+    }
+}
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
 
 // One forward step (the forward kernel's arithmetic): h <- Abar h + q B u.
 __device__ __forceinline__ void fwd_step(float (&h)[NS], const Chan& c, const float (&arow)[NS],
@@ -457,14 +487,22 @@ __device__ __forceinline__ void fwd_step(float (&h)[NS], const Chan& c, const fl
 }
 
 template <typename T>
-__global__ void __launch_bounds__(CB, 2)
+__global__ void __launch_bounds__(CB, 3)
 bwd_unit_kernel(const BwdParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
+    BwdSmem<T>& sm = *reinterpret_cast<BwdSmem<T>*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long G = gridDim.x;
     const long long r0 = blockIdx.x * p.units / G, r1 = (blockIdx.x + 1) * p.units / G;
     const long long nch = p.batch * p.D;
+
+    // TMEM: 128 columns, the states at the NSUB sub-chunk starts (16 columns
+    // each); warp w's threads own lanes 32 w .. 32 w + 31
+    if (warp == 0) tmem::alloc(&sm.tmem, 128);
+    tmem::fence_before_sync();
+    __syncthreads();
+    tmem::fence_after_sync();
+    const uint32_t tbase = sm.tmem + ((uint32_t)(32 * warp) << 16);
 
     long long cur_cb = -1;
     float dacc[NS];            // dA accumulator of the channel (see the header)
@@ -501,18 +539,20 @@ bwd_unit_kernel(const BwdParams p) {
             valid = d < p.D;
             c = load_chan(p, d, valid, arow);
         }
-        __syncthreads();   // the previous unit is done with the rows
+        __syncthreads();   // the previous unit is done with the rows and inputs
+        bwd_issue<T>(p, w, sm);
+        cpa_commit();
         load_rows<T>(p, w, sm.Bs, sm.Bp, sm.Cs, true);
+        cpa_wait_all();
         __syncthreads();
 
         const long long base = w.b * p.L * p.D + (valid ? d : 0);
-        const T* usrc = static_cast<const T*>(p.u) + base;
-        const T* dsrc = static_cast<const T*>(p.delta) + base;
-        const T* zsrc = p.z ? static_cast<const T*>(p.z) + base : nullptr;
-        const T* ysrc = static_cast<const T*>(p.dy) + base;
+        const bool zsrc = p.z != nullptr;
         const long long ch = w.b * p.D + (valid ? d : 0);
+        const int nsteps = (int)(w.t1 - w.t0);
+        const int s_last = (nsteps - 1) / KS;
 
-        // sweep 1: the states at the sub-chunk starts
+        // sweep 1: the states at the sub-chunk starts, into TMEM
         float h[NS];
         {
             const float4* hs = reinterpret_cast<const float4*>(p.hin + (w.k * nch + ch) * NS);
@@ -525,44 +565,18 @@ bwd_unit_kernel(const BwdParams p) {
                 h[4 * q + 3] = v.w;
             }
         }
-        const int nsteps = (int)(w.t1 - w.t0);
-        // Sub-chunk s is needed here only if another follows it (then it is
-        // full); its loads are issued one sub-chunk ahead.
-        const int nsw1 = (nsteps - 1) / KS;   // sub-chunks walked by sweep 1
-        float u1[KS], d1[KS];
-        if (nsw1 > 0) {
-#pragma unroll
-            for (int j = 0; j < KS; ++j) {
-                u1[j] = valid ? ldf(usrc + (w.t0 + j) * p.D) : 0.0f;
-                d1[j] = valid ? ldf(dsrc + (w.t0 + j) * p.D) : 0.0f;
-            }
-        }
-        for (int s = 0; s < NSUB; ++s) {
-#pragma unroll
-            for (int q = 0; q < NS / 4; ++q)
-                sm.starts[s][q][tid] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-            if (s >= nsw1) break;   // later starts are not used
-            float uc[KS], dc[KS];
-#pragma unroll
-            for (int j = 0; j < KS; ++j) {
-                uc[j] = u1[j];
-                dc[j] = d1[j];
-            }
-            if (s + 1 < nsw1) {
-#pragma unroll
-                for (int j = 0; j < KS; ++j) {
-                    const long long t = w.t0 + (s + 1) * KS + j;   // a full sub-chunk
-                    u1[j] = valid ? ldf(usrc + t * p.D) : 0.0f;
-                    d1[j] = valid ? ldf(dsrc + t * p.D) : 0.0f;
-                }
-            }
+        for (int s = 0; s < s_last; ++s) {
+            tmem::st16(tbase + (uint32_t)(NS * s), h);
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
                 const int tt = s * KS + j;
-                fwd_step(h, c, arow, uc[j], softplus_l2(fmaf(dc[j], kLog2e, c.kb2)),
+                fwd_step(h, c, arow, to_f(sm.in[0][tt][tid]),
+                         softplus_l2(fmaf(to_f(sm.in[1][tt][tid]), kLog2e, c.kb2)),
                          sm.Bs + tt * NS, sm.Bp + tt * NS);
             }
         }
+        tmem::st16(tbase + (uint32_t)(NS * s_last), h);
+        tmem::wait_st();
 
         // the adjoint entering the unit at its end
         float lam[NS];
@@ -578,48 +592,23 @@ bwd_unit_kernel(const BwdParams p) {
             }
         }
 
-        // sweep 2: sub-chunks from the last, each recomputed then walked back
-        // Inputs of the sub-chunk walked next, loaded one sub-chunk ahead
-        // (raw u, delta, z, dy; zero past the unit's end).
-        float nu[KS], nd[KS], nz[KS], ny[KS];
-        auto load_sub = [&](int tb2) {
-#pragma unroll
-            for (int j = 0; j < KS; ++j) {
-                const bool in = valid && tb2 + j < nsteps;
-                const long long t = w.t0 + tb2 + j;
-                nu[j] = in ? ldf(usrc + t * p.D) : 0.0f;
-                nd[j] = in ? ldf(dsrc + t * p.D) : 0.0f;
-                nz[j] = (in && zsrc) ? ldf(zsrc + t * p.D) : 0.0f;
-                ny[j] = in ? ldf(ysrc + t * p.D) : 0.0f;
-            }
-        };
-        const int s_last = (nsteps - 1) / KS;
-        load_sub(s_last * KS);
+        // sweep 2: sub-chunks from the last, each recomputed into shared
+        // memory from its start state, then walked back
         for (int s = s_last; s >= 0; --s) {
             const int tb = s * KS;
             const int cnt = nsteps - tb < KS ? nsteps - tb : KS;
+            tmem::ld16(tbase + (uint32_t)(NS * s), h);
+            tmem::wait_ld();
+            float dlj[KS];
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q) {
-                const float4 v = sm.starts[s][q][tid];
-                h[4 * q] = v.x;
-                h[4 * q + 1] = v.y;
-                h[4 * q + 2] = v.z;
-                h[4 * q + 3] = v.w;
-            }
-            float uj[KS], dlj[KS], vj[KS], zj[KS], dyj[KS];
+            for (int j = 0; j < KS; ++j)
+                dlj[j] = j < cnt ? softplus_l2(fmaf(to_f(sm.in[1][tb + j][tid]), kLog2e, c.kb2))
+                                 : 0.0f;
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
-                uj[j] = nu[j];
-                zj[j] = nz[j];
-                dyj[j] = ny[j];
-                vj[j] = fmaf(nd[j], kLog2e, c.kb2);
-                dlj[j] = j < cnt ? softplus_l2(vj[j]) : 0.0f;
-            }
-            if (s > 0) load_sub(tb - KS);
-#pragma unroll
-            for (int j = 0; j < KS; ++j) {
-                if (j < cnt) {
-                    fwd_step(h, c, arow, uj[j], dlj[j], sm.Bs + (tb + j) * NS, sm.Bp + (tb + j) * NS);
+                if (j < cnt) {   // uniform over the CTA
+                    fwd_step(h, c, arow, to_f(sm.in[0][tb + j][tid]), dlj[j],
+                             sm.Bs + (tb + j) * NS, sm.Bp + (tb + j) * NS);
 #pragma unroll
                     for (int q = 0; q < NS / 4; ++q)
                         sm.hist[j][q][tid] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
@@ -633,13 +622,16 @@ bwd_unit_kernel(const BwdParams p) {
                 const float* Bt = sm.Bs + tt * NS;
                 const float* Bpt = sm.Bp + tt * NS;
                 const float* Ct = sm.Cs + tt * NS;
-                const float u = uj[j], dl = dlj[j], dt = dl * kLn2;
+                const float u = to_f(sm.in[0][tb + j][tid]), dl = dlj[j], dt = dl * kLn2;
+                const float zjj = zsrc ? to_f(sm.in[2][tb + j][tid]) : 0.0f;
+                const float dyjj = to_f(sm.in[3][tb + j][tid]);
+                const float vjj = fmaf(to_f(sm.in[1][tb + j][tid]), kLog2e, c.kb2);
                 float g = 1.0f, sg = 0.0f;
                 if (zsrc) {
-                    sg = ptx::rcp(1.0f + ptx::ex2(-zj[j] * kLog2e));
-                    g = zj[j] * sg;
+                    sg = ptx::rcp(1.0f + ptx::ex2(-zjj * kLog2e));
+                    g = zjj * sg;
                 }
-                const float ds = dyj[j] * g;
+                const float ds = dyjj * g;
                 float hv[NS];
 #pragma unroll
                 for (int q = 0; q < NS / 4; ++q) {
@@ -698,7 +690,7 @@ bwd_unit_kernel(const BwdParams p) {
                     }
                 }
                 const float du = fmaf(ds, c.dsk, c.geo ? vsum * c.ia0 : vsum);
-                const float dd = ddt * sigmoid_l2(vj[j]);
+                const float dd = ddt * sigmoid_l2(vjj);
                 dsk_acc = fmaf(ds, u, dsk_acc);
                 dtb_acc += dd;
                 if (valid) {
@@ -706,7 +698,7 @@ bwd_unit_kernel(const BwdParams p) {
                     static_cast<T*>(p.du)[o] = from_f32<T>(du);
                     static_cast<T*>(p.ddelta)[o] = from_f32<T>(dd);
                     if (zsrc) {
-                        const float dzv = dyj[j] * sacc * sg * fmaf(zj[j], 1.0f - sg, 1.0f);
+                        const float dzv = dyjj * sacc * sg * fmaf(zjj, 1.0f - sg, 1.0f);
                         static_cast<T*>(p.dz)[o] = from_f32<T>(dzv);
                     }
                 }
@@ -727,6 +719,10 @@ bwd_unit_kernel(const BwdParams p) {
         }
     }
     flush();
+    tmem::fence_before_sync();
+    __syncthreads();
+    tmem::fence_after_sync();
+    if (warp == 0) tmem::dealloc(sm.tmem, 128);
 }
 
 // dC[b,t,n] = sum over blocks of part[..][n]; dB[b,t,n] = that of part[..][16+n] / (n+1).

@@ -23,6 +23,37 @@ inline cudaError_t resident(K kern, int threads, int smem, int* per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, threads, smem);
 }
 
+// CTAs of a kernel that fit on one SM by its registers, shared memory and
+// threads, and by `tmem_cols` columns of the SM's 512 TMEM columns per CTA.
+// For kernels that allocate TMEM the occupancy query answers 1 (it cannot
+// know how many columns a CTA takes); the allocation itself waits for free
+// columns, so this count is what the SM actually holds.
+template <typename K>
+inline cudaError_t resident_tmem(K kern, int threads, int smem, int tmem_cols, int* per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+    int dev = 0, regs_sm = 0, smem_sm = 0, resv = 0, thr_sm = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+    if (e != cudaSuccess) return e;
+    const int warps = (threads + 31) / 32;
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;   // allocated per warp in units of 256
+    const int by_regs = regs_sm / (regs_warp * warps);
+    const int by_smem = smem_sm / (smem + (int)fa.sharedSizeBytes + resv);
+    const int by_thr = thr_sm / (warps * 32);
+    const int by_tmem = 512 / tmem_cols;
+    int n = by_regs < by_smem ? by_regs : by_smem;
+    n = n < by_thr ? n : by_thr;
+    n = n < by_tmem ? n : by_tmem;
+    *per_sm = n;
+    return cudaSuccess;
+}
+
 // Returns an ssm_status_t.  Preconditions (checked by the caller): N == 16;
 // u, delta, z, dy, B, C, A and du 16-byte aligned; D * sizeof(T) % 16 == 0;
 // batch*D > 0; L > 0; dz given when z is.
@@ -42,7 +73,7 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
         return SSM_ERR_CUDA;
     int occ_sum = 0, occ_unit = 0;
     if (resident(adjoint_summary_kernel<T>, CB, (int)sizeof(AdjSmem<T>), &occ_sum) != cudaSuccess ||
-        resident(bwd_unit_kernel<T>, CB, (int)sizeof(BwdSmem), &occ_unit) != cudaSuccess ||
+        resident_tmem(bwd_unit_kernel<T>, CB, (int)sizeof(BwdSmem<T>), 128, &occ_unit) != cudaSuccess ||
         occ_sum < 1 || occ_unit < 1)
         return SSM_ERR_CUDA;
 
@@ -155,7 +186,7 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
         // 3. the unit kernel
         {
             const long long g = (long long)sms * occ_unit;
-            bwd_unit_kernel<T><<<(unsigned)(bp.units < g ? bp.units : g), CB, sizeof(BwdSmem),
+            bwd_unit_kernel<T><<<(unsigned)(bp.units < g ? bp.units : g), CB, sizeof(BwdSmem<T>),
                                  stream>>>(bp);
         }
         // 4. dB and dC
