@@ -29,16 +29,17 @@
 //      Q_k = Abar_{t0} lam_{t0} and sum(dl); adj_carry_kernel combines them
 //      from the last unit down into mu[k], the adjoint entering unit k at its
 //      end (mu[P-1] = dh_last);
-//   3. bwd_unit_kernel: per unit, a forward sweep from hin[k] stores the
-//      states at the start of each KS-step sub-chunk in shared memory; then,
-//      sub-chunk by sub-chunk from the last, the states of the sub-chunk are
-//      recomputed into shared memory and walked backward from mu[k].  dB and
-//      dC are summed over the warp's 32 channels by a butterfly of shuffles
-//      and over the CTA's 128 channels in shared memory, then written as one
-//      partial per 128-channel block;
+//   3. bwd_unit_kernel: per unit, the unit's inputs come into shared memory
+//      by cp.async; a forward sweep from hin[k] stores the states at the
+//      start of each KS-step sub-chunk in TMEM (16 columns per start, each
+//      thread in its own lane); then, sub-chunk by sub-chunk from the last,
+//      the states of the sub-chunk are recomputed into shared memory and
+//      walked backward from mu[k].  dB and dC are summed over the warp's 32
+//      channels by a butterfly of shuffles and over the CTA's 128 channels in
+//      shared memory, then written as one partial per 128-channel block;
 //   4. bwd_reduce_bc_kernel sums the partials over the blocks.
-// Threads: one channel per thread, 128 channels (4 warps) per CTA; two CTAs
-// share an SM.
+// Threads: one channel per thread, 128 channels (4 warps) per CTA; three
+// CTAs share an SM (74 KB of shared memory and 128 TMEM columns each).
 #pragma once
 
 #include "common.cuh"
