@@ -622,9 +622,47 @@ def bench_backward(ssm, inp, w, stream, reps: int = 5):
     es = 2 if "bf16" in w.name else 4
     nbytes = (7 * es * w.elements + 2 * w.batch * w.L * w.N * (es + 4)
               + w.D * w.N * 8 + w.batch * w.D * w.N * 4 + 6 * w.D * 4)
+
+    # The training pairing: a forward pass that writes the state entering
+    # every 32-step unit, and the backward pass that reads them instead of
+    # recomputing them (ssm_scan_fwd_ckpt / ssm_scan_bwd_ckpt).
+    ckpt = torch.empty(((w.L + 31) // 32, w.batch, w.D, w.N), device=dev)
+    y, h = torch.empty_like(u), torch.empty((w.batch, w.D, w.N), device=dev)
+
+    def fwd_ckpt():
+        ssm.ssm_scan_fwd_ckpt(u, inp["delta"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                              inp["Dskip"], inp["z"], y, h, ckpt, stream=stream)
+
+    def bwd_ckpt():
+        ssm.ssm_scan_bwd_ckpt(u, inp["delta"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                              inp["Dskip"], inp["z"], dy, dh, ckpt, du, ddelta, ddt_bias, dA, dB,
+                              dC, dDskip, dz, stream=stream)
+
+    def best_of(fn):
+        for _ in range(3):
+            fn()
+        b = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            b = ms if b is None or ms < b else b
+        return b
+
+    fwd_ckpt_ms = best_of(fwd_ckpt)
+    bwd_ckpt_ms = best_of(bwd_ckpt)
     return {"ms": best, "elements_per_s": w.elements / (best * 1e-3),
             "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (best * 1e-3) / 1e9,
             "kernel_launches": 6 if w.L > 32 else 3,
+            "with_forward_checkpoints": {
+                "backward_ms": bwd_ckpt_ms, "forward_ms": fwd_ckpt_ms,
+                "checkpoint_bytes": ckpt.numel() * 4, "kernel_launches": 4 if w.L > 32 else 3,
+                "note": "ssm_scan_bwd_ckpt reading the unit states that ssm_scan_fwd_ckpt "
+                        "wrote (no summary pass of its own); forward_ms is that forward "
+                        "pass, y and h_last as ssm_scan_fwd plus the states"},
             "note": "one ssm_scan_bwd call: forward unit summaries + carry (state checkpoints "
                     "every 32 steps), adjoint summaries + carry, the unit kernel, the dB/dC "
                     "reduction; best of %d" % reps}

@@ -194,6 +194,38 @@ SSM_API int ssm_scan_bwd(const void *u, const void *delta, const float *dt_bias,
                          void *stream);
 
 /*
+ * ssm_scan_fwd_ckpt / ssm_scan_bwd_ckpt -- the forward and backward passes of
+ * a training step, sharing the states at the 32-step unit boundaries: the
+ * forward pass writes them as it walks the sequence, and the backward pass
+ * reads them instead of recomputing them in a pass of its own (the
+ * backward's other phases, and its arithmetic, are those of ssm_scan_bwd).
+ * This pairing is the library's; the pages say only that the fused kernel
+ * recomputes the states rather than storing them all.
+ *
+ *   ckpt : [ceil(L / 32), batch, D, 16] float32, 16-byte aligned.  Entry k
+ *          (k >= 1) is the state entering step 32 k; entry 0 (the zero state)
+ *          is neither written nor read.  May be NULL when L <= 32.
+ * ssm_scan_fwd_ckpt takes ssm_scan_fwd's arguments (zero-order hold, y and
+ * h_last as there) and writes ckpt.  ssm_scan_bwd_ckpt takes ssm_scan_bwd's
+ * arguments and ckpt, which must come from ssm_scan_fwd_ckpt with the same
+ * inputs (nothing checks that); it needs no workspace for the states.  Both
+ * run the N == 16 kernels only: N != 16, or a tensor or row that those
+ * kernels cannot take (see ssm_scan_fwd and ssm_scan_bwd), returns
+ * SSM_ERR_UNSUPPORTED before anything is enqueued.  Returns an ssm_status_t.
+ */
+SSM_API int ssm_scan_fwd_ckpt(const void *u, const void *delta, const float *dt_bias,
+                              const float *A, const void *B, const void *C, const float *Dskip,
+                              const void *z, void *y, float *h_last, float *ckpt, int64_t batch,
+                              int64_t L, int64_t D, int64_t N, int dtype, void *stream);
+SSM_API int ssm_scan_bwd_ckpt(const void *u, const void *delta, const float *dt_bias,
+                              const float *A, const void *B, const void *C, const float *Dskip,
+                              const void *z, const void *dy, const float *dh_last,
+                              const float *ckpt, void *du, void *ddelta, float *ddt_bias,
+                              float *dA, float *dB, float *dC, float *dDskip, void *dz,
+                              int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
+                              void *stream);
+
+/*
  * ssm_ssd_fwd -- the Mamba-2 form of the scan (structured state-space
  * duality; news.han.ihouse.idv.tw article 1304: most of the SSM computation is
  * a masked matrix multiplication, A is a scalar, Euler discretisation):

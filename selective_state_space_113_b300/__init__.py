@@ -10,12 +10,12 @@ library raises ImportError (there is no CPU fallback).
 """
 from __future__ import annotations
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd", "ssm_ssd_fwd", "ssm_scan_fwd_noalloc", "ssm_step", "ssm_device_status", "ssm_status_string",
+__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd", "ssm_scan_fwd_ckpt", "ssm_scan_bwd_ckpt", "ssm_ssd_fwd", "ssm_scan_fwd_noalloc", "ssm_step", "ssm_device_status", "ssm_status_string",
            "ssm_abi_version", "ssm_unit_ceilings", "SsmError", "scan", "step"]
 
 
 def __getattr__(name):
-    if name in ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd", "ssm_ssd_fwd", "SSM_DISC_ZOH", "SSM_DISC_EULER",
+    if name in ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd", "ssm_scan_fwd_ckpt", "ssm_scan_bwd_ckpt", "ssm_ssd_fwd", "SSM_DISC_ZOH", "SSM_DISC_EULER",
                 "SSM_DISC_TRAPEZOID", "ssm_scan_fwd_noalloc", "ssm_step", "ssm_device_status", "ssm_status_string",
                 "ssm_abi_version", "ssm_unit_ceilings", "SsmError", "lib", "LIB_PATH"):
         from . import _native

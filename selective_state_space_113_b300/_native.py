@@ -21,6 +21,7 @@ STATUS = {0: "SSM_OK", -1: "SSM_ERR_NULL", -2: "SSM_ERR_SIZE", -3: "SSM_ERR_DTYP
           -4: "SSM_ERR_ALIGN", -5: "SSM_ERR_UNSUPPORTED", -6: "SSM_ERR_CUDA",
           -7: "SSM_ERR_NOMEM", -8: "SSM_ERR_TIMEOUT", -9: "SSM_ERR_SCRATCH"}
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_fwd_disc", "ssm_conv_scan_fwd", "ssm_scan_bwd",
+           "ssm_scan_fwd_ckpt", "ssm_scan_bwd_ckpt",
            "ssm_ssd_fwd", "ssm_scan_fwd_noalloc", "ssm_step",
            "ssm_device_status", "ssm_status_string", "ssm_abi_version", "ssm_unit_ceilings")
 SSM_DISC_ZOH, SSM_DISC_EULER, SSM_DISC_TRAPEZOID = 0, 1, 2
@@ -46,6 +47,10 @@ def _load() -> ctypes.CDLL:
     lib.ssm_conv_scan_fwd.argtypes = [vp] * 3 + [ci] + [vp] * 9 + [i64] * 4 + [ci, vp]
     lib.ssm_scan_bwd.restype = ci
     lib.ssm_scan_bwd.argtypes = [vp] * 18 + [i64] * 4 + [ci, vp]
+    lib.ssm_scan_fwd_ckpt.restype = ci
+    lib.ssm_scan_fwd_ckpt.argtypes = [vp] * 11 + [i64] * 4 + [ci, vp]
+    lib.ssm_scan_bwd_ckpt.restype = ci
+    lib.ssm_scan_bwd_ckpt.argtypes = [vp] * 19 + [i64] * 4 + [ci, vp]
     lib.ssm_ssd_fwd.restype = ci
     lib.ssm_ssd_fwd.argtypes = [vp] * 9 + [i64] * 5 + [ci, vp]
     lib.ssm_scan_fwd_noalloc.restype = ci
@@ -145,6 +150,28 @@ def ssm_scan_bwd(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last, du, ddelta, 
                             _p(dy), _p(dh_last), _p(du), _p(ddelta), _p(ddt_bias), _p(dA), _p(dB),
                             _p(dC), _p(dDskip), _p(dz), batch, L, D, N, _dtype_code(u),
                             _stream(stream)), "ssm_scan_bwd")
+
+
+def ssm_scan_fwd_ckpt(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, ckpt, stream=None) -> None:
+    """ssm_scan_fwd that also writes ckpt [ceil(L/32), batch, D, 16] float32:
+    the state entering every 32-step unit, for ssm_scan_bwd_ckpt."""
+    batch, L, D = u.shape
+    N = A.shape[-1]
+    _check(lib.ssm_scan_fwd_ckpt(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip),
+                                 _p(z), _p(y), _p(h_last), _p(ckpt), batch, L, D, N,
+                                 _dtype_code(u), _stream(stream)), "ssm_scan_fwd_ckpt")
+
+
+def ssm_scan_bwd_ckpt(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last, ckpt, du, ddelta,
+                      ddt_bias, dA, dB, dC, dDskip, dz, stream=None) -> None:
+    """ssm_scan_bwd reading the unit states from ckpt (ssm_scan_fwd_ckpt's,
+    same inputs) instead of recomputing them."""
+    batch, L, D = u.shape
+    N = A.shape[-1]
+    _check(lib.ssm_scan_bwd_ckpt(_p(u), _p(delta), _p(dt_bias), _p(A), _p(B), _p(C), _p(Dskip),
+                                 _p(z), _p(dy), _p(dh_last), _p(ckpt), _p(du), _p(ddelta),
+                                 _p(ddt_bias), _p(dA), _p(dB), _p(dC), _p(dDskip), _p(dz), batch,
+                                 L, D, N, _dtype_code(u), _stream(stream)), "ssm_scan_bwd_ckpt")
 
 
 def ssm_ssd_fwd(x, dt, dt_bias, A, B, C, Dskip, y, h_last, stream=None) -> None:

@@ -72,7 +72,8 @@ struct ConvArgs {
 int scan_impl(const void* u, const void* delta, const float* dt_bias, const float* A,
               const void* B, const void* C, const float* Dskip, const void* z, void* y,
               float* h_last, int64_t batch, int64_t L, int64_t D, int64_t N, int dtype,
-              int disc, void* stream_, ConvArgs conv = {nullptr, nullptr, 0}) {
+              int disc, void* stream_, ConvArgs conv = {nullptr, nullptr, 0},
+              float* ckpt = nullptr, bool want_ckpt = false) {
     if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
@@ -90,6 +91,16 @@ int scan_impl(const void* u, const void* delta, const float* dt_bias, const floa
     if (!elems_aligned(dtype, {u, delta, B, C, z, y},
                        {dt_bias, A, Dskip, h_last, conv.w, conv.b}))
         return SSM_ERR_ALIGN;
+    const int plan = ssm::tile::forced_plan();
+    const bool fast = N == ssm::tile::NS && plan != ssm::tile::kPlanGeneric &&
+                      all_aligned16({u, delta, z, B, C, y, h_last, A, conv.w}) &&
+                      (D * (int64_t)elem_size(dtype)) % 16 == 0;
+    if (want_ckpt) {
+        // checkpoints come from the N == 16 kernel only (the backward's fast path)
+        if (bd && L > 32 && !ckpt) return SSM_ERR_NULL;
+        if (!all_aligned16({ckpt})) return SSM_ERR_ALIGN;
+        if (bd && L > 0 && !fast) return SSM_ERR_UNSUPPORTED;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (bd == 0) return SSM_OK;
     if (L == 0) {
@@ -98,10 +109,7 @@ int scan_impl(const void* u, const void* delta, const float* dt_bias, const floa
         return SSM_OK;
     }
     // Fast path: N == 16, 16-byte-aligned tensors and rows (TMA tiles).
-    const int plan = ssm::tile::forced_plan();
-    if (N == ssm::tile::NS && plan != ssm::tile::kPlanGeneric &&
-        all_aligned16({u, delta, z, B, C, y, h_last, A, conv.w}) &&
-        (D * (int64_t)elem_size(dtype)) % 16 == 0) {
+    if (fast) {
         using namespace ssm::tile;
         if (conv.w) {
             if (dtype == SSM_F32)
@@ -120,7 +128,7 @@ int scan_impl(const void* u, const void* delta, const float* dt_bias, const floa
     launch_scan_tile<TT, DISC>(static_cast<const TT*>(u), static_cast<const TT*>(delta), dt_bias, \
                                A, static_cast<const TT*>(B), static_cast<const TT*>(C), Dskip,   \
                                static_cast<const TT*>(z), static_cast<TT*>(y), h_last, batch, L, \
-                               D, plan, stream)
+                               D, plan, stream, nullptr, nullptr, 0, ckpt)
         if (dtype == SSM_F32) {
             if (disc == SSM_DISC_EULER) return SSM_TILE_CALL(float, kEuler);
             if (disc == SSM_DISC_TRAPEZOID) return SSM_TILE_CALL(float, kTrap);
@@ -159,6 +167,16 @@ extern "C" int ssm_scan_fwd(const void* u, const void* delta, const float* dt_bi
                      SSM_DISC_ZOH, stream_);
 }
 
+extern "C" int ssm_scan_fwd_ckpt(const void* u, const void* delta, const float* dt_bias,
+                                 const float* A, const void* B, const void* C,
+                                 const float* Dskip, const void* z, void* y, float* h_last,
+                                 float* ckpt, int64_t batch, int64_t L, int64_t D, int64_t N,
+                                 int dtype, void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_scan_fwd_ckpt");
+    return scan_impl(u, delta, dt_bias, A, B, C, Dskip, z, y, h_last, batch, L, D, N, dtype,
+                     SSM_DISC_ZOH, stream_, {nullptr, nullptr, 0}, ckpt, true);
+}
+
 extern "C" int ssm_scan_fwd_disc(const void* u, const void* delta, const float* dt_bias,
                                  const float* A, const void* B, const void* C,
                                  const float* Dskip, const void* z, void* y, float* h_last,
@@ -181,13 +199,12 @@ extern "C" int ssm_conv_scan_fwd(const void* x, const float* conv_w, const float
                      SSM_DISC_ZOH, stream_, ConvArgs{D > 0 ? conv_w : nullptr, conv_b, act});
 }
 
-extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bias,
-                            const float* A, const void* B, const void* C, const float* Dskip,
-                            const void* z, const void* dy, const float* dh_last, void* du,
-                            void* ddelta, float* ddt_bias, float* dA, float* dB, float* dC,
-                            float* dDskip, void* dz, int64_t batch, int64_t L, int64_t D,
-                            int64_t N, int dtype, void* stream_) {
-    const ssm::fault::Range nvtx_range("ssm_scan_bwd");
+namespace {
+int bwd_impl(const void* u, const void* delta, const float* dt_bias, const float* A, const void* B,
+             const void* C, const float* Dskip, const void* z, const void* dy,
+             const float* dh_last, const float* ckpt, bool want_ckpt, void* du, void* ddelta,
+             float* ddt_bias, float* dA, float* dB, float* dC, float* dDskip, void* dz,
+             int64_t batch, int64_t L, int64_t D, int64_t N, int dtype, void* stream_) {
     if (batch < 0 || L < 0 || D < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
@@ -202,6 +219,16 @@ extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bi
     if (!elems_aligned(dtype, {u, delta, B, C, z, dy, du, ddelta, dz},
                        {dt_bias, A, Dskip, dh_last, ddt_bias, dA, dB, dC, dDskip}))
         return SSM_ERR_ALIGN;
+    const int plan = ssm::tile::forced_plan();
+    const bool fast = N == ssm::bwd::NS && plan != ssm::tile::kPlanGeneric &&
+                      all_aligned16({u, delta, z, dy, B, C, A, du}) &&
+                      (D * (int64_t)elem_size(dtype)) % 16 == 0;
+    if (want_ckpt) {
+        // the forward pass's checkpoints serve the N == 16 kernels only
+        if (bd && L > 32 && !ckpt) return SSM_ERR_NULL;
+        if (!all_aligned16({ckpt})) return SSM_ERR_ALIGN;
+        if (bd && L > 0 && !fast) return SSM_ERR_UNSUPPORTED;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     // Sums start from zero: with no step or no channel they stay zero.
     if (dn && cudaMemsetAsync(dA, 0, sizeof(float) * dn, stream) != cudaSuccess) return SSM_ERR_CUDA;
@@ -214,22 +241,20 @@ extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bi
     if (bln && dC && cudaMemsetAsync(dC, 0, sizeof(float) * bln, stream) != cudaSuccess)
         return SSM_ERR_CUDA;
     if (bd == 0 || L == 0) return SSM_OK;
-    const int plan = ssm::tile::forced_plan();
-    if (N == ssm::bwd::NS && plan != ssm::tile::kPlanGeneric &&
-        all_aligned16({u, delta, z, dy, B, C, A, du}) && (D * (int64_t)elem_size(dtype)) % 16 == 0) {
+    if (fast) {
         if (dtype == SSM_F32)
             return ssm::bwd::launch_scan_bwd16<float>(
                 static_cast<const float*>(u), static_cast<const float*>(delta), dt_bias, A,
                 static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
                 static_cast<const float*>(z), static_cast<const float*>(dy), dh_last,
                 static_cast<float*>(du), static_cast<float*>(ddelta), ddt_bias, dA, dB, dC,
-                dDskip, static_cast<float*>(dz), batch, L, D, stream);
+                dDskip, static_cast<float*>(dz), batch, L, D, stream, ckpt);
         return ssm::bwd::launch_scan_bwd16<bf16>(
             static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
             static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
             static_cast<const bf16*>(z), static_cast<const bf16*>(dy), dh_last,
             static_cast<bf16*>(du), static_cast<bf16*>(ddelta), ddt_bias, dA, dB, dC, dDskip,
-            static_cast<bf16*>(dz), batch, L, D, stream);
+            static_cast<bf16*>(dz), batch, L, D, stream, ckpt);
     }
     float* scratch = nullptr;
     const size_t bytes = sizeof(float) * ssm::bwdg::bwd_generic_scratch_floats(batch, L, D, N);
@@ -254,6 +279,30 @@ extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bi
             static_cast<bf16*>(dz), scratch, batch, L, D, (int)N, stream);
     const cudaError_t ef = cudaFreeAsync(scratch, stream);
     return from_cuda(e != cudaSuccess ? e : ef);
+}
+}  // namespace
+
+extern "C" int ssm_scan_bwd(const void* u, const void* delta, const float* dt_bias,
+                            const float* A, const void* B, const void* C, const float* Dskip,
+                            const void* z, const void* dy, const float* dh_last, void* du,
+                            void* ddelta, float* ddt_bias, float* dA, float* dB, float* dC,
+                            float* dDskip, void* dz, int64_t batch, int64_t L, int64_t D,
+                            int64_t N, int dtype, void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_scan_bwd");
+    return bwd_impl(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last, nullptr, false, du, ddelta,
+                    ddt_bias, dA, dB, dC, dDskip, dz, batch, L, D, N, dtype, stream_);
+}
+
+extern "C" int ssm_scan_bwd_ckpt(const void* u, const void* delta, const float* dt_bias,
+                                 const float* A, const void* B, const void* C,
+                                 const float* Dskip, const void* z, const void* dy,
+                                 const float* dh_last, const float* ckpt, void* du, void* ddelta,
+                                 float* ddt_bias, float* dA, float* dB, float* dC, float* dDskip,
+                                 void* dz, int64_t batch, int64_t L, int64_t D, int64_t N,
+                                 int dtype, void* stream_) {
+    const ssm::fault::Range nvtx_range("ssm_scan_bwd_ckpt");
+    return bwd_impl(u, delta, dt_bias, A, B, C, Dskip, z, dy, dh_last, ckpt, true, du, ddelta,
+                    ddt_bias, dA, dB, dC, dDskip, dz, batch, L, D, N, dtype, stream_);
 }
 
 extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float* A,

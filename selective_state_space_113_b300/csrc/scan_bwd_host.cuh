@@ -62,8 +62,9 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
                       const T* Bm, const T* Cm, const float* Dskip, const T* z, const T* dy,
                       const float* dh_last, T* du, T* ddelta, float* ddt_bias, float* dA,
                       float* dB, float* dC, float* dDskip, T* dz, long long batch, long long L,
-                      long long D, cudaStream_t stream) {
+                      long long D, cudaStream_t stream, const float* ckpt = nullptr) {
     using namespace tile;
+    static_assert(TU == kCkptSteps, "checkpoint interval");
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -82,10 +83,12 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
     const long long nCB = cdiv(D, CB);
     const size_t head = header_bytes(batch, D);
     size_t off = head;
+    // with checkpoints from the forward pass, no unit summaries and no
+    // states of our own
     const size_t off_agg = off;
-    off = round256(off + (size_t)(P > 1 ? P - 1 : 0) * nch * (NS + 1) * 4);
+    if (!ckpt) off = round256(off + (size_t)(P > 1 ? P - 1 : 0) * nch * (NS + 1) * 4);
     const size_t off_hin = off;
-    off = round256(off + (size_t)P * nch * NS * 4);
+    if (!ckpt) off = round256(off + (size_t)P * nch * NS * 4);
     const size_t off_adj = off;
     off = round256(off + (size_t)P * nch * (NS + 1) * 4);
     const size_t off_mu = off;
@@ -107,9 +110,10 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
             status = SSM_ERR_CUDA;
             break;
         }
-        float* hin = reinterpret_cast<float*>(ws + off_hin);
-        // 1. the states entering every unit (unit 0 starts from zero)
-        if (P > 1) {
+        const float* hin = ckpt ? ckpt : reinterpret_cast<const float*>(ws + off_hin);
+        // 1. the states entering every unit (unit 0 starts from zero), unless
+        // the forward pass left them
+        if (P > 1 && !ckpt) {
             CUtensorMap maps[6];
             Params p;
             if (!setup<T>(maps, &p, u, delta, dt_bias, A, Bm, Cm, Dskip, z, du, nullptr, batch,
@@ -133,7 +137,8 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
                 status = SSM_ERR_CUDA;
                 break;
             }
-            carry_kernel<<<(unsigned)cdiv(nch * NS, 256), 256, 0, stream>>>(p.agg, A, hin, batch, D, P);
+            carry_kernel<<<(unsigned)cdiv(nch * NS, 256), 256, 0, stream>>>(
+                p.agg, A, reinterpret_cast<float*>(ws + off_hin), batch, D, P);
             if (cudaGetLastError() != cudaSuccess) {
                 status = SSM_ERR_CUDA;
                 break;

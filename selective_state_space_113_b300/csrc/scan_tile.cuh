@@ -108,6 +108,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 enum Mode : int { kChained = 0, kAggregate = 1, kFromState = 2 };
 
+// Steps per unit of the optional state checkpoints (the backward pass's unit).
+constexpr long long kCkptSteps = 32;
+
 enum Disc : int { kZOH = 0, kEuler = 1, kTrap = 2 };
 
 // Stage flags: first / last stage of a piece, end of work, carried state
@@ -158,6 +161,8 @@ struct Params {
     float* carry;           // [batch, D, NS] chained state (h_last or scratch)
     float* agg;             // [P][batch*D][NS+1] phase-1 summaries (kAggregate)
     const float* hin;       // [P][batch*D][NS] phase-3 initial states (kFromState)
+    float* ckpt;            // NULL, or [ceil(L/32)][batch*D][NS]: the state entering each
+                            // 32-step unit (entry 0, the zero state, not written)
     unsigned long long wait_ns;
 };
 
@@ -890,6 +895,17 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[slot]);
+        // the state entering the next 32-step unit, for a later backward pass
+        if (MODE != kAggregate && p.ckpt) {
+            const long long tend = m.t0 + m.nvalid;
+            if (tend % kCkptSteps == 0 && tend < p.L && valid) {
+                float4* dst = reinterpret_cast<float4*>(
+                    p.ckpt + ((tend / kCkptSteps) * p.batch * p.D + b * p.D + d) * NS);
+#pragma unroll
+                for (int i = 0; i < NS / 4; ++i)
+                    __stcg(dst + i, make_float4(H[2 * i].x, H[2 * i].y, H[2 * i + 1].x, H[2 * i + 1].y));
+            }
+        }
         if (m.flags & kLast) {
             if (MODE == kChained) {
                 if (!(m.flags & kChainEnd)) {

@@ -162,7 +162,7 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
                      const T* Bm, const T* Cm, const float* Dskip, const T* z, T* y,
                      float* h_last, long long batch, long long L, long long D, int plan,
                      cudaStream_t stream, const float* conv_w = nullptr,
-                     const float* conv_b = nullptr, int act = 0) {
+                     const float* conv_b = nullptr, int act = 0, float* ckpt = nullptr) {
     constexpr long long TC = Cfg<T>::TC;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -182,6 +182,7 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
     p.conv_w = conv_w;
     p.conv_b = conv_b;
     p.act = act;
+    p.ckpt = ckpt;
 
     bool narrow = false;
     if (plan == kPlanNarrow) narrow = true;

@@ -52,6 +52,13 @@ int main(void) {
     expect(ssm_scan_bwd(FAKE, FAKE, NULL, FAKEF, FAKE, FAKE, NULL, NULL, NULL, NULL, FAKE, FAKE,
                         NULL, FAKEF, NULL, NULL, NULL, NULL, 1, 4, 8, 16, SSM_BF16, NULL),
            SSM_ERR_NULL, "backward, dy NULL");
+    expect(ssm_scan_fwd_ckpt(FAKE, FAKE, NULL, FAKEF, FAKE, FAKE, NULL, NULL, FAKE, NULL, NULL, 1,
+                             64, 8, 16, SSM_BF16, NULL),
+           SSM_ERR_NULL, "forward with checkpoints, checkpoints NULL");
+    expect(ssm_scan_bwd_ckpt(FAKE, FAKE, NULL, FAKEF, FAKE, FAKE, NULL, NULL, FAKE, NULL, FAKEF,
+                             FAKE, FAKE, NULL, FAKEF, NULL, NULL, NULL, NULL, 1, 64, 8, 7,
+                             SSM_BF16, NULL),
+           SSM_ERR_UNSUPPORTED, "backward with checkpoints, N = 7");
     expect(ssm_ssd_fwd(FAKE, FAKE, NULL, FAKEF, FAKE, FAKE, NULL, FAKE, NULL, 0, 4, 2, 0, 64,
                        SSM_BF16, NULL),
            SSM_ERR_SIZE, "SSD, P = 0");

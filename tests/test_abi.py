@@ -154,6 +154,39 @@ def test_bwd_argument_validation(lib):
     assert bwd(lib, dh_last=FAKE + 2) == -4
 
 
+def ckpt_fwd(lib, batch=1, L=64, D=8, N=16, dtype=1, **kw):
+    a = dict(u=FAKE, delta=FAKE, dt_bias=None, A=FAKE, B=FAKE, C=FAKE, Dskip=None, z=None, y=FAKE,
+             h_last=None, ckpt=FAKE)
+    a.update(kw)
+    return lib.ssm_scan_fwd_ckpt(a["u"], a["delta"], a["dt_bias"], a["A"], a["B"], a["C"],
+                                 a["Dskip"], a["z"], a["y"], a["h_last"], a["ckpt"], batch, L, D, N,
+                                 dtype, None)
+
+
+def ckpt_bwd(lib, batch=1, L=64, D=8, N=16, dtype=1, **kw):
+    a = dict(u=FAKE, delta=FAKE, dt_bias=None, A=FAKE, B=FAKE, C=FAKE, Dskip=None, z=None, dy=FAKE,
+             dh_last=None, ckpt=FAKE, du=FAKE, ddelta=FAKE, ddt_bias=None, dA=FAKE, dB=None,
+             dC=None, dDskip=None, dz=None)
+    a.update(kw)
+    return lib.ssm_scan_bwd_ckpt(a["u"], a["delta"], a["dt_bias"], a["A"], a["B"], a["C"],
+                                 a["Dskip"], a["z"], a["dy"], a["dh_last"], a["ckpt"], a["du"],
+                                 a["ddelta"], a["ddt_bias"], a["dA"], a["dB"], a["dC"],
+                                 a["dDskip"], a["dz"], batch, L, D, N, dtype, None)
+
+
+def test_checkpoint_argument_validation(lib):
+    """The checkpoint pair's rejections, all before anything is enqueued:
+    checkpoints needed (L > 32) but NULL, misaligned, or a shape that the
+    N == 16 kernels do not take; no channels is a no-op."""
+    for fn in (ckpt_fwd, ckpt_bwd):
+        assert fn(lib, ckpt=None) == -1, fn.__name__
+        assert fn(lib, ckpt=FAKE + 4) == -4, fn.__name__
+        assert fn(lib, N=7) == -5, fn.__name__
+        assert fn(lib, D=4) == -5, fn.__name__              # a bf16 row of 8 bytes
+        assert fn(lib, u=None) == -1, fn.__name__
+    assert ckpt_fwd(lib, batch=0) == 0
+
+
 def ssd(lib, batch=0, L=4, H=2, P=64, N=64, dtype=1, **kw):
     a = dict(x=FAKE, dt=FAKE, dt_bias=None, A=FAKE, B=FAKE, C=FAKE, Dskip=None, y=FAKE,
              h_last=None)

@@ -207,3 +207,81 @@ def test_bwd_mamba2p8b_sampled_and_identities():
     scale_b = (out["dB"].double() * inp["B"].double()).abs().sum((1, 2)) + dyy.abs().sum((1, 2)) \
         + (f["dh_last"].double() * hl.double()).abs().sum((1, 2))
     assert bool(((dbb - rhs_b).abs() <= 3e-6 * scale_b).all()), (dbb, rhs_b, scale_b)
+
+
+def run_ckpt(inp, plan=None, monkeypatch=None):
+    """ssm_scan_fwd_ckpt then ssm_scan_bwd_ckpt; returns (y, h_last, outputs)."""
+    u = inp["u"]
+    batch, L, D = u.shape
+    N = inp["A"].shape[1]
+    ckpt = torch.full(((L + 31) // 32, batch, D, N), float("nan"), device=DEV)
+    y = torch.empty_like(u)
+    h = torch.empty((batch, D, N), device=DEV)
+    ssm.ssm_scan_fwd_ckpt(u, inp["delta"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                          inp["Dskip"], inp["z"], y, h, ckpt)
+    out = {
+        "du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+        "dz": torch.empty_like(u) if inp["z"] is not None else None,
+        "dB": torch.empty((batch, L, N), device=DEV), "dC": torch.empty((batch, L, N), device=DEV),
+        "dA": torch.empty((D, N), device=DEV), "ddt_bias": torch.empty(D, device=DEV),
+        "dDskip": torch.empty(D, device=DEV),
+    }
+    ssm.ssm_scan_bwd_ckpt(u, inp["delta"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                          inp["Dskip"], inp["z"], inp["dy"], inp["dh_last"], ckpt, out["du"],
+                          out["ddelta"], out["ddt_bias"], out["dA"], out["dB"], out["dC"],
+                          out["dDskip"], out["dz"])
+    torch.cuda.synchronize()
+    assert ssm.ssm_device_status() == 0
+    return y, h, ckpt, out
+
+
+CKPT_SHAPES = [  # (batch, L, D, dtype, plan)
+    (2, 100, 96, torch.bfloat16, None),       # ragged last unit
+    (1, 300, 256, torch.float32, None),       # 16-step stages: every other one writes
+    (2, 1000, 128, torch.bfloat16, "narrow"), # the narrow plan's output pass writes them
+    (2, 31, 32, torch.bfloat16, None),        # one unit: nothing to write
+    (3, 64, 40, torch.bfloat16, None),        # a ragged channel block, L a multiple of 32
+]
+
+
+@pytest.mark.parametrize("shape", CKPT_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}x{s[2]}_{s[3]}_{s[4]}")
+def test_bwd_with_forward_checkpoints(monkeypatch, shape):
+    """The forward pass that writes the unit states gives y and h_last
+    bit-identical to ssm_scan_fwd; its checkpoints equal the oracle's states
+    at the unit boundaries; the backward that reads them matches the oracle
+    and ssm_scan_bwd."""
+    batch, L, D, dtype, plan = shape
+    if plan:
+        monkeypatch.setenv("SSM_FORCE_PLAN", plan)
+    inp = inputs(batch, L, D, 16, dtype, 60 + L)
+    y, h, ckpt, out = run_ckpt(inp)
+    y_ref, h_ref = ssm.scan(inp["u"], inp["delta"], inp["dt_bias"], inp["A"], inp["B"], inp["C"],
+                            inp["Dskip"], inp["z"])
+    assert torch.equal(y, y_ref) and torch.equal(h, h_ref)
+    tol = parity.TOL[dtype]
+    # the states at the unit boundaries, from the oracle's scan of the first 32 k steps
+    for k in range(1, (L + 31) // 32):
+        sub = {n: (t[:, :32 * k] if t is not None and t.dim() == 3 and n in ("u", "delta", "z", "B", "C")
+                   else t) for n, t in inp.items()}
+        _, hk = parity.oracle_scan(sub)
+        parity.check(parity.to_f64(ckpt[k]), hk, tol, f"checkpoint {k}")
+        if k >= 3:
+            break
+    ref = oracle_bwd(inp)
+    compare(out, ref, 1e-4 if dtype == torch.float32 else 2e-2, f"ckpt {shape}")
+    plain = run_bwd(inp)
+    for k in OUTS:
+        if out[k] is not None:
+            parity.check(parity.to_f64(out[k]), parity.to_f64(plain[k]),
+                         2e-5 if dtype == torch.float32 else 1e-2, f"ckpt vs ssm_scan_bwd {k}")
+
+
+def test_checkpoints_refuse_other_state_sizes():
+    """N != 16 has no unit kernels: both calls refuse before any work."""
+    inp = inputs(1, 64, 32, 8, torch.float32, 3)
+    ckpt = torch.empty((2, 1, 32, 8), device=DEV)
+    y, h = torch.empty_like(inp["u"]), torch.empty((1, 32, 8), device=DEV)
+    with pytest.raises(ssm.SsmError) as e:
+        ssm.ssm_scan_fwd_ckpt(inp["u"], inp["delta"], inp["dt_bias"], inp["A"], inp["B"],
+                              inp["C"], inp["Dskip"], inp["z"], y, h, ckpt)
+    assert e.value.status == -5
