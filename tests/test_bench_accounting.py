@@ -32,10 +32,14 @@ def test_decode_algorithmic_bytes():
 
 
 def test_scan_fma_count():
-    # per state and step: the exponential recurrence, the two multiply-adds of
-    # the update and the readout
+    # the kernel, per state and step: the exponential recurrence, the two
+    # multiply-adds of the update and the readout
     assert bench.FMA_PER_ELEMENT_N16 == 4 * 16
     assert 2 * bench.FMA_PER_ELEMENT_N16 * wl.MAMBA_2P8B.elements == 10_737_418_240
+    # the method as written (the ALU roofline): the input term, the update and
+    # the readout, the exponentials counted on the special-function unit
+    assert bench.FMA_PER_ELEMENT_METHOD == 3 * 16
+    assert bench.SFU_PER_ELEMENT_AS_WRITTEN == 16 + 2 + 2
 
 
 def test_launches_per_call_matches_the_plan_choice():
