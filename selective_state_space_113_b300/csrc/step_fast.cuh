@@ -167,7 +167,13 @@ static cudaError_t launch_step16(float* state, const T* u, const T* delta, const
 // G groups of TC compute threads take the ring's tiles in turn; a thread owns
 // one channel, walks the tile's NB batch entries and keeps A and 1/A of its
 // channel in registers (tiles are ordered channel block first, so a CTA meets
-// few channel blocks).  The new state goes back into the tile in place, each
+// few channel blocks).  STAGES is a multiple of G, so every stage has one
+// group as its only reader.  The wait on a stage's full barrier names the
+// phase by its parity, which only identifies the phase if the previous one
+// has completed; the group that waits for round j of a stage is the one that
+// waited for round j - 1, so that holds.  With readers alternating between
+// groups, a group could meet a stage whose previous copy had not landed and
+// pass its wait at once, reading the old tile and freeing the stage early.  The new state goes back into the tile in place, each
 // warp re-reads its 32 rows linearly and stores them to global memory in
 // 512-byte coalesced pieces; y is stored directly.  Tensor copies read
 // out-of-range rows (channels past D, entries past batch) as zeros; nothing
@@ -181,8 +187,14 @@ static cudaError_t launch_step16(float* state, const T* u, const T* delta, const
 // and the readout adds C h, D u and the SiLU gate as the kernel above does.
 constexpr int kTileTC = 128;   // channels per tile
 constexpr int kTileNB = 4;     // batch entries per tile
-constexpr int kTileStages = 5;
-constexpr int kTileGroups = 3;
+
+// Ring depth and compute groups per element type: six bf16 stages (216 KB) or
+// four float32 stages (156 KB) fit in shared memory.
+template <typename T>
+struct TileRing {
+    static constexpr int kStages = sizeof(T) == 2 ? 6 : 4;
+    static constexpr int kGroups = sizeof(T) == 2 ? 3 : 2;
+};
 
 struct StepMaps {
     CUtensorMap state, u, delta, z, B, C;
@@ -231,6 +243,7 @@ step16_tiled_kernel(const __grid_constant__ StepMaps maps, float* __restrict__ s
                     const float* __restrict__ Dskip, int has_z, T* __restrict__ y, int batch,
                     int D, int tiles, unsigned long long wait_ns) {
     using L = TileLayout<T, TC, NB>;
+    static_assert(STAGES % G == 0, "each stage needs a single reading group");
     constexpr int kCompute = G * TC;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (ptx::smem_u32(smem_raw) & 1023)) & 1023);
@@ -388,9 +401,10 @@ static cudaError_t launch_step16_tiled(float* state, const T* u, const T* delta,
                                        const T* Cm, const float* Dskip, const T* z, T* y,
                                        long long batch, long long D, unsigned long long wait_ns,
                                        cudaStream_t stream) {
-    constexpr int TC = kTileTC, NB = kTileNB, S = kTileStages, G = kTileGroups;
+    constexpr int TC = kTileTC, NB = kTileNB, S = TileRing<T>::kStages, G = TileRing<T>::kGroups;
     auto kern = step16_tiled_kernel<T, TC, NB, S, G>;
     constexpr int smem = tile_smem_bytes<T, TC, NB, S>();
+    static_assert(smem <= 227 * 1024, "ring exceeds a CTA's shared memory");
     const CUtensorMapDataType dt =
         sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const cuuint64_t es = sizeof(T);

@@ -82,6 +82,50 @@ def test_decode_full_size_tiled_matches_one_pass(monkeypatch):
     parity.check(parity.to_f64(y), parity.to_f64(y_ref), 8e-3, "tiled vs one-pass y")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_full_size_tiled_repeatable(dtype):
+    """The tiled kernel's result does not depend on timing: the 256 x 5120
+    decode, 64 steps, gives bit-identical states and outputs as plain
+    launches, with L2 flushed before every step (copies landing out of
+    order), and replayed as one CUDA graph.  A ring whose stages were read by
+    alternating groups failed this, a group passing its wait on a stage whose
+    previous copy had not landed."""
+    w = wl.DECODE if dtype == torch.bfloat16 else wl.StepWorkload(
+        "decode f32", wl.DECODE.batch, wl.DECODE.D, 16, wl.DECODE.steps, torch.float32, 41)
+    inp = wl.make_step_inputs(w, device=DEV)
+    state = inp["state"].clone()
+    ys = torch.empty((w.steps, w.batch, w.D), device=DEV, dtype=w.dtype)
+    flush = torch.empty(64 << 20, device=DEV, dtype=torch.float32)
+
+    def run(flushed=False):
+        for s in range(w.steps):
+            if flushed:
+                flush.zero_()
+            ssm.ssm_step(state, inp["u"][s], inp["delta"][s], inp["dt_bias"], inp["A"],
+                         inp["B"][s], inp["C"][s], inp["Dskip"], inp["z"][s], ys[s])
+
+    results = []
+    for flushed in (False, False, True, True):
+        state.copy_(inp["state"])
+        run(flushed)
+        torch.cuda.synchronize()
+        results.append((state.clone(), ys.clone()))
+    state.copy_(inp["state"])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        state.copy_(inp["state"])
+        g.replay()
+        torch.cuda.synchronize()
+        results.append((state.clone(), ys.clone()))
+    assert ssm.ssm_device_status() == 0
+    st0, y0 = results[0]
+    for i, (st, y) in enumerate(results[1:], 1):
+        assert torch.equal(st, st0), f"run {i}: state differs"
+        assert torch.equal(y, y0), f"run {i}: y differs"
+
+
 @pytest.mark.parametrize("N", [1, 5, 16, 32, 256])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_step_small_full(N, dtype):
