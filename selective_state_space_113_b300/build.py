@@ -80,13 +80,16 @@ def build(out: str = LIB, extra=(), verbose: bool = False, force: bool = False) 
     if not force and not extra and up_to_date(out):
         return out
     cmd = command(out, extra)
+    # the sources as compiled: hashed before nvcc reads them, so an edit
+    # made while it runs leaves the stamp stale rather than wrong
+    d = digest(cmd)
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
     stamp = stamp_path(out)
     os.makedirs(os.path.dirname(stamp), exist_ok=True)
     with open(stamp, "w") as fh:
-        fh.write(digest(cmd) + "\n")
+        fh.write(d + "\n")
     return out
 
 

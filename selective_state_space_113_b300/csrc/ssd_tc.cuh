@@ -338,36 +338,47 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             }
             ptx::tma_load_4d(in + Layout::kX, &tmX, full, 0, (int)hh, t0, (int)b);
         };
+        // The descriptors of a product are formed once and stepped per K
+        // slice: the start address sits in the low 14 bits (in 16-byte
+        // units; shared memory is below 256 KB), so adding a slice's offset
+        // in 16-byte units moves only that field.  Each MMA is then an add
+        // and the instruction; this thread shares its SM sub-partition with
+        // two epilogue warps, and the tensor cores wait for what it issues.
+        // K-major operands (C, and B as S's operand): slice k at
+        // (k / 4) * 16384 + (k % 4) * 32 bytes; MN-major ones: k * 2048.
+        auto koff = [](int k) { return (uint64_t)((k >> 2) * 1024 + (k & 3) * 2); };
         auto issue_s = [&](long long c) {   // S = C B^T
             const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
-                mma(tmem + kColS, sdesc(in + Layout::kC + ko, 16, 1024),
-                    sdesc(in + Layout::kB + ko, 16, 1024), idS, k > 0);
-            }
+            const uint64_t da = sdesc(in + Layout::kC, 16, 1024), db = sdesc(in + Layout::kB, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(tmem + kColS, da + koff(k), db + koff(k), idS, k > 0);
             mma_commit(&bar[kMmaS]);
         };
         auto issue_yx = [&](long long c) {   // Yx = C H, H as hi then lo
             const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
-            for (int part = 0; part < 2; ++part)
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ko = (uint32_t)((k >> 2) * 16384 + (k & 3) * 32);
-                    mma(tmem + kColYx, sdesc(in + Layout::kC + ko, 16, 1024),
-                        sdesc((part ? sHl : sHh) + k * 2048, 16384, 1024), idY, part > 0 || k > 0);
-                }
+            const uint64_t da = sdesc(in + Layout::kC, 16, 1024);
+            const uint64_t dh = sdesc(sHh, 16384, 1024), dl = sdesc(sHl, 16384, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(tmem + kColYx, da + koff(k), dh + (uint64_t)(k * 128), idY, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(tmem + kColYx, da + koff(k), dl + (uint64_t)(k * 128), idY, 1);
             mma_commit(&bar[kMmaYx]);
         };
         auto issue_2 = [&](long long c) {   // G = B^T (w o X), then Yi = (masked S) X
             const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
-            for (int part = 0; part < 2; ++part)
-                for (int k = 0; k < 8; ++k)
-                    mma(tmem + kColG, sdesc(in + Layout::kB + k * 2048, 16384, 1024),
-                        sdesc((part ? sWl : sWh) + k * 2048, 16384, 1024), idG, part > 0 || k > 0);
+            const uint64_t db = sdesc(in + Layout::kB, 16384, 1024), dx = sdesc(in + Layout::kX, 16384, 1024);
+            const uint64_t dh = sdesc(sWh, 16384, 1024), dl = sdesc(sWl, 16384, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma(tmem + kColG, db + (uint64_t)(k * 128), dh + (uint64_t)(k * 128), idG, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(tmem + kColG, db + (uint64_t)(k * 128), dl + (uint64_t)(k * 128), idG, 1);
             mma_commit(&bar[kMmaG]);
-            for (int part = 0; part < 2; ++part)
-                for (int k = 0; k < 8; ++k)
-                    mma_ta(tmem + kColYi, tmem + (part ? kColSl : kColSh) + 8 * k,
-                           sdesc(in + Layout::kX + k * 2048, 16384, 1024), idY, part > 0 || k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma_ta(tmem + kColYi, tmem + kColSh + 8 * k, dx + (uint64_t)(k * 128), idY, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma_ta(tmem + kColYi, tmem + kColSl + 8 * k, dx + (uint64_t)(k * 128), idY, 1);
             mma_commit(&bar[kMmaYi]);
         };
         auto wait = [&](int which, long long k) {   // k-th completion of a barrier, whole warp
