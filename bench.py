@@ -666,16 +666,16 @@ def bench_backward(ssm, inp, w, stream, reps: int = 5):
     bwd_ckpt_ms = best_of(bwd_ckpt)
     return {"ms": best, "elements_per_s": w.elements / (best * 1e-3),
             "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (best * 1e-3) / 1e9,
-            "kernel_launches": 6 if w.L > 32 else 3,
+            "kernel_launches": 5 if w.L > 32 else 3,
             "with_forward_checkpoints": {
                 "backward_ms": bwd_ckpt_ms, "forward_ms": fwd_ckpt_ms,
                 "checkpoint_bytes": ckpt.numel() * 4, "kernel_launches": 4 if w.L > 32 else 3,
                 "note": "ssm_scan_bwd_ckpt reading the unit states that ssm_scan_fwd_ckpt "
                         "wrote (no summary pass of its own); forward_ms is that forward "
                         "pass, y and h_last as ssm_scan_fwd plus the states"},
-            "note": "one ssm_scan_bwd call: forward unit summaries + carry (state checkpoints "
-                    "every 32 steps), adjoint summaries + carry, the unit kernel, the dB/dC "
-                    "reduction; best of %d" % reps}
+            "note": "one ssm_scan_bwd call: the chained forward scan writing the state "
+                    "entering every 32-step unit (its y into du), adjoint summaries + carry, "
+                    "the unit kernel, the dB/dC reduction; best of %d" % reps}
 
 
 def bench_ssd(ssm, dev, stream, reps: int = 5):

@@ -248,13 +248,13 @@ int bwd_impl(const void* u, const void* delta, const float* dt_bias, const float
                 static_cast<const float*>(B), static_cast<const float*>(C), Dskip,
                 static_cast<const float*>(z), static_cast<const float*>(dy), dh_last,
                 static_cast<float*>(du), static_cast<float*>(ddelta), ddt_bias, dA, dB, dC,
-                dDskip, static_cast<float*>(dz), batch, L, D, stream, ckpt);
+                dDskip, static_cast<float*>(dz), batch, L, D, stream, ckpt, plan);
         return ssm::bwd::launch_scan_bwd16<bf16>(
             static_cast<const bf16*>(u), static_cast<const bf16*>(delta), dt_bias, A,
             static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip,
             static_cast<const bf16*>(z), static_cast<const bf16*>(dy), dh_last,
             static_cast<bf16*>(du), static_cast<bf16*>(ddelta), ddt_bias, dA, dB, dC, dDskip,
-            static_cast<bf16*>(dz), batch, L, D, stream, ckpt);
+            static_cast<bf16*>(dz), batch, L, D, stream, ckpt, plan);
     }
     float* scratch = nullptr;
     const size_t bytes = sizeof(float) * ssm::bwdg::bwd_generic_scratch_floats(batch, L, D, N);

@@ -56,22 +56,49 @@ inline cudaError_t resident_tmem(K kern, int threads, int smem, int tmem_cols, i
 
 // Returns an ssm_status_t.  Preconditions (checked by the caller): N == 16;
 // u, delta, z, dy, B, C, A and du 16-byte aligned; D * sizeof(T) % 16 == 0;
-// batch*D > 0; L > 0; dz given when z is.
+// batch*D > 0; L > 0; dz given when z is.  `plan` is the forward's plan
+// choice (kPlanAuto unless forced).
 template <typename T>
 int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const float* A,
                       const T* Bm, const T* Cm, const float* Dskip, const T* z, const T* dy,
                       const float* dh_last, T* du, T* ddelta, float* ddt_bias, float* dA,
                       float* dB, float* dC, float* dDskip, T* dz, long long batch, long long L,
-                      long long D, cudaStream_t stream, const float* ckpt = nullptr) {
+                      long long D, cudaStream_t stream, const float* ckpt = nullptr,
+                      int plan = tile::kPlanAuto) {
     using namespace tile;
     static_assert(TU == kCkptSteps, "checkpoint interval");
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SSM_ERR_CUDA;
-    long long wa = 0;
-    if (prepare<T, (int)kAggregate, (int)kZOH>(sms, &wa) != cudaSuccess || wa < 1)
+    long long wa = 0, wc = 0;
+    if (prepare<T, (int)kAggregate, (int)kZOH>(sms, &wa) != cudaSuccess || wa < 1 ||
+        prepare<T, (int)kChained, (int)kZOH>(sms, &wc) != cudaSuccess || wc < 1)
         return SSM_ERR_CUDA;
+    // Without the forward pass's checkpoints, the states entering the units
+    // come from the forward scan itself when it would run its chained plan
+    // (the chains fill the GPU): one pass, which writes every unit boundary's
+    // state and a y that goes into du (the unit kernel overwrites all of du).
+    // That is cheaper than the unit summaries and their carry below, which
+    // remain for problems with too few chains, where the forward itself
+    // would run them and an output pass besides.
+    float* own_ckpt = nullptr;
+    if (!ckpt && L > TU && plan != kPlanNarrow &&
+        (plan == kPlanChained || batch * cdiv(D, tile::CB) * 100 >= wc * 55)) {
+        const size_t bytes = (size_t)cdiv(L, TU) * (size_t)(batch * D) * NS * 4;
+        if (fault::malloc_async(reinterpret_cast<void**>(&own_ckpt), bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SSM_ERR_NOMEM;
+        }
+        const int st = launch_scan_tile<T, (int)kZOH>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, du,
+                                                      nullptr, batch, L, D, kPlanChained, stream,
+                                                      nullptr, nullptr, 0, own_ckpt);
+        if (st != SSM_OK) {
+            cudaFreeAsync(own_ckpt, stream);
+            return st;
+        }
+        ckpt = own_ckpt;
+    }
     int occ_sum = 0, occ_unit = 0;
     if (resident(adjoint_summary_kernel<T>, CB, (int)sizeof(AdjSmem<T>), &occ_sum) != cudaSuccess ||
         resident_tmem(bwd_unit_kernel<T>, CB, (int)sizeof(BwdSmem<T>), 128, &occ_unit) != cudaSuccess ||
@@ -99,6 +126,7 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
     unsigned char* ws = nullptr;
     if (fault::malloc_async(reinterpret_cast<void**>(&ws), off, stream) != cudaSuccess) {
         cudaGetLastError();
+        if (own_ckpt) cudaFreeAsync(own_ckpt, stream);
         return SSM_ERR_NOMEM;
     }
     int status = SSM_OK;
@@ -200,6 +228,8 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
         if (cudaGetLastError() != cudaSuccess) status = SSM_ERR_CUDA;
     } while (0);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && status == SSM_OK) status = SSM_ERR_CUDA;
+    if (own_ckpt && cudaFreeAsync(own_ckpt, stream) != cudaSuccess && status == SSM_OK)
+        status = SSM_ERR_CUDA;
     return status;
 }
 

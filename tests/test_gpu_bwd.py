@@ -72,6 +72,13 @@ SHAPES = [  # (batch, L, D, dtype, plan)
     (2, 31, 32, torch.bfloat16, None),        # a single unit
     (1, 1, 16, torch.float32, None),
     (2, 200, 72, torch.bfloat16, "generic"),
+    # the states entering the units from the forward scan's chained plan
+    # (taken unforced when the chains fill the GPU, as at full size)
+    (2, 100, 96, torch.bfloat16, "chained"),
+    (1, 300, 256, torch.float32, "chained"),
+    (3, 97, 40, torch.bfloat16, "chained"),
+    # and from the unit summaries with their carry
+    (1, 300, 256, torch.float32, "narrow"),
 ]
 
 
