@@ -189,7 +189,12 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
     else if (plan == kPlanAuto) narrow = p.nchains * 100 < wc * 55;
     const long long forced_steps = env_ll("SSM_CHUNK_T", 0);
     if (narrow) {
-        const long long P0 = cdiv(4 * wa, p.nchains);
+        // About four units per resident CTA of the output pass, and no more:
+        // the units are of equal length and taken from a ticket, so a count
+        // just past a multiple of the CTAs leaves a last round with most of
+        // them idle (12 chains x 50 units on 148 CTAs ran as 5 rounds of
+        // work for 4.05 rounds' worth; 12 x 49 fits in 4).
+        const long long P0 = (4 * (wf < wa ? wf : wa)) / p.nchains;
         long long steps = cdiv(cdiv(L, P0 < 2 ? 2 : P0), TC) * TC;
         if (forced_steps > 0) steps = cdiv(forced_steps, TC) * TC;
         if (steps < TC) steps = TC;
