@@ -23,8 +23,11 @@
 // which is a_n times the one above, and divided by a_n once per flush.
 //
 // Plan (N == 16): the sequence is cut into units of TU steps.
-//   1. states entering every unit: the forward kernel's unit summaries and
-//      carry (scan_tile.cuh, kAggregate + carry_kernel) -> hin[k];
+//   1. states entering every unit -> hin[k]: the forward pass's checkpoints
+//      when the caller has them (ssm_scan_bwd_ckpt); else, when the chains
+//      fill the GPU, the chained forward scan writing them as it goes; else
+//      the forward kernel's unit summaries and carry (scan_tile.cuh,
+//      kAggregate + carry_kernel);
 //   2. adjoint summaries: each unit, walked backward from lam = 0, gives
 //      Q_k = Abar_{t0} lam_{t0} and sum(dl); adj_carry_kernel combines them
 //      from the last unit down into mu[k], the adjoint entering unit k at its

@@ -1,7 +1,8 @@
 // scan_bwd_host.cuh -- workspace and launches of the N == 16 backward pass
-// (scan_bwd.cuh): the forward unit summaries and carry for the states entering
-// every unit, the adjoint summaries and their carry, the unit kernel and the
-// dB/dC reduction, all on one stream.
+// (scan_bwd.cuh): the states entering every unit (the caller's checkpoints,
+// the chained forward scan, or the forward unit summaries and carry), the
+// adjoint summaries and their carry, the unit kernel and the dB/dC
+// reduction, all on one stream.
 #pragma once
 
 #include "scan_bwd.cuh"
