@@ -23,16 +23,23 @@
 // (hi = bf16(v), lo = bf16(v - hi)) and multiplied twice, every sum in fp32.
 // The masked scores go back into TMEM (packed bf16 pairs, the A operand of
 // Yi); C, B and X are double-buffered, so a chunk's loads and its S overlap
-// the previous chunk's epilogue.
+// the previous chunk's epilogue, and so is C H in TMEM, so that C H of a chunk
+// can go as soon as its entering state is written.
 //
-// One CTA owns one (b, h) and walks its chunks in order.  Nine warps:
-//   warp 8      control: TMA loads of a chunk's C, B (K-major, two 64-wide
-//               regions each) and X (its 128 steps x 64 channels) into one of
-//               two buffers, and the MMAs, one elected thread, each group
-//               issued as soon as what it reads is ready; the whole warp
-//               computes the next chunk's step sizes and cumulative decay
-//               (from dt values prefetched a chunk ahead) while the tensor
-//               cores work on the current one;
+// One CTA owns one (b, h) and walks its chunks in order.  Ten warps:
+//   warp 8      products: one elected thread issues the MMAs, each as soon as
+//               what it reads is written and its accumulator has been read,
+//               in the order the epilogue produces them: C H of chunk c (the
+//               state after c - 1), G (w o X of c, signalled apart from the
+//               scores), Yi (the masked scores of c), then S of c + 1;
+//   warp 9      copies and decays: TMA loads of a chunk's C, B (K-major, two
+//               64-wide regions each) and X (its 128 steps x 64 channels) into
+//               one of two buffers once the epilogue is done with the buffer,
+//               and, for the whole warp, each chunk's step sizes and
+//               cumulative decay (from dt values loaded a chunk ahead) once the
+//               previous chunk's scores have read the shared copy.  Kept apart
+//               from warp 8 because an MMA issue can stall until the tensor
+//               cores take it;
 //   warps 0..7  epilogue, two warps per TMEM lane quadrant (warp e serves
 //               lanes 32 (e % 4) .. +31, i.e. rows of every product, and one
 //               half of its columns): w o X, the masked scores, the outputs,
@@ -58,8 +65,9 @@ constexpr int Q = 128;           // steps per chunk
 constexpr int P = 64;            // channels per head
 constexpr int NP = 128;          // state rows as the kernel holds them (N padded to 128)
 constexpr int kEpWarps = 8;      // two per TMEM lane quadrant, each half the columns
-constexpr int THREADS = 32 * (kEpWarps + 1);
-constexpr int kCtl = kEpWarps;   // the control warp
+constexpr int THREADS = 32 * (kEpWarps + 2);
+constexpr int kCtl = kEpWarps;       // the warp that issues the products
+constexpr int kLdr = kEpWarps + 1;   // the warp that issues the copies and forms the decays
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory: every operand tile is 1024-byte aligned, rows of 128 bytes,
@@ -76,25 +84,29 @@ struct Layout {
     static constexpr int kCum = kHl + 16384;  // cum_t log2(e), [Q] float
     static constexpr int kDt = kCum + 512;    // dt_t, [Q] float
     static constexpr int kBar = kDt + 512;    // mbarriers
-    static constexpr int kNumBars = 11;
+    static constexpr int kNumBars = 12;
     static constexpr int kTmem = kBar + 8 * kNumBars;   // TMEM base address (written by alloc)
     static constexpr int kBytes = kTmem + 16;
     static constexpr int kSmemBytes = kBytes + 1024;    // + slack to align the base
 };
 static_assert(Layout::kSmemBytes <= 227 * 1024, "CTA shared memory");
 
-// TMEM columns: the fp32 accumulators (lane = row), then the masked scores
-// as the A operand of Yi (packed bf16 pairs, s = 2c and 2c+1 in column c).
-constexpr uint32_t kColS = 0, kColYx = 128, kColYi = 192, kColG = 256;
-constexpr uint32_t kColSh = 320, kColSl = 384;
+// TMEM columns: the fp32 accumulators (lane = row; C H in two buffers, by
+// chunk parity), then the masked scores as the A operand of Yi (packed bf16
+// pairs, s = 2c and 2c+1 in column c).
+constexpr uint32_t kColS = 0, kColYx0 = 128, kColYi = 192, kColG = 256;
+constexpr uint32_t kColSh = 320, kColSl = 384, kColYx1 = 448;
 constexpr uint32_t kTmemCols = 512;
 
 // kInFull[2] / kInFree[2]: a buffer's C, B, X landed / the epilogue is done
 // with them; kMmaS, kMmaYx, kMmaYi, kMmaG: S, C H, the masked product, G
-// completed; kEpReady: the masked scores and w o X are written; kHReady: the
-// entering state's copy is written; kCum: the cumulative decays are written.
+// completed; kWxReady: w o X is written (by the four warps that form it);
+// kEpReady: the masked scores are written; kHReady: the entering state's copy
+// is written; kCum: the cumulative decays are written.
 enum Bar : int { kInFull = 0, kInFree = 2, kMmaS = 4, kMmaYx, kEpReady, kMmaYi, kMmaG, kHReady,
-                 kCum };
+                 kCum, kWxReady };
+static_assert(kWxReady + 1 <= Layout::kNumBars, "barrier count");
+constexpr int kWxWarps = 4;   // the epilogue warps of lane quadrants 0 and 1
 
 struct Args {
     const bf16* x;
@@ -278,6 +290,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         ptx::mbar_init(&bar[kMmaG], 1);
         ptx::mbar_init(&bar[kHReady], kEpWarps);
         ptx::mbar_init(&bar[kCum], 1);
+        ptx::mbar_init(&bar[kWxReady], kWxWarps);
         ptx::fence_mbar_init();
     }
     {
@@ -306,12 +319,15 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     const uint32_t tmem = *tmem_slot;
     bool failed = false;
 
-    if (warp == kCtl) {
+    if (warp >= kCtl) {
         // ------------------------------------------------------------- control
-        // Lane 0 issues the loads and the products; the whole warp waits and
-        // computes the step sizes and the cumulative decay of each chunk.
+        // Two warps, so that neither holds the other back: an MMA issue can
+        // stall until the tensor cores take it.  Warp kCtl: lane 0 issues
+        // the products.  Warp kLdr: lane 0 issues the copies, and the whole
+        // warp computes the step sizes and the cumulative decay of each
+        // chunk.  Both wait as whole warps.
         const bool leader = lane == 0;
-        if (leader) {
+        if (leader && warp == kLdr) {
             ptx::prefetch_tensormap(&tmX);
             ptx::prefetch_tensormap(&tmB);
             ptx::prefetch_tensormap(&tmC);
@@ -354,19 +370,20 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             for (int k = 0; k < 8; ++k) mma(tmem + kColS, da + koff(k), db + koff(k), idS, k > 0);
             mma_commit(&bar[kMmaS]);
         };
-        auto issue_yx = [&](long long c) {   // Yx = C H, H as hi then lo
+        auto issue_yx = [&](long long c) {   // Yx = C H into buffer c % 2, H as hi then lo
             const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            const uint32_t col = tmem + ((c & 1) ? kColYx1 : kColYx0);
             const uint64_t da = sdesc(in + Layout::kC, 16, 1024);
             const uint64_t dh = sdesc(sHh, 16384, 1024), dl = sdesc(sHl, 16384, 1024);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mma(tmem + kColYx, da + koff(k), dh + (uint64_t)(k * 128), idY, k > 0);
+            for (int k = 0; k < 8; ++k) mma(col, da + koff(k), dh + (uint64_t)(k * 128), idY, k > 0);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mma(tmem + kColYx, da + koff(k), dl + (uint64_t)(k * 128), idY, 1);
+            for (int k = 0; k < 8; ++k) mma(col, da + koff(k), dl + (uint64_t)(k * 128), idY, 1);
             mma_commit(&bar[kMmaYx]);
         };
-        auto issue_2 = [&](long long c) {   // G = B^T (w o X), then Yi = (masked S) X
+        auto issue_g = [&](long long c) {   // G = B^T (w o X)
             const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
-            const uint64_t db = sdesc(in + Layout::kB, 16384, 1024), dx = sdesc(in + Layout::kX, 16384, 1024);
+            const uint64_t db = sdesc(in + Layout::kB, 16384, 1024);
             const uint64_t dh = sdesc(sWh, 16384, 1024), dl = sdesc(sWl, 16384, 1024);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -374,6 +391,10 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
 #pragma unroll
             for (int k = 0; k < 8; ++k) mma(tmem + kColG, db + (uint64_t)(k * 128), dl + (uint64_t)(k * 128), idG, 1);
             mma_commit(&bar[kMmaG]);
+        };
+        auto issue_yi = [&](long long c) {   // Yi = (masked S) X
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            const uint64_t dx = sdesc(in + Layout::kX, 16384, 1024);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mma_ta(tmem + kColYi, tmem + kColSh + 8 * k, dx + (uint64_t)(k * 128), idY, k > 0);
@@ -384,13 +405,16 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         auto wait = [&](int which, long long k) {   // k-th completion of a barrier, whole warp
             return __all_sync(0xffffffffu, bwait(&bar[which], (uint32_t)(k & 1), a.wait_ns));
         };
-        // raw dt of the steps 4 lane .. 4 lane + 3 of a chunk (a chunk ahead)
-        float raw[4];
+        // raw dt of the steps 4 lane .. 4 lane + 3 of a chunk (a chunk ahead),
+        // kept as loaded: nothing here uses the values, so the loads complete
+        // while this warp goes on (steps past L read the last one, and the
+        // decay masks them)
+        unsigned short raw[4];
         auto load_dt = [&](long long c) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const long long t = c * Q + 4 * lane + j;
-                raw[j] = t < a.L ? __bfloat162float(a.dt[(b * a.L + t) * a.H + hh]) : 0.0f;
+                raw[j] = reinterpret_cast<const unsigned short*>(a.dt)[(b * a.L + (t < a.L ? t : a.L - 1)) * a.H + hh];
             }
         };
         // step sizes and cumulative decay of chunk c into the shared copy (its
@@ -400,7 +424,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             float d[4], cl[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float v2 = fmaf(raw[j], kLog2e, kb2);
+                const float v2 = fmaf(__bfloat162float(__ushort_as_bfloat16(raw[j])), kLog2e, kb2);
                 const float sp = (v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2))) * 0.6931471805599453f;
                 d[j] = 4 * lane + j < nv ? sp : 0.0f;
                 cl[j] = (j ? cl[j - 1] : 0.0f) + A * d[j];
@@ -419,53 +443,86 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             __syncwarp();
             if (leader) ptx::mbar_arrive(&bar[kCum]);
         };
-        // prologue: chunk 0's decay, the first two chunks' loads, chunk 0's S and C H
-        load_dt(0);
-        scan(0);
-        if (nchunks > 1) load_dt(1);
-        if (leader) {
-            load(0);
-            if (nchunks > 1) load(1);
-        }
-        if (!wait(kInFull, 0)) failed = true;
-        if (!failed) {
-            fence_after_sync();
-            if (leader) issue_s(0);
-            if (!wait(kHReady, 0)) failed = true;
-        }
-        if (!failed) {
-            fence_after_sync();
-            if (leader) issue_yx(0);
-        }
-        for (long long c = 0; c < nchunks && !failed; ++c) {
-            // the masked scores of chunk c are in TMEM, w o X in shared memory
-            if (!wait(kEpReady, c)) { failed = true; break; }
-            fence_after_sync();
-            if (leader) issue_2(c);
-            if (c + 1 < nchunks) {
+        if (warp == kLdr) {
+            // The first two chunks' copies and chunk 0's decay; then, per
+            // chunk c, the copies of chunk c + 1 once the outputs of chunk
+            // c - 1 are done with its buffer, and the decay of chunk c + 1
+            // once the scores of chunk c have read the shared copy (the
+            // order in which the epilogue's iteration for chunk c frees them).
+            load_dt(0);
+            scan(0);
+            if (nchunks > 1) load_dt(1);
+            if (leader) {
+                load(0);
+                if (nchunks > 1) load(1);
+            }
+            for (long long c = 0; c + 1 < nchunks && !failed; ++c) {
+                if (c > 0) {
+                    if (!wait(kInFree + (int)((c - 1) & 1), (c - 1) >> 1)) { failed = true; break; }
+                    if (leader) load(c + 1);
+                }
+                if (!wait(kEpReady, c)) { failed = true; break; }
                 scan(c + 1);
                 if (c + 2 < nchunks) load_dt(c + 2);
-                // chunk c+1's S (S of chunk c has been read by the epilogue)
-                if (!wait(kInFull + (int)((c + 1) & 1), (c + 1) >> 1)) { failed = true; break; }
-                fence_after_sync();
-                if (leader) issue_s(c + 1);
             }
-            if (c + 1 < nchunks) {
-                // The epilogue is done with chunk c: its outputs have read Yx
-                // (which chunk c+1's C H overwrites) and buffer c % 2 is free.
-                if (!wait(kInFree + (int)(c & 1), c >> 1)) { failed = true; break; }
-                if (leader && c + 2 < nchunks) load(c + 2);
-                if (!wait(kHReady, c + 1)) { failed = true; break; }
+            // Every copy issued here is waited for by the product warp
+            // before the products that read it.
+            if (failed && leader) atomicOr(&g_error_word, kErrTimeout);
+            __syncwarp();
+        } else {
+            // chunk 0's S and C H (of the zero state)
+            if (!wait(kInFull, 0)) failed = true;
+            if (!failed) {
                 fence_after_sync();
-                if (leader) issue_yx(c + 1);
+                if (leader) issue_s(0);
+                if (!wait(kHReady, 0)) failed = true;
             }
+            if (!failed) {
+                fence_after_sync();
+                if (leader) issue_yx(0);
+            }
+            // Each product goes as soon as what it reads is written and its
+            // accumulator has been read, in the order the epilogue's phases
+            // produce them within its iteration for chunk c (the state after
+            // chunk c - 1, w o X of chunk c, the outputs of chunk c - 1, the
+            // masked scores of chunk c): this thread issues in order, so a
+            // wait on a later event would hold back an earlier product.
+            for (long long c = 0; c < nchunks && !failed; ++c) {
+                if (c > 0) {
+                    // The state entering chunk c is written, and every
+                    // epilogue warp has read G of chunk c - 1.  C H of chunk
+                    // c goes into buffer c % 2, last read by the outputs of
+                    // chunk c - 2, which precede the scores of chunk c - 1
+                    // (kEpReady, seen in the previous iteration); C of chunk
+                    // c landed before its S went.
+                    if (!wait(kHReady, c)) { failed = true; break; }
+                    fence_after_sync();
+                    if (leader) issue_yx(c);
+                }
+                // G(c): w o X of chunk c is written
+                if (!wait(kWxReady, c)) { failed = true; break; }
+                fence_after_sync();
+                if (leader) issue_g(c);
+                // Yi(c): the masked scores of chunk c are in TMEM; then S of
+                // chunk c + 1 (S of chunk c has been read)
+                if (!wait(kEpReady, c)) { failed = true; break; }
+                fence_after_sync();
+                if (leader) issue_yi(c);
+                if (c + 1 < nchunks) {
+                    if (!wait(kInFull + (int)((c + 1) & 1), (c + 1) >> 1)) { failed = true; break; }
+                    fence_after_sync();
+                    if (leader) issue_s(c + 1);
+                }
+            }
+            // Leave no product in flight (bounded): the last chunk's Yi,
+            // the last product issued, completes after all of them; a
+            // parity wait names the last phase alone, and Yi of the chunk
+            // before completed (the outputs of that chunk, which precede
+            // the last chunk's scores, waited for it).
+            if (nchunks > 0 && !failed && !wait(kMmaYi, nchunks - 1)) failed = true;
+            if (failed && leader) atomicOr(&g_error_word, kErrTimeout);
+            __syncwarp();
         }
-        if (failed && leader) atomicOr(&g_error_word, kErrTimeout);
-        // Leave no copy or product in flight (bounded): every load was
-        // waited for before its MMAs, and the last chunk's Yi, the last
-        // product issued, completes after all of them.
-        if (nchunks > 0 && !failed) wait(kMmaYi, nchunks - 1);
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3, hf = warp >> 2;   // TMEM lane quadrant; column half
@@ -502,7 +559,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             const int nv = (int)(a.L - c * Q < Q ? a.L - c * Q : Q);
             float yi[32], yx[32];
             tmem_ld32_nowait(lane_addr + kColYi + 32 * hf, yi);
-            tmem_ld32_nowait(lane_addr + kColYx + 32 * hf, yx);
+            tmem_ld32_nowait(lane_addr + ((c & 1) ? kColYx1 : kColYx0) + 32 * hf, yx);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             bf16* yrow = a.y + ((b * a.L + c * Q + row) * a.H + hh) * P + 32 * hf;
 #pragma unroll
@@ -572,6 +629,8 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                         *reinterpret_cast<uint4*>(sm + Layout::kWl + sw128(s_, cc)) = l;
                     }
                 }
+                ptx::fence_proxy_async_shared();   // w o X, for the tensor cores (G)
+                warp_arrive(&bar[kWxReady], lane);
             }
             // the previous chunk's outputs (its Yi ran after G)
             if (c > 0 && !outputs(c - 1, ecum_prev)) { failed = true; break; }
@@ -584,13 +643,16 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                 break;
             }
             fence_after_sync();
+            float sv[2][32];
+            tmem_ld32_nowait(lane_addr + kColS + 32 * hf, sv[0]);
+            if (hf + 2 <= quad) tmem_ld32_nowait(lane_addr + kColS + 32 * (hf + 2), sv[1]);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int piece = hf + 2 * k;
                 uint32_t hi[16], lo[16];
                 if (piece <= quad) {   // some s of the piece are <= t (warp-uniform)
-                    float v[32];
-                    tmem_ld32(lane_addr + kColS + 32 * piece, v);
+                    float (&v)[32] = sv[k];
                     const float4* cum4 = reinterpret_cast<const float4*>(cum + 32 * piece);
                     const float4* dt4 = reinterpret_cast<const float4*>(dts + 32 * piece);
 #pragma unroll
