@@ -7,6 +7,16 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# Property tests draw the same examples on every run, so that a result does
+# not depend on which run found which case.
+try:
+    from hypothesis import settings as _hyp_settings
+
+    _hyp_settings.register_profile("repeatable", derandomize=True, database=None)
+    _hyp_settings.load_profile("repeatable")
+except ImportError:
+    pass
+
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")

@@ -68,6 +68,16 @@ def scan(lib, p, dtype=oracle.F32):
                            p["C"], p["Dskip"], p["z"], dtype=dtype, lib=lib)
 
 
+def _close_scaled(got, want, scale, rtol, what):
+    """|got - want| <= rtol * scale, scale the size of the terms summed."""
+    got, want = np.asarray(got), np.asarray(want)
+    assert got.shape == want.shape, f"{what}: shape {got.shape} != {want.shape}"
+    err = np.abs(got - want)
+    bad = ~(err <= rtol * np.asarray(scale))
+    assert not bad.any(), (f"{what}: {int(bad.sum())} mismatches, max err "
+                           f"{float(np.nanmax(err)):.3e}")
+
+
 def _close(got, want, rtol, atol, what):
     got, want = np.asarray(got), np.asarray(want)
     assert got.shape == want.shape, f"{what}: shape {got.shape} != {want.shape}"
@@ -413,15 +423,24 @@ def step_pipeline_check(lib, rng, batch, D, N):
     silu = torch.nn.functional.silu(torch.from_numpy(z.astype(np.float64))).numpy()
     want_s = np.zeros_like(st0)
     want_y = np.zeros((batch, D))
+    # the size of the terms each result sums: two float64 evaluations of the
+    # same sum differ by rounding relative to its terms, not to the sum
+    # (which can cancel to near zero)
+    scale_s = np.zeros_like(st0)
+    scale_y = np.zeros((batch, D))
     for b in range(batch):
         for d in range(D):
             for n in range(N):
                 ad, bd = zoh_ref(float(A[d, n]), float(dt[b, d]))
-                want_s[b, d, n] = ad * st0[b, d, n] + bd * float(B[b, n]) * float(u[b, d])
-            want_y[b, d] = (want_s[b, d] @ C[b].astype(np.float64)
-                            + float(Dskip[d]) * float(u[b, d])) * silu[b, d]
-    _close(st1, want_s, 1e-12, 1e-14, "library step state")
-    _close(y1, want_y, 1e-12, 1e-14, "library step y")
+                t1, t2 = ad * st0[b, d, n], bd * float(B[b, n]) * float(u[b, d])
+                want_s[b, d, n] = t1 + t2
+                scale_s[b, d, n] = abs(t1) + abs(t2)
+            cs = C[b].astype(np.float64)
+            want_y[b, d] = (want_s[b, d] @ cs + float(Dskip[d]) * float(u[b, d])) * silu[b, d]
+            scale_y[b, d] = (np.abs(want_s[b, d]) @ np.abs(cs)
+                             + abs(float(Dskip[d]) * float(u[b, d]))) * abs(silu[b, d])
+    _close_scaled(st1, want_s, scale_s, 1e-12, "library step state")
+    _close_scaled(y1, want_y, scale_y, 1e-12, "library step y")
 
 
 def pin_step_matches_library_pipeline(lib):
