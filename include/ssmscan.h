@@ -98,8 +98,12 @@ typedef enum {
  *                 last step (h_last == NULL: not written).  It has the layout
  *                 of ssm_step's `state`, so a prefill continues into decode.
  * Sizes: batch, L, D >= 0; 1 <= N <= SSM_MAX_N.  L == 0 writes h_last = 0.
- * The fast path may take a small stream-ordered workspace
- * (cudaMallocAsync/cudaFreeAsync on `stream`); SSM_ERR_NOMEM if that fails.
+ * The fast path may take a small stream-ordered workspace (allocated and
+ * freed on `stream`); SSM_ERR_NOMEM if that fails.  Workspaces of every entry
+ * point come from a memory pool the library makes on each device (per
+ * context), which keeps up to 1 GiB reserved between calls so that a call
+ * after a synchronisation does not map its workspace again; that memory is
+ * held until the process exits or the context is destroyed.
  * Returns an ssm_status_t.
  */
 SSM_API int ssm_scan_fwd(const void *u, const void *delta, const float *dt_bias,

@@ -495,23 +495,8 @@ struct NoallocSlot {
 };
 NoallocSlot g_noalloc_slot[kMaxDevices] = {};
 
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-
-// cuCtxGetCurrent from the driver, found once through the runtime (the
-// library does not link libcuda).
-CtxGetCurrentFn ctx_get_current() {
-    static CtxGetCurrentFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<CtxGetCurrentFn>(f);
-    });
-    return fn;
-}
+using ssm::pool::CtxGetCurrentFn;
+using ssm::pool::ctx_get_current;
 
 // Device address of g_noalloc_scratch in the current device's current
 // context.  It is looked up with that device current the first time a call

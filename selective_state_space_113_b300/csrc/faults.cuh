@@ -16,6 +16,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include "pool.cuh"
+
 namespace ssm {
 namespace fault {
 
@@ -24,13 +26,16 @@ inline bool injected(const char* kind) {
     return v && std::strcmp(v, kind) == 0;
 }
 
-// cudaMallocAsync, or cudaErrorMemoryAllocation under SSM_FAULT_INJECT=alloc.
+// A stream-ordered workspace allocation from the library's pool (pool.cuh),
+// freed by the caller with cudaFreeAsync; cudaErrorMemoryAllocation under
+// SSM_FAULT_INJECT=alloc.
 inline cudaError_t malloc_async(void** p, size_t bytes, cudaStream_t s) {
-    if (injected("alloc")) {
-        *p = nullptr;
-        return cudaErrorMemoryAllocation;
-    }
-    return cudaMallocAsync(p, bytes, s);
+    *p = nullptr;
+    if (injected("alloc")) return cudaErrorMemoryAllocation;
+    cudaMemPool_t pl = nullptr;
+    const cudaError_t e = pool::current(&pl);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(p, bytes, pl, s);
 }
 
 // True when the launch about to be made must fail (SSM_FAULT_INJECT=launch);
