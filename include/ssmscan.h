@@ -100,10 +100,10 @@ typedef enum {
  * Sizes: batch, L, D >= 0; 1 <= N <= SSM_MAX_N.  L == 0 writes h_last = 0.
  * The fast path may take a small stream-ordered workspace (allocated and
  * freed on `stream`); SSM_ERR_NOMEM if that fails.  Workspaces of every entry
- * point come from a memory pool the library makes on each device (per
- * context), which keeps up to 1 GiB reserved between calls so that a call
- * after a synchronisation does not map its workspace again; that memory is
- * held until the process exits or the context is destroyed.
+ * point come from a memory pool the library makes on each device, which
+ * keeps up to 1 GiB reserved between calls so that a call after a
+ * synchronisation does not map its workspace again; that memory is held
+ * until the process exits.
  * Returns an ssm_status_t.
  */
 SSM_API int ssm_scan_fwd(const void *u, const void *delta, const float *dt_bias,
@@ -304,11 +304,11 @@ SSM_API int ssm_step(float *state, const void *u, const void *delta,
  *     SSM_NOALLOC_SCRATCH_BYTES; otherwise SSM_ERR_SCRATCH is returned before
  *     anything is enqueued.  (batch 4, D 5120 needs 2.8 KB with h_last and
  *     1.3 MB without.)
- *   - The first call in a device's context looks up the array's device
- *     address with that device current, and the first call on a device also
- *     sets the kernel's shared-memory attribute and queries its occupancy
- *     (both once per device).  Make that first call before any stream
- *     capture.
+ *   - The first call in each context of a device looks up the array's
+ *     device address with that device current, sets the kernel's
+ *     shared-memory attribute and queries its occupancy (a context made
+ *     after cudaDeviceReset counts as new).  Make that first call before
+ *     any stream capture.
  *   - All calls share the one array, and it keeps the last call's contents
  *     (each call clears the parts that must start at zero).  Calls whose
  *     work overlaps on the GPU -- on different streams, or from different

@@ -488,29 +488,24 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 constexpr int kMaxDevices = 128;
 std::mutex g_noalloc_mu;
-// Per device: the context the address was looked up in, and the address.
+// Per device: the ID of the context the address was looked up in, and the
+// address.
 struct NoallocSlot {
-    CUcontext ctx;
+    unsigned long long ctx;
     void* ptr;
 };
 NoallocSlot g_noalloc_slot[kMaxDevices] = {};
 
-using ssm::pool::CtxGetCurrentFn;
-using ssm::pool::ctx_get_current;
-
 // Device address of g_noalloc_scratch in the current device's current
 // context.  It is looked up with that device current the first time a call
-// runs in that context (the first call on a device, and again after the
-// context was destroyed and another one made current), so an address is never
-// reused from a context that is gone.
+// runs in that context (the first call on a device, and again in a context
+// made after the last one was destroyed, which may reuse its handle but not
+// its ID), so an address is never reused from a context that is gone.
 int noalloc_scratch_ptr(unsigned char** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSM_ERR_CUDA;
-    CtxGetCurrentFn get_ctx = ctx_get_current();
-    if (!get_ctx) return SSM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    CUcontext ctx = nullptr;
-    if (get_ctx(&ctx) != CUDA_SUCCESS) return SSM_ERR_CUDA;
+    unsigned long long ctx = ssm::context::current_id();
     NoallocSlot& slot = g_noalloc_slot[dev];
     if (!ctx || slot.ctx != ctx || !slot.ptr) {
         void* p = nullptr;
@@ -519,7 +514,8 @@ int noalloc_scratch_ptr(unsigned char** out) {
             return SSM_ERR_CUDA;
         }
         // The lookup makes the device's primary context current if none was.
-        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return SSM_ERR_CUDA;
+        ctx = ssm::context::current_id();
+        if (!ctx) return SSM_ERR_CUDA;
         slot.ctx = ctx;
         slot.ptr = p;
     }

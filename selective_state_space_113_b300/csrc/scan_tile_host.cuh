@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/ssmscan.h"
+#include "context.cuh"
 #include "faults.cuh"
 #include "scan_tile.cuh"
 #include "tma_host.cuh"
@@ -51,20 +52,27 @@ inline int forced_plan() {
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 // Sets the kernel's shared-memory limit and returns in *workers the number of
-// CTAs that can be resident at once.  Done once per device and kernel; later
-// calls read the cached count.
+// CTAs that can be resident at once.  Done once per device, context and
+// kernel (a kernel's attributes belong to its context: in a context made
+// after the last one was destroyed, the limit is set again); later calls
+// read the cached count.
 template <typename T, int MODE, int DISC, bool CONV = false>
 inline cudaError_t prepare(int sms, long long* workers) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
-    static long long cached[kMaxDev] = {};
+    struct Slot {
+        unsigned long long ctx;   // context ID
+        long long workers;
+    };
+    static Slot cached[kMaxDev] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDev) {
+    unsigned long long ctx = context::current_id();
+    if (ctx && dev >= 0 && dev < kMaxDev) {
         std::lock_guard<std::mutex> lock(mu);
-        if (cached[dev] > 0) {
-            *workers = cached[dev];
+        if (cached[dev].ctx == ctx && cached[dev].workers > 0) {
+            *workers = cached[dev].workers;
             return cudaSuccess;
         }
     }
@@ -76,9 +84,10 @@ inline cudaError_t prepare(int sms, long long* workers) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS, smem);
     if (e != cudaSuccess) return e;
     *workers = (long long)sms * occ;
-    if (dev >= 0 && dev < kMaxDev && *workers > 0) {
+    ctx = context::current_id();   // current now
+    if (ctx && dev >= 0 && dev < kMaxDev && *workers > 0) {
         std::lock_guard<std::mutex> lock(mu);
-        cached[dev] = *workers;
+        cached[dev] = Slot{ctx, *workers};
     }
     return cudaSuccess;
 }

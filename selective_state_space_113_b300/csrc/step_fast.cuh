@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "context.cuh"
 #include "faults.cuh"
 #include "ptx.cuh"
 #include "tma_host.cuh"
@@ -435,25 +436,33 @@ static cudaError_t launch_step16_tiled(float* state, const T* u, const T* delta,
             !tma::cached_map(&m.C, dt, 3, Cm, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
-    // per device, once: the kernel's shared-memory limit and the SM count
+    // per device and context, once: the kernel's shared-memory limit (an
+    // attribute of the context, set again after the context was destroyed
+    // and another made current) and the SM count
     constexpr int kMaxDev = 64;
     static std::mutex mu;
-    static int sms_of[kMaxDev] = {};
+    struct Slot {
+        unsigned long long ctx;   // context ID
+        int sms;
+    };
+    static Slot sms_of[kMaxDev] = {};
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDev) {
+    unsigned long long ctx = context::current_id();
+    if (ctx && dev >= 0 && dev < kMaxDev) {
         std::lock_guard<std::mutex> lock(mu);
-        sms = sms_of[dev];
+        if (sms_of[dev].ctx == ctx) sms = sms_of[dev].sms;
     }
     if (sms == 0) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDev) {
+        ctx = context::current_id();   // current now
+        if (ctx && dev >= 0 && dev < kMaxDev) {
             std::lock_guard<std::mutex> lock(mu);
-            sms_of[dev] = sms;
+            sms_of[dev] = Slot{ctx, sms};
         }
     }
     const long long tiles = ((D + TC - 1) / TC) * ((batch + NB - 1) / NB);
