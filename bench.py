@@ -156,7 +156,8 @@ def algorithmic_bytes(w) -> int:
 
 
 # Sources of the timed scan kernel: a recorded DRAM-traffic figure is used only
-# while these are unchanged since it was measured.
+# while these, and the library's compile flags, are unchanged since it was
+# measured.
 SCAN_KERNEL_SOURCES = ("scan_tile.cuh", "scan_tile_host.cuh", "ptx.cuh", "common.cuh")
 
 
@@ -175,7 +176,9 @@ def bench_config(w, world: int) -> dict:
 
 
 def csrc_digest() -> str:
+    from selective_state_space_113_b300 import build as libbuild
     h = hashlib.sha256()
+    h.update("\0".join(libbuild.FLAGS).encode())
     for name in SCAN_KERNEL_SOURCES:
         with open(os.path.join(ROOT, "selective_state_space_113_b300", "csrc", name), "rb") as fh:
             h.update(fh.read())

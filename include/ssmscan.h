@@ -247,7 +247,14 @@ SSM_API int ssm_scan_bwd_ckpt(const void *u, const void *delta, const float *dt_
  *                 layout of ssm_step's state with D = H * P channels
  * bf16 with P == 64, N == 64 or 128 and x, B, C, y 16-byte aligned runs the
  * tensor-core chunked kernel (the products in bf16, every sum in fp32);
- * anything else runs a one-thread-per-channel kernel.  Allocates nothing.
+ * anything else runs a one-thread-per-channel kernel.  The tensor-core kernel
+ * takes one head per CTA, and allocates nothing, unless that would leave its
+ * last wave of CTAs mostly empty (batch * H above the SM count, and the waves
+ * rounded up more than 15% above the heads' share of the SMs).  Then
+ * persistent CTAs take segments of heads from a ticket counter and pass each
+ * head's state between segments through a stream-ordered workspace of about
+ * batch * H * 32 KB (SSM_ERR_NOMEM if that allocation fails); the results are
+ * the same bits either way.
  * Returns an ssm_status_t.
  */
 SSM_API int ssm_ssd_fwd(const void *x, const void *dt, const float *dt_bias, const float *A,

@@ -335,7 +335,9 @@ extern "C" int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, 
             static_cast<const bf16*>(x), static_cast<const bf16*>(dt), dt_bias, A,
             static_cast<const bf16*>(B), static_cast<const bf16*>(C), Dskip, static_cast<bf16*>(y),
             h_last, batch, L, H, (int)N,
-            (unsigned long long)ssm::tile::env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL), stream);
+            (unsigned long long)ssm::tile::env_ll("SSM_WAIT_LIMIT_NS", 2000000000LL), stream,
+            ssm::tile::env_ll("SSM_SSD_SEG", 0), ssm::tile::env_ll("SSM_SSD_CTAS", 0));
+        if (e == cudaErrorMemoryAllocation) return SSM_ERR_NOMEM;
     } else if (dtype == SSM_F32) {
         e = ssm::ssd::launch_ssd_generic<float>(
             static_cast<const float*>(x), static_cast<const float*>(dt), dt_bias, A,

@@ -26,7 +26,16 @@
 // the previous chunk's epilogue, and so is C H in TMEM, so that C H of a chunk
 // can go as soon as its entering state is written.
 //
-// One CTA owns one (b, h) and walks its chunks in order.  Ten warps:
+// ssd_tc_kernel: one CTA owns one (b, h) and walks its chunks in order.
+// ssd_tc_dyn_kernel, the same roles and products on a ticket walk: head j =
+// b H + h is cut into segments of U chunks, and each (head, segment) is a
+// unit.  Persistent CTAs, one per SM, take units from a ticket counter,
+// segment-major (ticket t is segment t / heads of head t % heads), and walk
+// each in chunk order.  A unit's predecessor in its head went out `heads`
+// tickets earlier and has long finished when the unit needs its state, which
+// comes fp32 through global memory behind a counter the eight epilogue warps
+// release.  It is the launch's choice where one head per CTA would leave the
+// last wave mostly empty (see launch_ssd_tc).  Ten warps in both:
 //   warp 8      products: one elected thread issues the MMAs, each as soon as
 //               what it reads is written and its accumulator has been read,
 //               in the order the epilogue produces them: C H of chunk c (the
@@ -120,6 +129,94 @@ struct Args {
     int N;
     unsigned long long wait_ns;
 };
+
+// The ticket walk's arguments: those of the one-head walk, and its own.  Kept
+// to 120 bytes, so that with the three 128-byte tensor maps the kernel's
+// parameters stay within 512 bytes: the one-head kernel, given 40 bytes more
+// (its parameters at 520 bytes), ran 13% slower, registers and shared memory
+// unchanged (measured).
+struct ArgsDyn {
+    const bf16* x;
+    const bf16* dt;
+    const float* dt_bias;
+    const float* A;
+    const float* Dskip;
+    bf16* y;
+    float* h_last;
+    unsigned long long* ticket;   // units handed out (NULL: one unit per CTA, its index)
+    float* carry;                 // [heads][NP][P]: the state after a head's last segment done
+    unsigned* done;               // [heads]: 8 x the segments of the head done
+    long long batch, L, H;
+    int N;
+    int seg;                      // U, chunks per segment
+    unsigned long long wait_ns;
+};
+static_assert(sizeof(ArgsDyn) == 120 && 3 * sizeof(CUtensorMap) + sizeof(ArgsDyn) <= 512,
+              "ticket kernel parameters");
+
+// The ticket walk's shared memory: the one-head layout up to the step sizes,
+// then the two chunk records and the CTA's first ticket, the barriers and
+// the TMEM address.
+struct LayoutDyn {
+    static constexpr int kRec = Layout::kDt + 512;   // ChunkRec of the k-th chunk at [k % 2]
+    static constexpr int kFirst = kRec + 96;          // the CTA's first ticket
+    static constexpr int kBar = kFirst + 16;          // mbarriers
+    static constexpr int kTmem = kBar + 8 * Layout::kNumBars;
+    static constexpr int kBytes = kTmem + 16;
+    static constexpr int kSmemBytes = kBytes + 1024;
+};
+static_assert(LayoutDyn::kSmemBytes <= 227 * 1024, "CTA shared memory");
+
+// The unit a CTA walks and its chunk: head j, segment sg, chunk c of the
+// head, and the end hi of the segment's chunks.
+struct Walk {
+    int j, sg, c, hi;
+    __device__ __forceinline__ void unit(long long t, long long heads, int U, int nch) {
+        sg = (int)(t / heads);
+        j = (int)(t - (long long)sg * heads);
+        c = sg * U;
+        hi = c + U < nch ? c + U : nch;
+    }
+};
+
+// A load issued here, in program order with the other volatile asm (the
+// waits), so that its latency passes while the warp goes on.
+__device__ __forceinline__ float ld_early(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// What the epilogue (and, for `next`, the product warp) needs of the k-th
+// chunk a CTA walks, written by the copy warp with the chunk's decays: where
+// its outputs go, how its state enters (`start`: it continues the chunk
+// before, starts its head from zero, or continues the segment before, done
+// by whichever CTA), whether the state after it leaves (`end`: as h_last, or
+// for the head's next segment), and how the next chunk's enters (`next`,
+// with that chunk's head and segment; kNone: no next chunk).
+enum : int { kCont = 0, kZero = 1, kHand = 2, kNone = 3 };   // start / next
+enum : int { kEndNone = 0, kEndHead = 1, kEndHand = 2 };      // end
+struct ChunkRec {
+    int b, h, c, nv, j, sg, start, end, next, nj, nsg;
+    float dsk;
+};
+static_assert(sizeof(ChunkRec) == 48, "record size");
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait for a counter in global memory to reach `target` (acquire).
+__device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target,
+                                           unsigned long long ns) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::ld_acquire(p) < target) {
+        if (ptx::globaltimer() - t0 > ns) return false;
+        ptx::nanosleep(128);
+    }
+    return true;
+}
+
 
 // Byte offset of 16-byte chunk c of row r in a 128B-swizzled region.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
@@ -703,6 +800,569 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                      : "memory");
 }
 
+__global__ void __launch_bounds__(THREADS, 1)
+ssd_tc_dyn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmC, const ArgsDyn a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + LayoutDyn::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LayoutDyn::kTmem);
+    float* cum = reinterpret_cast<float*>(sm + Layout::kCum);
+    float* dts = reinterpret_cast<float*>(sm + Layout::kDt);
+    ChunkRec* recs = reinterpret_cast<ChunkRec*>(sm + LayoutDyn::kRec);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nchunks = (int)((a.L + Q - 1) / Q);
+    const long long heads = a.batch * a.H;
+    const bool two_regions = a.N > 64;
+    unsigned long long* first = reinterpret_cast<unsigned long long*>(sm + LayoutDyn::kFirst);
+
+    // ---- set-up: barriers, zeroed state operand and padding regions, TMEM
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&bar[kInFull + i], 1);
+            ptx::mbar_init(&bar[kInFree + i], kEpWarps);
+        }
+        ptx::mbar_init(&bar[kMmaS], 1);
+        ptx::mbar_init(&bar[kMmaYx], 1);
+        ptx::mbar_init(&bar[kEpReady], kEpWarps);
+        ptx::mbar_init(&bar[kMmaYi], 1);
+        ptx::mbar_init(&bar[kMmaG], 1);
+        ptx::mbar_init(&bar[kHReady], kEpWarps);
+        ptx::mbar_init(&bar[kCum], 1);
+        ptx::mbar_init(&bar[kWxReady], kWxWarps);
+        ptx::fence_mbar_init();
+        *first = a.ticket ? atomicAdd(a.ticket, 1ull) : (unsigned long long)blockIdx.x;
+    }
+    {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < 2 * 16384 / 16; i += THREADS) {
+            reinterpret_cast<uint4*>(sm + Layout::kHh)[i] = z;   // kHh and kHl are adjacent
+            if (!two_regions) {
+                const int j = i % 1024, buf = i / 1024;
+                unsigned char* in = sm + buf * Layout::kInBytes;
+                reinterpret_cast<uint4*>(in + Layout::kC + 16384)[j] = z;
+                reinterpret_cast<uint4*>(in + Layout::kB + 16384)[j] = z;
+            }
+        }
+    }
+    if (warp == kCtl) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         ptx::smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    ptx::fence_proxy_async_shared();   // the zeroed operands, for the tensor cores
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool failed = false;
+    const long long units = heads * ((nchunks + a.seg - 1) / a.seg);   // heads x segments
+    const bool work = (long long)*first < units;   // the CTA has a unit at all
+
+    if (!work) {
+        // no unit left for this CTA: straight to the tear-down
+    } else if (warp >= kCtl) {
+        // ------------------------------------------------------------- control
+        // Two warps, so that neither holds the other back: an MMA issue can
+        // stall until the tensor cores take it.  Warp kCtl: lane 0 issues
+        // the products.  Warp kLdr: lane 0 issues the copies, and the whole
+        // warp computes the step sizes and the cumulative decay of each
+        // chunk.  Both wait as whole warps.
+        const bool leader = lane == 0;
+        if (leader && warp == kLdr) {
+            ptx::prefetch_tensormap(&tmX);
+            ptx::prefetch_tensormap(&tmB);
+            ptx::prefetch_tensormap(&tmC);
+        }
+        const uint32_t in_bytes = (two_regions ? 4 : 2) * 16384 + 16384;
+        const uint32_t s0 = ptx::smem_u32(sm);
+        const uint32_t sWh = s0 + Layout::kWh, sWl = s0 + Layout::kWl;
+        const uint32_t sHh = s0 + Layout::kHh, sHl = s0 + Layout::kHl;
+        constexpr uint32_t idS = idesc(128, 128, 0, 0), idY = idesc(128, 64, 0, 1),
+                           idG = idesc(128, 64, 1, 1);
+        // The walk, a chunk ahead of the copies: load_dt() takes the chunk
+        // `cur` and moves it on (taking a ticket at a unit's end), and leaves
+        // the chunk's head and step for the copies in slot k % 2.
+        Walk cur;
+        cur.unit((long long)*first, heads, a.seg, nchunks);
+        int qb0 = 0, qh0 = 0, qt0 = 0, qb1 = 0, qh1 = 0, qt1 = 0;   // slots 0 and 1
+        long long last = -1;   // index of the walk's last chunk, once known
+        auto load = [&](long long k) {   // the k-th chunk into buffer k % 2
+            const int b = (k & 1) ? qb1 : qb0, hh = (k & 1) ? qh1 : qh0;
+            const int i = (int)(k & 1);
+            unsigned char* in = sm + i * Layout::kInBytes;
+            uint64_t* full = &bar[kInFull + i];
+            const int t0 = (k & 1) ? qt1 : qt0;
+            ptx::mbar_arrive_expect_tx(full, in_bytes);
+            ptx::tma_load_3d(in + Layout::kC, &tmC, full, 0, t0, (int)b);
+            ptx::tma_load_3d(in + Layout::kB, &tmB, full, 0, t0, (int)b);
+            if (two_regions) {
+                ptx::tma_load_3d(in + Layout::kC + 16384, &tmC, full, 64, t0, (int)b);
+                ptx::tma_load_3d(in + Layout::kB + 16384, &tmB, full, 64, t0, (int)b);
+            }
+            ptx::tma_load_4d(in + Layout::kX, &tmX, full, 0, (int)hh, t0, (int)b);
+        };
+        // The descriptors of a product are formed once and stepped per K
+        // slice: the start address sits in the low 14 bits (in 16-byte
+        // units; shared memory is below 256 KB), so adding a slice's offset
+        // in 16-byte units moves only that field.  Each MMA is then an add
+        // and the instruction; this thread shares its SM sub-partition with
+        // two epilogue warps, and the tensor cores wait for what it issues.
+        // K-major operands (C, and B as S's operand): slice k at
+        // (k / 4) * 16384 + (k % 4) * 32 bytes; MN-major ones: k * 2048.
+        auto koff = [](int k) { return (uint64_t)((k >> 2) * 1024 + (k & 3) * 2); };
+        auto issue_s = [&](long long c) {   // S = C B^T
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            const uint64_t da = sdesc(in + Layout::kC, 16, 1024), db = sdesc(in + Layout::kB, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(tmem + kColS, da + koff(k), db + koff(k), idS, k > 0);
+            mma_commit(&bar[kMmaS]);
+        };
+        auto issue_yx = [&](long long c) {   // Yx = C H into buffer c % 2, H as hi then lo
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            const uint32_t col = tmem + ((c & 1) ? kColYx1 : kColYx0);
+            const uint64_t da = sdesc(in + Layout::kC, 16, 1024);
+            const uint64_t dh = sdesc(sHh, 16384, 1024), dl = sdesc(sHl, 16384, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(col, da + koff(k), dh + (uint64_t)(k * 128), idY, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(col, da + koff(k), dl + (uint64_t)(k * 128), idY, 1);
+            mma_commit(&bar[kMmaYx]);
+        };
+        auto issue_g = [&](long long c) {   // G = B^T (w o X)
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            const uint64_t db = sdesc(in + Layout::kB, 16384, 1024);
+            const uint64_t dh = sdesc(sWh, 16384, 1024), dl = sdesc(sWl, 16384, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma(tmem + kColG, db + (uint64_t)(k * 128), dh + (uint64_t)(k * 128), idG, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma(tmem + kColG, db + (uint64_t)(k * 128), dl + (uint64_t)(k * 128), idG, 1);
+            mma_commit(&bar[kMmaG]);
+        };
+        auto issue_yi = [&](long long c) {   // Yi = (masked S) X
+            const uint32_t in = s0 + (uint32_t)((c & 1) * Layout::kInBytes);
+            const uint64_t dx = sdesc(in + Layout::kX, 16384, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma_ta(tmem + kColYi, tmem + kColSh + 8 * k, dx + (uint64_t)(k * 128), idY, k > 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma_ta(tmem + kColYi, tmem + kColSl + 8 * k, dx + (uint64_t)(k * 128), idY, 1);
+            mma_commit(&bar[kMmaYi]);
+        };
+        auto wait = [&](int which, long long k) {   // k-th completion of a barrier, whole warp
+            return __all_sync(0xffffffffu, bwait(&bar[which], (uint32_t)(k & 1), a.wait_ns));
+        };
+        // raw dt of the steps 4 lane .. 4 lane + 3 of a chunk (a chunk ahead),
+        // with its head's A, dt_bias and D, kept as loaded: nothing here uses
+        // the values, so the loads complete while this warp goes on (steps
+        // past L read the last one, and the decay masks them)
+        unsigned short raw[4];
+        float rawA = 0.0f, rawbias = 0.0f, rawdsk = 0.0f;
+        ChunkRec rec;   // of the chunk whose dt is held
+        long long ndt = 0, nscan = 0;   // chunks whose dt was loaded; scanned
+        auto load_dt = [&]() {   // chunk cur, the ndt-th
+            const Walk ch = cur;
+            const int b = ch.j / (int)a.H, hh = ch.j - b * (int)a.H;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const long long t = (long long)ch.c * Q + 4 * lane + j;
+                raw[j] = reinterpret_cast<const unsigned short*>(a.dt)[((long long)b * a.L + (t < a.L ? t : a.L - 1)) * a.H + hh];
+            }
+            rawA = ld_early(a.A + hh);
+            rawbias = a.dt_bias ? ld_early(a.dt_bias + hh) : 0.0f;
+            rawdsk = a.Dskip ? ld_early(a.Dskip + hh) : 0.0f;
+            rec.b = b;
+            rec.h = hh;
+            rec.c = ch.c;
+            rec.nv = (int)(a.L - (long long)ch.c * Q < Q ? a.L - (long long)ch.c * Q : Q);
+            rec.j = ch.j;
+            rec.sg = ch.sg;
+            rec.start = ch.c != ch.sg * a.seg ? kCont : ch.sg == 0 ? kZero : kHand;
+            rec.end = ch.c != ch.hi - 1 ? kEndNone : ch.hi == nchunks ? kEndHead : kEndHand;
+            if (ndt & 1) {
+                qb1 = b;
+                qh1 = hh;
+                qt1 = ch.c * Q;
+            } else {
+                qb0 = b;
+                qh0 = hh;
+                qt0 = ch.c * Q;
+            }
+            // the next chunk: the unit's next, or the first of the next ticket's
+            if (cur.c + 1 < cur.hi) {
+                ++cur.c;
+                rec.next = kCont;
+            } else {
+                unsigned long long t = 0;
+                if (lane == 0) t = a.ticket ? atomicAdd(a.ticket, 1ull) : ~0ull;
+                t = __shfl_sync(0xffffffffu, t, 0);
+                if ((long long)t < units && t != ~0ull) {
+                    cur.unit((long long)t, heads, a.seg, nchunks);
+                    rec.next = cur.sg == 0 ? kZero : kHand;
+                } else {
+                    rec.next = kNone;
+                    last = ndt;
+                }
+            }
+            rec.nj = cur.j;
+            rec.nsg = cur.sg;
+            ++ndt;
+        };
+        // step sizes and cumulative decay of the chunk whose dt load_dt holds
+        // into the shared copy (its previous readers, the masked scores of the
+        // chunk before, are done), and its record into its slot (last read
+        // by the outputs of the chunk two before, which precede those scores)
+        auto scan = [&]() {   // the chunk whose dt load_dt holds
+            const int nv = rec.nv;
+            const float A = rawA, kb2 = rawbias * kLog2e;
+            float d[4], cl[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float v2 = fmaf(__bfloat162float(__ushort_as_bfloat16(raw[j])), kLog2e, kb2);
+                const float sp = (v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2))) * 0.6931471805599453f;
+                d[j] = 4 * lane + j < nv ? sp : 0.0f;
+                cl[j] = (j ? cl[j - 1] : 0.0f) + A * d[j];
+            }
+            float inc = cl[3];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            const float ex = inc - cl[3];
+            *reinterpret_cast<float4*>(cum + 4 * lane) =
+                make_float4((cl[0] + ex) * kLog2e, (cl[1] + ex) * kLog2e, (cl[2] + ex) * kLog2e,
+                            (cl[3] + ex) * kLog2e);
+            *reinterpret_cast<float4*>(dts + 4 * lane) = make_float4(d[0], d[1], d[2], d[3]);
+            if (leader) {   // read by the chunk's state update and outputs
+                rec.dsk = rawdsk;
+                recs[nscan & 1] = rec;
+            }
+            ++nscan;
+            __syncwarp();
+            if (leader) ptx::mbar_arrive(&bar[kCum]);
+        };
+        if (warp == kLdr) {
+            // The first two chunks' copies and chunk 0's decay; then, per
+            // chunk c, the copies of chunk c + 1 once the outputs of chunk
+            // c - 1 are done with its buffer, and the decay of chunk c + 1
+            // once the scores of chunk c have read the shared copy (the
+            // order in which the epilogue's iteration for chunk c frees them).
+            // whether the walk has a k-th chunk (known once the walk has
+            // passed the chunk before)
+            auto more = [&](long long k) { return last < 0 || k <= last; };
+            load_dt();
+            scan();
+            if (more(1)) load_dt();
+            if (leader) {
+                load(0);
+                if (more(1)) load(1);
+            }
+            for (long long c = 0; more(c + 1) && !failed; ++c) {
+                if (c > 0) {
+                    if (!wait(kInFree + (int)((c - 1) & 1), (c - 1) >> 1)) { failed = true; break; }
+                    if (leader) load(c + 1);
+                }
+                if (!wait(kEpReady, c)) { failed = true; break; }
+                scan();
+                if (more(c + 2)) load_dt();
+            }
+            // Every copy issued here is waited for by the product warp
+            // before the products that read it.
+            if (failed && leader) atomicOr(&g_error_word, kErrTimeout);
+            __syncwarp();
+        } else {
+            // chunk 0's S and C H (of the zero state)
+            if (!wait(kInFull, 0)) failed = true;
+            if (!failed) {
+                fence_after_sync();
+                if (leader) issue_s(0);
+                if (!wait(kHReady, 0)) failed = true;
+            }
+            if (!failed) {
+                fence_after_sync();
+                if (leader) issue_yx(0);
+            }
+            // Each product goes as soon as what it reads is written and its
+            // accumulator has been read, in the order the epilogue's phases
+            // produce them within its iteration for chunk c (the state after
+            // chunk c - 1, w o X of chunk c, the outputs of chunk c - 1, the
+            // masked scores of chunk c): this thread issues in order, so a
+            // wait on a later event would hold back an earlier product.
+            long long c = 0;
+            for (;; ++c) {
+                if (c > 0) {
+                    // The state entering chunk c is written, and every
+                    // epilogue warp has read G of chunk c - 1.  C H of chunk
+                    // c goes into buffer c % 2, last read by the outputs of
+                    // chunk c - 2, which precede the scores of chunk c - 1
+                    // (kEpReady, seen in the previous iteration); C of chunk
+                    // c landed before its S went.
+                    if (!wait(kHReady, c)) { failed = true; break; }
+                    fence_after_sync();
+                    if (leader) issue_yx(c);
+                }
+                // G(c): w o X of chunk c is written
+                if (!wait(kWxReady, c)) { failed = true; break; }
+                fence_after_sync();
+                if (leader) issue_g(c);
+                // Yi(c): the masked scores of chunk c are in TMEM; then S of
+                // chunk c + 1 (S of chunk c has been read)
+                if (!wait(kEpReady, c)) { failed = true; break; }
+                fence_after_sync();
+                if (leader) issue_yi(c);
+                // the chunk's record (written before its scores) says
+                // whether another chunk follows
+                if (recs[c & 1].next == kNone) break;
+                if (!wait(kInFull + (int)((c + 1) & 1), (c + 1) >> 1)) { failed = true; break; }
+                fence_after_sync();
+                if (leader) issue_s(c + 1);
+            }
+            // Leave no product in flight (bounded): the last chunk's Yi,
+            // the last product issued, completes after all of them; a
+            // parity wait names the last phase alone, and Yi of the chunk
+            // before completed (the outputs of that chunk, which precede
+            // the last chunk's scores, waited for it).
+            if (!failed && !wait(kMmaYi, c)) failed = true;
+            if (failed && leader) atomicOr(&g_error_word, kErrTimeout);
+            __syncwarp();
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3, hf = warp >> 2;   // TMEM lane quadrant; column half
+        const int row = 32 * quad + lane;            // step t, or state row n
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
+        float Hs[32];   // columns 32 hf .. 32 hf + 31 of row `row` of the state
+#pragma unroll
+        for (int j = 0; j < 32; ++j) Hs[j] = 0.0f;
+        // The state entering a chunk that starts a unit: zero at its head's
+        // start, else the one left by the head's segment before (done by
+        // whichever CTA took it, once all eight of its epilogue warps have
+        // released their parts).
+        auto enter = [&](int kind, int j, int sg) -> bool {
+            if (kind == kCont || kind == kNone) return true;
+            if (kind == kZero) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) Hs[i] = 0.0f;
+                return true;
+            }
+            if (!__all_sync(0xffffffffu,
+                            wait_count(a.done + j, (unsigned)(kEpWarps * sg), a.wait_ns)))
+                return false;
+            const float4* src = reinterpret_cast<const float4*>(
+                a.carry + ((long long)j * NP + row) * P + 32 * hf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 v = src[j];
+                Hs[4 * j] = v.x;
+                Hs[4 * j + 1] = v.y;
+                Hs[4 * j + 2] = v.z;
+                Hs[4 * j + 3] = v.w;
+            }
+            return true;
+        };
+        // The state after a chunk that ends a unit leaves: as h_last at its
+        // head's end, else for the head's next segment.
+        auto leave = [&](int kind, int j) {
+            if (kind == kEndNone) return;
+            if (kind == kEndHead) {
+                if (a.h_last && row < a.N) {
+                    float* base = a.h_last + (long long)j * P * a.N + row;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) base[(long long)(32 * hf + j) * a.N] = Hs[j];
+                }
+                return;
+            }
+            float4* dst = reinterpret_cast<float4*>(a.carry + ((long long)j * NP + row) * P + 32 * hf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(Hs[4 * i], Hs[4 * i + 1], Hs[4 * i + 2], Hs[4 * i + 3]);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) red_release_add(a.done + j, 1u);
+        };
+        // The state after the c-th chunk: H <- exp(cum_end) H + G (row n =
+        // row, this warp's 32 columns); it leaves if the chunk ends a piece,
+        // and the next chunk's entering state, if that starts one, replaces
+        // it; then its hi + lo copy for the next chunk's C H (the previous
+        // copy was read by this chunk's Yx, which completed).
+        auto state_update = [&](long long c, float dend) -> bool {
+            if (!wwait(&bar[kMmaG], (uint32_t)(c & 1), a.wait_ns) ||
+                !wwait(&bar[kMmaYx], (uint32_t)(c & 1), a.wait_ns))
+                return false;
+            fence_after_sync();
+            float g[32];
+            tmem_ld32(lane_addr + kColG + 32 * hf, g);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) Hs[j] = fmaf(dend, Hs[j], g[j]);
+            const ChunkRec& r = recs[c & 1];
+            leave(r.end, r.j);
+            if (!enter(r.next, r.nj, r.nsg)) return false;
+            store_split32(sm + Layout::kHh, sm + Layout::kHl, row, 4 * hf, Hs);
+            ptx::fence_proxy_async_shared();
+            fence_before_sync();
+            warp_arrive(&bar[kHReady], lane);
+            return true;
+        };
+        // The outputs of the c-th chunk, step t = row, this warp's 32 columns:
+        // Yi + exp(cum_t) Yx + Dskip x; then the chunk's buffer is free.
+        auto outputs = [&](long long c, float ecum) -> bool {
+            if (!wwait(&bar[kMmaYi], (uint32_t)(c & 1), a.wait_ns)) return false;
+            fence_after_sync();
+            const ChunkRec& r = recs[c & 1];
+            const long long b = r.b, hh = r.h, cc = r.c;
+            const float dsk = r.dsk;
+            const unsigned char* X = sm + (c & 1) * Layout::kInBytes + Layout::kX;
+            const int nv = r.nv;
+            float yi[32], yx[32];
+            tmem_ld32_nowait(lane_addr + kColYi + 32 * hf, yi);
+            tmem_ld32_nowait(lane_addr + ((c & 1) ? kColYx1 : kColYx0) + 32 * hf, yx);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            bf16* yrow = a.y + ((b * a.L + cc * Q + row) * a.H + hh) * P + 32 * hf;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(row, 4 * hf + cc));
+                const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+                uint4 o;
+                uint32_t* op = &o.x;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __bfloat1622float2(x2[q]);
+                    const int j = 8 * cc + 2 * q;
+                    const __nv_bfloat162 r2 = __floats2bfloat162_rn(
+                        fmaf(dsk, f.x, fmaf(ecum, yx[j], yi[j])),
+                        fmaf(dsk, f.y, fmaf(ecum, yx[j + 1], yi[j + 1])));
+                    op[q] = *reinterpret_cast<const uint32_t*>(&r2);
+                }
+                if (row < nv) *reinterpret_cast<uint4*>(yrow + 8 * cc) = o;
+            }
+            // X (read above and by Yi) and B (read by G) are free for chunk c + 2
+            fence_before_sync();
+            warp_arrive(&bar[kInFree + (int)(c & 1)], lane);
+            return true;
+        };
+        // the state entering the first chunk, as its record (which comes
+        // with its decays) says
+        if (!wwait(&bar[kCum], 0u, a.wait_ns) || !enter(recs[0].start, recs[0].j, recs[0].sg))
+            failed = true;
+        store_split32(sm + Layout::kHh, sm + Layout::kHl, row, 4 * hf, Hs);
+        ptx::fence_proxy_async_shared();
+        fence_before_sync();
+        warp_arrive(&bar[kHReady], lane);
+        float ecum_prev = 0.0f, dend_prev = 0.0f;
+        for (long long c = 0; !failed; ++c) {
+            const uint32_t ph = (uint32_t)(c & 1);
+            const unsigned char* X = sm + (c & 1) * Layout::kInBytes + Layout::kX;
+            // the previous chunk's state (its G ran first) lets chunk c's C H go
+            if (c > 0 && !state_update(c - 1, dend_prev)) { failed = true; break; }
+            // the walk ended with the previous chunk: its outputs, and done
+            if (c > 0 && recs[(c - 1) & 1].next == kNone) {
+                if (!outputs(c - 1, ecum_prev)) failed = true;
+                break;
+            }
+            // this row's cumulative decay (log2 units) and step size, and the chunk's total
+            if (!wwait(&bar[kCum], ph, a.wait_ns)) { failed = true; break; }
+            const float ct = cum[row], cend2 = cum[Q - 1];
+            const float ecum = ptx::ex2(ct);                 // exp(cum_t)
+            const float dend = ptx::ex2(cend2);              // exp(cum_end)
+            if (!wwait(&bar[kInFull + (int)(c & 1)], (uint32_t)((c >> 1) & 1), a.wait_ns)) {
+                failed = true;
+                break;
+            }
+            // w o X, split hi + lo (the previous chunk's G, which read them,
+            // completed: state_update).  The causal mask gives the warps of
+            // lane quadrants 2 and 3 the most score columns, so the warps of
+            // quadrants 0 and 1 form all of w o X: warp e < 4 (quad 0 or 1,
+            // column half hf) takes rows s = 32 (e & 1) + lane and s + 64 of
+            // its column half, with the w_s of those rows from the shared copy.
+            if (quad < 2) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int s_ = 32 * quad + 64 * rr + lane;
+                    const float ws = ptx::ex2(cend2 - cum[s_]) * dts[s_];
+#pragma unroll
+                    for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
+                        const uint4 xv = *reinterpret_cast<const uint4*>(X + sw128(s_, cc));
+                        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+                        uint4 h, l;
+                        uint32_t* hp = &h.x;
+                        uint32_t* lp = &l.x;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = __bfloat1622float2(x2[q]);
+                            split2(ws * f.x, ws * f.y, hp[q], lp[q]);
+                        }
+                        *reinterpret_cast<uint4*>(sm + Layout::kWh + sw128(s_, cc)) = h;
+                        *reinterpret_cast<uint4*>(sm + Layout::kWl + sw128(s_, cc)) = l;
+                    }
+                }
+                ptx::fence_proxy_async_shared();   // w o X, for the tensor cores (G)
+                warp_arrive(&bar[kWxReady], lane);
+            }
+            // the previous chunk's outputs (its Yi ran after G)
+            if (c > 0 && !outputs(c - 1, ecum_prev)) { failed = true; break; }
+            // masked scores of row t = row, pieces hf and hf + 2 (32 columns
+            // each): S[t,s] exp(cum_t - cum_s) dt_s for s <= t, into TMEM as
+            // packed bf16 hi and lo (the previous chunk's Yi, which read them,
+            // completed: outputs)
+            if (!wwait(&bar[kMmaS], ph, a.wait_ns)) {
+                failed = true;
+                break;
+            }
+            fence_after_sync();
+            float sv[2][32];
+            tmem_ld32_nowait(lane_addr + kColS + 32 * hf, sv[0]);
+            if (hf + 2 <= quad) tmem_ld32_nowait(lane_addr + kColS + 32 * (hf + 2), sv[1]);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int piece = hf + 2 * k;
+                uint32_t hi[16], lo[16];
+                if (piece <= quad) {   // some s of the piece are <= t (warp-uniform)
+                    float (&v)[32] = sv[k];
+                    const float4* cum4 = reinterpret_cast<const float4*>(cum + 32 * piece);
+                    const float4* dt4 = reinterpret_cast<const float4*>(dts + 32 * piece);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 cq = cum4[j4], dq = dt4[j4];
+                        const float cs[4] = {cq.x, cq.y, cq.z, cq.w}, ds[4] = {dq.x, dq.y, dq.z, dq.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 4 * j4 + e, s_ = 32 * piece + j;
+                            v[j] = s_ <= row ? v[j] * ptx::ex2(ct - cs[e]) * ds[e] : 0.0f;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) split2(v[2 * j], v[2 * j + 1], hi[j], lo[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) hi[j] = lo[j] = 0u;
+                }
+                tmem_st16(lane_addr + kColSh + 16 * piece, hi);
+                tmem_st16(lane_addr + kColSl + 16 * piece, lo);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            ptx::fence_proxy_async_shared();   // w o X, for the tensor cores
+            fence_before_sync();
+            warp_arrive(&bar[kEpReady], lane);
+            ecum_prev = ecum;
+            dend_prev = dend;
+        }
+        if (failed && lane == 0) atomicOr(&g_error_word, kErrTimeout);
+    }
+    // ---- tear-down: every TMEM access and MMA is done before the columns go
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == kCtl)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
 }  // namespace ssdtc
 }  // namespace ssm
 
@@ -713,11 +1373,42 @@ namespace ssdtc {
 
 // bf16, P == 64, N == 64 or 128, x, B, C, y 16-byte aligned, batch*H > 0,
 // L > 0 (checked by the caller).
+//
+// Which walk: one head per CTA (the block scheduler hands heads to SMs as
+// they free up) unless that leaves the last wave mostly empty -- the waves,
+// rounded up, more than 15% above the heads' share of the SMs -- as 320 heads
+// on 148 SMs do (2.16 waves, run as 3).  Then the ticket walk (DYN), whose
+// per-chunk bookkeeping cost 5-15% where the waves were full (measured).  Its
+// segments are about a sixteenth of a CTA's share of the chunks, and the
+// ticket, the per-head counters and the states handed between segments live
+// in a stream-ordered workspace of about heads x 32 KB, freed on the stream
+// after the launch; a failed allocation returns cudaErrorMemoryAllocation.
+// `want_seg` > 0 or `want_ctas` > 0 (development and tests) ask for the
+// ticket walk with segments of that many chunks and at most that many CTAs.
+// The one-head walk's arguments, from the ticket walk's.
+inline Args one_head(const ArgsDyn& d) {
+    Args a;
+    a.x = d.x;
+    a.dt = d.dt;
+    a.dt_bias = d.dt_bias;
+    a.A = d.A;
+    a.Dskip = d.Dskip;
+    a.y = d.y;
+    a.h_last = d.h_last;
+    a.batch = d.batch;
+    a.L = d.L;
+    a.H = d.H;
+    a.N = d.N;
+    a.wait_ns = d.wait_ns;
+    return a;
+}
+
 inline cudaError_t launch_ssd_tc(const bf16* x, const bf16* dt, const float* dt_bias,
                                  const float* A, const bf16* Bm, const bf16* Cm,
                                  const float* Dskip, bf16* y, float* h_last, long long batch,
                                  long long L, long long H, int N, unsigned long long wait_ns,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, long long want_seg = 0,
+                                 long long want_ctas = 0) {
     CUtensorMap mX, mB, mC;
     const cuuint64_t es = 2;
     const cuuint64_t dX[4] = {(cuuint64_t)P, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)batch};
@@ -731,7 +1422,30 @@ inline cudaError_t launch_ssd_tc(const bf16* x, const bf16* dt, const float* dt_
         !tma::cached_map(&mB, bf, 3, Bm, dBC, sBC, bBC, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tma::cached_map(&mC, bf, 3, Cm, dBC, sBC, bBC, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    Args a;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long heads = batch * H, nch = (L + Q - 1) / Q;
+    if (nch >= (1ll << 30)) return cudaErrorInvalidValue;   // chunk indices are int
+    const long long waves = (heads + sms - 1) / sms;
+    const bool dyn = (heads > sms && waves * sms * 100 > heads * 115) || want_seg > 0 ||
+                     want_ctas > 0;
+    // segment length (DYN): about a sixteenth of a CTA's share of the chunks
+    long long U = nch;
+    if (dyn) {
+        U = (heads * nch + 16LL * sms - 1) / (16LL * sms);
+        if (U > nch) U = nch;
+        if (want_seg > 0) U = want_seg < nch ? want_seg : nch;
+    }
+    const long long nseg = (nch + U - 1) / U, units = heads * nseg;
+    long long G = dyn ? (units < sms ? units : sms) : heads;
+    if (want_ctas > 0 && want_ctas < G) G = want_ctas;
+    ArgsDyn a;
+    a.ticket = nullptr;
+    a.carry = nullptr;
+    a.done = nullptr;
+    a.seg = (int)U;
     a.x = x;
     a.dt = dt;
     a.dt_bias = dt_bias;
@@ -744,12 +1458,39 @@ inline cudaError_t launch_ssd_tc(const bf16* x, const bf16* dt, const float* dt_
     a.H = H;
     a.N = N;
     a.wait_ns = wait_ns;
-    cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Layout::kSmemBytes);
+    const int smem = dyn ? LayoutDyn::kSmemBytes : Layout::kSmemBytes;
+    e = dyn ? cudaFuncSetAttribute(ssd_tc_dyn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+            : cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (fault::launch_refused()) return cudaErrorLaunchFailure;
-    ssd_tc_kernel<<<(unsigned)(batch * H), THREADS, Layout::kSmemBytes, s>>>(mX, mB, mC, a);
-    return cudaGetLastError();
+    unsigned char* ws = nullptr;
+    if (dyn && (G < units || nseg > 1)) {   // tickets (more units than CTAs); hand-offs (heads cut)
+        const size_t head_bytes = (8 + (size_t)heads * 4 + 255) & ~(size_t)255;
+        const size_t bytes = head_bytes + (nseg > 1 ? (size_t)heads * NP * P * sizeof(float) : 0);
+        if (fault::malloc_async(reinterpret_cast<void**>(&ws), bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            return cudaErrorMemoryAllocation;
+        }
+        if (G < units) a.ticket = reinterpret_cast<unsigned long long*>(ws);
+        a.done = reinterpret_cast<unsigned*>(ws + 8);
+        if (nseg > 1) a.carry = reinterpret_cast<float*>(ws + head_bytes);
+        e = cudaMemsetAsync(ws, 0, head_bytes, s);
+    }
+    if (e == cudaSuccess) {
+        if (fault::launch_refused()) {
+            e = cudaErrorLaunchFailure;
+        } else {
+            if (dyn)
+                ssd_tc_dyn_kernel<<<(unsigned)G, THREADS, smem, s>>>(mX, mB, mC, a);
+            else
+                ssd_tc_kernel<<<(unsigned)G, THREADS, smem, s>>>(mX, mB, mC, one_head(a));
+            e = cudaGetLastError();
+        }
+    }
+    if (ws) {
+        const cudaError_t f = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = f;
+    }
+    return e;
 }
 
 }  // namespace ssdtc

@@ -144,3 +144,30 @@ def test_launch_injection_covers_step_ssd_and_noalloc():
         assert status_of(fn) == 0
     torch.cuda.synchronize()
     assert ssm.ssm_device_status() == 0
+
+
+def test_ssd_ticket_walk_reports_injected_failure_then_recovers():
+    """The SSD kernel's ticket walk takes a workspace (its ticket, the
+    per-head counters and states): a failed allocation or launch is reported
+    and the next call gives the oracle's result."""
+    from tests.test_gpu_ssd import oracle_ssd
+    q = wl.make_ssd_inputs(wl.SSD_SMALL, device=DEV, batch=2, L=300, H=3, N=128)
+    y = torch.empty_like(q["x"])
+    h = torch.empty((2, 3, 64, 128), device=DEV)
+
+    def ssd():
+        ssm.ssm_ssd_fwd(q["x"], q["dt"], q["dt_bias"], q["A"], q["B"], q["C"], q["Dskip"], y, h)
+
+    with env(SSM_SSD_SEG="1", SSM_SSD_CTAS="4"):
+        with env(SSM_FAULT_INJECT="alloc"):
+            assert status_of(ssd) == NOMEM
+        with env(SSM_FAULT_INJECT="launch"):
+            assert status_of(ssd) == CUDA_ERR
+        torch.cuda.synchronize()
+        assert ssm.ssm_device_status() == 0
+        assert status_of(ssd) == 0
+        torch.cuda.synchronize()
+    assert ssm.ssm_device_status() == 0
+    y_ref, h_ref = oracle_ssd(q)
+    parity.check(parity.to_f64(y), y_ref, 2e-2, "ssd y after injection")
+    parity.check(parity.to_f64(h), h_ref, 2e-2, "ssd h_last after injection")

@@ -61,6 +61,40 @@ def test_ssd_parity(monkeypatch, shape):
     parity.check(parity.to_f64(h), h_ref, tol, f"{shape} h_last")
 
 
+# The ticket walk (heads cut into segments, persistent CTAs taking them from a
+# counter, each head's state passed between segments through global memory),
+# forced on small shapes: (batch, L, H, N, chunks per segment, CTAs).
+TICKET_SHAPES = [
+    (2, 640, 4, 128, 1, 0),     # every chunk its own segment, one per CTA
+    (2, 640, 4, 128, 2, 3),     # 24 units on 3 CTAs
+    (2, 383, 3, 64, 1, 4),      # ragged last chunk, N = 64
+    (1, 1000, 5, 128, 3, 2),    # segments of 3 chunks, the last one short
+    (3, 300, 7, 128, 0, 5),     # whole heads, 21 units on 5 CTAs
+    (1, 128, 1, 128, 1, 1),     # one chunk, one unit
+]
+
+
+@pytest.mark.parametrize("shape", TICKET_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_ssd_ticket_walk_parity(monkeypatch, shape):
+    b, L, H, N, seg, ctas = shape
+    if seg:
+        monkeypatch.setenv("SSM_SSD_SEG", str(seg))
+    if ctas:
+        monkeypatch.setenv("SSM_SSD_CTAS", str(ctas))
+    inp = wl.make_ssd_inputs(wl.SSD_SMALL, device=DEV, batch=b, L=L, H=H, P=64, N=N,
+                             dtype=torch.bfloat16)
+    y, h = run_ssd(inp)
+    assert ssm.ssm_device_status() == 0
+    y_ref, h_ref = oracle_ssd(inp)
+    parity.check(parity.to_f64(y), y_ref, 2e-2, f"{shape} y")
+    parity.check(parity.to_f64(h), h_ref, 2e-2, f"{shape} h_last")
+    # the same bits as one head per CTA
+    monkeypatch.delenv("SSM_SSD_SEG", raising=False)
+    monkeypatch.delenv("SSM_SSD_CTAS", raising=False)
+    y1, h1 = run_ssd(inp)
+    assert torch.equal(y1, y) and torch.equal(h1, h)
+
+
 def test_ssd_nulls_and_empty():
     inp = wl.make_ssd_inputs(wl.SSD_SMALL, device=DEV, batch=1, L=100, H=2)
     q = dict(inp, dt_bias=None, Dskip=None)
@@ -75,7 +109,9 @@ def test_ssd_nulls_and_empty():
 
 def test_ssd_mamba2_2p7b_sampled_heads():
     """The 4 x 4096 x (80 heads x 64) layer with N = 128 on the tensor-core
-    kernel; every output of sampled heads against the oracle.  The sample
+    kernel (the ticket walk: 320 heads on the SMs of a B300 would leave a last
+    wave of 24 CTAs, so every head runs as segments on several CTAs); every
+    output of sampled heads against the oracle.  The sample
     always holds the six most slowly decaying heads (smallest |A|), whose long
     memories make the largest states and the most cancellation in y: rounding
     the bf16 operands of the products once (without a low part) put y 4.6% off
