@@ -1379,7 +1379,7 @@ namespace ssdtc {
 // rounded up, more than 15% above the heads' share of the SMs -- as 320 heads
 // on 148 SMs do (2.16 waves, run as 3).  Then the ticket walk (DYN), whose
 // per-chunk bookkeeping cost 5-15% where the waves were full (measured).  Its
-// segments are about a sixteenth of a CTA's share of the chunks, and the
+// segments are about a sixth of a CTA's share of the chunks, and the
 // ticket, the per-head counters and the states handed between segments live
 // in a stream-ordered workspace of about heads x 32 KB, freed on the stream
 // after the launch; a failed allocation returns cudaErrorMemoryAllocation.
@@ -1431,11 +1431,19 @@ inline cudaError_t launch_ssd_tc(const bf16* x, const bf16* dt, const float* dt_
     const long long waves = (heads + sms - 1) / sms;
     const bool dyn = (heads > sms && waves * sms * 100 > heads * 115) || want_seg > 0 ||
                      want_ctas > 0;
-    // segment length (DYN): about a sixteenth of a CTA's share of the chunks
+    // segment length (DYN): the head cut into equal segments of about a sixth
+    // of a CTA's share of the chunks.  Measured on the 2.7B layer (32 chunks
+    // per head, 69 per CTA), on one box: segments of 2, 3, 4, 5, 8, 11, 16, 32
+    // chunks took 0.389, 0.353, 0.337, 0.327, 0.324, 0.313, 0.326, 0.376 ms;
+    // on another, 5, 8 and 11 took 0.330, 0.325 and 0.325 -- each unit costs
+    // about 3 us of hand-off and restart, and the tail is up to a unit.
     long long U = nch;
     if (dyn) {
-        U = (heads * nch + 16LL * sms - 1) / (16LL * sms);
-        if (U > nch) U = nch;
+        const long long share = heads * nch / sms;   // chunks per CTA
+        long long nseg = share > 0 ? (6 * nch + share - 1) / share : 1;
+        if (nseg < 1) nseg = 1;
+        if (nseg > nch) nseg = nch;
+        U = (nch + nseg - 1) / nseg;
         if (want_seg > 0) U = want_seg < nch ? want_seg : nch;
     }
     const long long nseg = (nch + U - 1) / U, units = heads * nseg;
