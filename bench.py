@@ -719,7 +719,8 @@ def bench_ssd(ssm, dev, stream, reps: int = 5):
             "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (best * 1e-3) / 1e9,
             "tensor_path": "tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM), TMA 128B-swizzled "
                            "operand tiles",
-            "note": "best of %d; one launch per call" % reps}
+            "note": "best of %d; one kernel launch per call (320 heads on 148 SMs: the ticket "
+                    "walk, whose workspace counters are cleared by a memset first)" % reps}
 
 
 def launches_per_call(w) -> int:
