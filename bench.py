@@ -676,9 +676,9 @@ def bench_backward(ssm, inp, w, stream, reps: int = 5):
                 "note": "ssm_scan_bwd_ckpt reading the unit states that ssm_scan_fwd_ckpt "
                         "wrote (no summary pass of its own); forward_ms is that forward "
                         "pass, y and h_last as ssm_scan_fwd plus the states"},
-            "note": "one ssm_scan_bwd call: the chained forward scan writing the state "
-                    "entering every 32-step unit (its y into du), adjoint summaries + carry, "
-                    "the unit kernel, the dB/dC reduction; best of %d" % reps}
+            "note": "one ssm_scan_bwd call: the forward scan's chained walk writing only the "
+                    "state entering every 32-step unit, adjoint summaries + carry, the unit "
+                    "kernel, the dB/dC reduction; best of %d" % reps}
 
 
 def bench_ssd(ssm, dev, stream, reps: int = 5):

@@ -78,8 +78,9 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
         return SSM_ERR_CUDA;
     // Without the forward pass's checkpoints, the states entering the units
     // come from the forward scan itself when it would run its chained plan
-    // (the chains fill the GPU): one pass, which writes every unit boundary's
-    // state and a y that goes into du (the unit kernel overwrites all of du).
+    // (the chains fill the GPU): one pass of its chained walk that writes
+    // every unit boundary's state and nothing else (no C, z, readout or y;
+    // du only lends its tensor map).
     // That is cheaper than the unit summaries and their carry below, which
     // remain for problems with too few chains, where the forward itself
     // would run them and an output pass besides.
@@ -93,7 +94,7 @@ int launch_scan_bwd16(const T* u, const T* delta, const float* dt_bias, const fl
         }
         const int st = launch_scan_tile<T, (int)kZOH>(u, delta, dt_bias, A, Bm, Cm, Dskip, z, du,
                                                       nullptr, batch, L, D, kPlanChained, stream,
-                                                      nullptr, nullptr, 0, own_ckpt);
+                                                      nullptr, nullptr, 0, own_ckpt, true);
         if (st != SSM_OK) {
             cudaFreeAsync(own_ckpt, stream);
             return st;

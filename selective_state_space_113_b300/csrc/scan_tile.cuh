@@ -24,7 +24,7 @@
 // Warp w runs on SM sub-partition w % 4, so each sub-partition holds one
 // consumer (FMA-bound) next to its helper (SFU-bound).
 //
-// Three plans use this kernel:
+// Three plans and the backward's first phase use this kernel:
 //   kChained   -- a static split: the chain-major space of (chain, stage) is
 //                 cut into one equal contiguous range per CTA, and each CTA
 //                 walks its range from the last chain to the first.  A chain
@@ -40,6 +40,9 @@
 //                 state (the unit's affine summary; no y is written).
 //   kFromState -- phase 3: each unit starts from a state computed by the carry
 //                 kernel (phase 2) from the phase-1 summaries, and writes y.
+//   kCkptOnly  -- kChained's walk that writes only the states entering each
+//                 32-step unit (the backward pass's checkpoints): no C or z
+//                 copies, no readout, no y.
 //
 // Per-step arithmetic (geometric A, A[d,n] = (n+1) a0, detected per warp):
 //   v2 = delta*log2(e) + dt_bias*log2(e);  x = 2^v2 = e^(delta+bias)
@@ -106,7 +109,14 @@ constexpr unsigned kSleepNs = 64;   // back-off of the TMA warp's waits
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-enum Mode : int { kChained = 0, kAggregate = 1, kFromState = 2 };
+// kCkptOnly: the chained walk that writes only the state checkpoints (no C,
+// z, readout or y), the backward pass's first phase.
+enum Mode : int { kChained = 0, kAggregate = 1, kFromState = 2, kCkptOnly = 3 };
+
+// Whether a mode forms y (and so reads C and z), and whether it walks whole
+// chains with its predecessor's state.
+__host__ __device__ constexpr bool forms_y(int mode) { return mode == kChained || mode == kFromState; }
+__host__ __device__ constexpr bool walks_chains(int mode) { return mode == kChained || mode == kCkptOnly; }
 
 // Steps per unit of the optional state checkpoints (the backward pass's unit).
 constexpr long long kCkptSteps = 32;
@@ -252,12 +262,12 @@ __device__ __forceinline__ void widen_rows(unsigned char* st, int row0, int lane
     for (int i = 0; i < kPairs / 32; ++i) {
         const int w = lane + 32 * i;
         bv[i] = make_float2(ld_elem(Br + 2 * w) * s0, ld_elem(Br + 2 * w + 1) * s1);
-        if (MODE != kAggregate) cv[i] = make_float2(ld_elem(Cr + 2 * w), ld_elem(Cr + 2 * w + 1));
+        if (forms_y(MODE)) cv[i] = make_float2(ld_elem(Cr + 2 * w), ld_elem(Cr + 2 * w + 1));
     }
 #pragma unroll
     for (int i = 0; i < kPairs / 32; ++i) {
         Bc[lane + 32 * i] = bv[i];
-        if (MODE != kAggregate) Cc[lane + 32 * i] = cv[i];
+        if (forms_y(MODE)) Cc[lane + 32 * i] = cv[i];
     }
 }
 
@@ -317,7 +327,7 @@ __device__ int fill_header(unsigned char* st, const Params& p, long long b, long
     *has_state = false;
     *ok_out = true;
     const float* src = nullptr;
-    if (MODE == kChained && k > 0) {
+    if (walks_chains(MODE) && k > 0) {
         // Lane w polls the flag of sub-block w (bounded); the state is read
         // only once all four predecessors have published.
         bool ok = true;
@@ -407,7 +417,7 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
         // agree to float32 and 2^v2 could overflow
         const float dl = v2 > 28.853901f ? v2 : ptx::lg2(1.0f + ptx::ex2(v2));
         float g = 1.0f;
-        if (MODE != kAggregate) {
+        if (forms_y(MODE)) {
             if constexpr (HASZ) {
                 const float z = ld_elem(Z + t * CB + col);
                 g = z * ptx::rcp(1.0f + ptx::ex2(z * -kLog2e));
@@ -421,13 +431,13 @@ __device__ __forceinline__ void prologue_chunk(const unsigned char* st, int row0
             else o[j].y = dl * (0.5f * kLn2);
             if (DISC == kTrap) {
                 o[j].z = u;
-                o[j].w = MODE == kAggregate ? dl : g;
+                o[j].w = !forms_y(MODE) ? dl : g;
             } else {
-                o[j].z = MODE == kAggregate ? 0.0f : g;
-                o[j].w = MODE == kAggregate ? dl : sug;
+                o[j].z = !forms_y(MODE) ? 0.0f : g;
+                o[j].w = !forms_y(MODE) ? dl : sug;
             }
         } else {
-            o[j] = make_float4(dl, u, MODE == kAggregate ? 0.0f : g, MODE == kAggregate ? dl : sug);
+            o[j] = make_float4(dl, u, !forms_y(MODE) ? 0.0f : g, !forms_y(MODE) ? dl : sug);
         }
     }
 #pragma unroll
@@ -494,7 +504,7 @@ __device__ __forceinline__ void steps_geo(const unsigned char* st, int row0, int
                 H[k1] = ffma2(UP, Pn, ffma2(E, Sv, Sv));
                 P[k1] = Pn;
             }
-            if (MODE != kAggregate) {
+            if (forms_y(MODE)) {
                 const float4 c4 = C4[q];
                 Y0 = ffma2(make_float2(c4.x, c4.y), H[k0], Y0);
                 Y1 = ffma2(make_float2(c4.z, c4.w), H[k1], Y1);
@@ -502,13 +512,13 @@ __device__ __forceinline__ void steps_geo(const unsigned char* st, int row0, int
         }
         if (MODE == kAggregate) {
             S2 += pv.w;
-        } else {
+        } else if (forms_y(MODE)) {
             const float sum = (Y0.x + Y0.y) + (Y1.x + Y1.y);
             if (DISC == kTrap) yv[j] = fmaf(dsk, pv.z, sum) * pv.w;   // (sum + D u) g
             else yv[j] = fmaf(sum, pv.z, pv.w);                       // sum g + D u g
         }
     }
-    if (MODE != kAggregate) {
+    if (forms_y(MODE)) {
 #pragma unroll
         for (int j = 0; j < KP; ++j) {
             if (!FULL && j >= cnt) break;
@@ -558,11 +568,11 @@ __device__ __forceinline__ void steps_general(const unsigned char* st, int row0,
                 po = pn;
             }
             if (n & 1) H[n / 2].y = hn; else H[n / 2].x = hn;
-            if (MODE != kAggregate) y = fmaf(Cc[t * NS + n], hn, y);
+            if (forms_y(MODE)) y = fmaf(Cc[t * NS + n], hn, y);
         }
-        if (MODE != kAggregate) yv[j] = fmaf(y, pv.z, pv.w);
+        if (forms_y(MODE)) yv[j] = fmaf(y, pv.z, pv.w);
     }
-    if (MODE != kAggregate) {
+    if (forms_y(MODE)) {
 #pragma unroll
         for (int j = 0; j < KP; ++j) {
             if (j >= cnt) break;
@@ -611,21 +621,21 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             ptx::prefetch_tensormap(&tmU);
             ptx::prefetch_tensormap(&tmD);
             ptx::prefetch_tensormap(&tmB);
-            if (MODE != kAggregate) {
+            if (forms_y(MODE)) {
                 ptx::prefetch_tensormap(&tmC);
                 if (p.has_z) ptx::prefetch_tensormap(&tmZ);
             }
         }
         const uint32_t stage_tx =
-            (MODE == kAggregate) ? 2 * C::kTile + C::kRaw
+            !forms_y(MODE) ? 2 * C::kTile + C::kRaw
                                  : 2 * C::kTile + 2 * C::kRaw + (p.has_z ? C::kTile : 0);
-        // Piece source.  kChained: the CTA's range [r0, r1) of the
+        // Piece source.  kChained, kCkptOnly: the CTA's range [r0, r1) of the
         // chain-major stage space, walked from its last chain to its first.
         // Narrow-plan modes: units k * T .. (k+1) * T of a chain, from the
         // ticket counter.
         const long long r0 = (long long)blockIdx.x * p.Wst / (p.G > 0 ? p.G : 1);
         const long long r1 = ((long long)blockIdx.x + 1) * p.Wst / (p.G > 0 ? p.G : 1);
-        long long next_chain = (MODE == kChained) ? (r1 - 1) / (p.nst > 0 ? p.nst : 1) : 0;
+        long long next_chain = walks_chains(MODE) ? (r1 - 1) / (p.nst > 0 ? p.nst : 1) : 0;
         long long cur_chain = -1, cur_t0 = 0, cur_end = 0, cur_b = 0, cur_d0 = 0, cur_k = 0;
         bool chain_end = false;
         long long j = 0;
@@ -640,7 +650,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             int flags = 0, geo = 0;
             if (cur_chain < 0 || cur_t0 >= cur_end) {
                 bool more;
-                if (MODE == kChained) {
+                if (walks_chains(MODE)) {
                     more = r0 < r1 && next_chain >= r0 / p.nst;
                     if (more) {
                         const long long c = next_chain--;
@@ -711,7 +721,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
                 ptx::tma_load_3d(st + C::offU, &tmU, &full[slot], x, yy, z);
                 ptx::tma_load_3d(st + C::offD, &tmD, &full[slot], x, yy, z);
                 ptx::tma_load_3d(st + C::offBr, &tmB, &full[slot], 0, yy, z);
-                if (MODE != kAggregate) {
+                if (forms_y(MODE)) {
                     if (p.has_z) ptx::tma_load_3d(st + C::offZ, &tmZ, &full[slot], x, yy, z);
                     ptx::tma_load_3d(st + C::offCr, &tmC, &full[slot], 0, yy, z);
                 }
@@ -855,7 +865,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             Arow = p.A + (valid ? d : 0) * NS;
         }
         T* ytile = ytiles + (int)(j & 1) * (C::kY / (int)sizeof(T));
-        if (MODE != kAggregate) {
+        if (forms_y(MODE)) {
             // The store that last read this y buffer (two stages ago) must
             // have finished reading it.
             if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -883,7 +893,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             if (lane == 0) ptx::mbar_arrive(&pempty[NPB * w + buf]);
         }
         if (failed) break;
-        if (MODE != kAggregate && block_live) {
+        if (forms_y(MODE) && block_live) {
             // Hand the y tile to the TMA engine (rows past L and columns past
             // D fall outside the tensor and are not written).
             ptx::fence_proxy_async_shared();
@@ -907,7 +917,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
             }
         }
         if (m.flags & kLast) {
-            if (MODE == kChained) {
+            if (walks_chains(MODE)) {
                 if (!(m.flags & kChainEnd)) {
                     if (valid) {
                         float4* dst = reinterpret_cast<float4*>(p.carry + (b * p.D + d) * NS);
@@ -948,7 +958,7 @@ scan_tile_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant_
     }
     if (failed && lane == 0) raise_failure(p);
     // Every y store must have completed before the CTA's shared memory goes.
-    if (MODE != kAggregate && lane == 0) ptx::bulk_wait_group<0>();
+    if (forms_y(MODE) && lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();
 }
 

@@ -166,18 +166,31 @@ inline bool setup(CUtensorMap* maps, Params* p, const T* u, const T* delta, cons
 // u, delta, z, B, C, y, A and h_last 16-byte aligned, D * sizeof(T) % 16 == 0,
 // batch*D > 0, L > 0.
 // CONV: u is x, convolved with conv_w/conv_b (act: SiLU) before the scan.
+// ckpt_only (zero-order hold without the convolution, the chained plan, ckpt
+// given): only the checkpoints are written (kCkptOnly; y and h_last are not).
 template <typename T, int DISC, bool CONV = false>
 int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const float* A,
                      const T* Bm, const T* Cm, const float* Dskip, const T* z, T* y,
                      float* h_last, long long batch, long long L, long long D, int plan,
                      cudaStream_t stream, const float* conv_w = nullptr,
-                     const float* conv_b = nullptr, int act = 0, float* ckpt = nullptr) {
+                     const float* conv_b = nullptr, int act = 0, float* ckpt = nullptr,
+                     bool ckpt_only = false) {
     constexpr long long TC = Cfg<T>::TC;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SSM_ERR_CUDA;
     long long wc = 0, wa = 0, wf = 0;
+    if (ckpt_only) h_last = nullptr;   // not written; nor used to hand states over
+    if constexpr (DISC == kZOH && !CONV) {
+        if (ckpt_only) {
+            if (!ckpt || plan != kPlanChained) return SSM_ERR_UNSUPPORTED;
+            if (prepare<T, (int)kCkptOnly, DISC, CONV>(sms, &wc) != cudaSuccess || wc < 1)
+                return SSM_ERR_CUDA;
+        }
+    } else {
+        if (ckpt_only) return SSM_ERR_UNSUPPORTED;
+    }
     if (prepare<T, (int)kChained, DISC, CONV>(sms, &wc) != cudaSuccess ||
         prepare<T, (int)kAggregate, DISC, CONV>(sms, &wa) != cudaSuccess ||
         prepare<T, (int)kFromState, DISC, CONV>(sms, &wf) != cudaSuccess || wc < 1 || wa < 1 ||
@@ -247,8 +260,17 @@ int launch_scan_tile(const T* u, const T* delta, const float* dt_bias, const flo
         if (!narrow) {
             p.ticket = reinterpret_cast<unsigned long long*>(ws);
             p.carry = h_last ? h_last : reinterpret_cast<float*>(ws + off_carry);
-            if (launch_mode<T, (int)kChained, DISC, CONV>(p.G, maps, p, stream) != cudaSuccess)
-                status = SSM_ERR_CUDA;
+            cudaError_t le = cudaSuccess;
+            if constexpr (DISC == kZOH && !CONV) {
+                if (ckpt_only) {
+                    le = launch_mode<T, (int)kCkptOnly, DISC, CONV>(p.G, maps, p, stream);
+                } else {
+                    le = launch_mode<T, (int)kChained, DISC, CONV>(p.G, maps, p, stream);
+                }
+            } else {
+                le = launch_mode<T, (int)kChained, DISC, CONV>(p.G, maps, p, stream);
+            }
+            if (le != cudaSuccess) status = SSM_ERR_CUDA;
         } else {
             p.agg = reinterpret_cast<float*>(ws + off_agg);
             p.hin = reinterpret_cast<float*>(ws + off_hin);
