@@ -292,3 +292,22 @@ def test_checkpoints_refuse_other_state_sizes():
         ssm.ssm_scan_fwd_ckpt(inp["u"], inp["delta"], inp["dt_bias"], inp["A"], inp["B"],
                               inp["C"], inp["Dskip"], inp["z"], y, h, ckpt)
     assert e.value.status == -5
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_bwd_checkpoint_only_walk_matches_forward_checkpoints(monkeypatch, dtype):
+    """ssm_scan_bwd, on the chained plan, takes its unit states from the
+    forward recurrence's checkpoint-only walk (no readout, no y); the
+    training pair takes them from the forward scan proper.  The recurrence is
+    the same arithmetic, so every per-element output agrees bit for bit (the
+    sums formed with atomic adds, dA, ddt_bias and dDskip, to rounding), on a
+    shape with several chains cut into pieces and a ragged last unit."""
+    monkeypatch.setenv("SSM_FORCE_PLAN", "chained")
+    monkeypatch.setenv("SSM_CHUNK_T", "96")
+    inp = inputs(2, 500, 384, 16, dtype, 77)
+    _, _, _, pair = run_ckpt(inp)
+    own = run_bwd(inp)
+    for k in ("du", "ddelta", "dz", "dB", "dC"):
+        assert torch.equal(own[k], pair[k]), k
+    for k in ("dA", "ddt_bias", "dDskip"):
+        parity.check(parity.to_f64(own[k]), parity.to_f64(pair[k]), 1e-5, f"{k}")
