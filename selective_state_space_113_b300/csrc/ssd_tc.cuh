@@ -34,8 +34,12 @@
 // each in chunk order.  A unit's predecessor in its head went out `heads`
 // tickets earlier and has long finished when the unit needs its state, which
 // comes fp32 through global memory behind a counter the eight epilogue warps
-// release.  It is the launch's choice where one head per CTA would leave the
-// last wave mostly empty (see launch_ssd_tc).  Ten warps in both:
+// release.  Tickets go only to CTAs that are running, and a unit waits only
+// on a smaller ticket, taken by a CTA that walks its units in order: the walk
+// cannot deadlock, even with some CTAs not yet resident (another stream's
+// kernel on some SMs).  It is the launch's choice where one head per CTA
+// would leave the last wave mostly empty (see launch_ssd_tc).  Ten warps in
+// both:
 //   warp 8      products: one elected thread issues the MMAs, each as soon as
 //               what it reads is written and its accumulator has been read,
 //               in the order the epilogue produces them: C H of chunk c (the
