@@ -134,11 +134,12 @@ struct Args {
     unsigned long long wait_ns;
 };
 
-// The ticket walk's arguments: those of the one-head walk, and its own.  Kept
-// to 120 bytes, so that with the three 128-byte tensor maps the kernel's
-// parameters stay within 512 bytes: the one-head kernel, given 40 bytes more
-// (its parameters at 520 bytes), ran 13% slower, registers and shared memory
-// unchanged (measured).
+// The ticket walk's arguments: those of the one-head walk, and its own, in a
+// struct of its own.  The one-head kernel, given these fields after its own
+// (its parameters at 520 bytes instead of 480), ran 13% slower, registers and
+// shared memory unchanged; the ticket kernel ran the same with 504 or 488
+// bytes of parameters (measured; the cause was not isolated).  The parameters
+// are kept within 512 bytes.
 struct ArgsDyn {
     const bf16* x;
     const bf16* dt;
