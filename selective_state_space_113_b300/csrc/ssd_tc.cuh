@@ -1371,6 +1371,7 @@ ssd_tc_dyn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 }  // namespace ssdtc
 }  // namespace ssm
 
+#include "ssd_plan.h"
 #include "tma_host.cuh"
 
 namespace ssm {
@@ -1379,15 +1380,11 @@ namespace ssdtc {
 // bf16, P == 64, N == 64 or 128, x, B, C, y 16-byte aligned, batch*H > 0,
 // L > 0 (checked by the caller).
 //
-// Which walk: one head per CTA (the block scheduler hands heads to SMs as
-// they free up) unless that leaves the last wave mostly empty -- the waves,
-// rounded up, more than 15% above the heads' share of the SMs -- as 320 heads
-// on 148 SMs do (2.16 waves, run as 3).  Then the ticket walk (DYN), whose
-// per-chunk bookkeeping cost 5-15% where the waves were full (measured).  Its
-// segments are about a sixth of a CTA's share of the chunks, and the
-// ticket, the per-head counters and the states handed between segments live
-// in a stream-ordered workspace of about heads x 32 KB, freed on the stream
-// after the launch; a failed allocation returns cudaErrorMemoryAllocation.
+// Which walk, and the ticket walk's segments: plan() (ssd_plan.h).  The
+// ticket walk's ticket, per-head counters and the states handed between
+// segments live in a stream-ordered workspace of about heads x 32 KB, freed
+// on the stream after the launch; a failed allocation returns
+// cudaErrorMemoryAllocation.
 // `want_seg` > 0 or `want_ctas` > 0 (development and tests) ask for the
 // ticket walk with segments of that many chunks and at most that many CTAs.
 // The one-head walk's arguments, from the ticket walk's.
@@ -1433,27 +1430,9 @@ inline cudaError_t launch_ssd_tc(const bf16* x, const bf16* dt, const float* dt_
     if (e != cudaSuccess) return e;
     const long long heads = batch * H, nch = (L + Q - 1) / Q;
     if (nch >= (1ll << 30)) return cudaErrorInvalidValue;   // chunk indices are int
-    const long long waves = (heads + sms - 1) / sms;
-    const bool dyn = (heads > sms && waves * sms * 100 > heads * 115) || want_seg > 0 ||
-                     want_ctas > 0;
-    // segment length (DYN): the head cut into equal segments of about a sixth
-    // of a CTA's share of the chunks.  Measured on the 2.7B layer (32 chunks
-    // per head, 69 per CTA), on one box: segments of 2, 3, 4, 5, 8, 11, 16, 32
-    // chunks took 0.389, 0.353, 0.337, 0.327, 0.324, 0.313, 0.326, 0.376 ms;
-    // on another, 5, 8 and 11 took 0.330, 0.325 and 0.325 -- each unit costs
-    // about 3 us of hand-off and restart, and the tail is up to a unit.
-    long long U = nch;
-    if (dyn) {
-        const long long share = heads * nch / sms;   // chunks per CTA
-        long long nseg = share > 0 ? (6 * nch + share - 1) / share : 1;
-        if (nseg < 1) nseg = 1;
-        if (nseg > nch) nseg = nch;
-        U = (nch + nseg - 1) / nseg;
-        if (want_seg > 0) U = want_seg < nch ? want_seg : nch;
-    }
-    const long long nseg = (nch + U - 1) / U, units = heads * nseg;
-    long long G = dyn ? (units < sms ? units : sms) : heads;
-    if (want_ctas > 0 && want_ctas < G) G = want_ctas;
+    const Plan pl = plan(heads, nch, sms, want_seg, want_ctas);
+    const bool dyn = pl.dyn;
+    const long long U = pl.seg, nseg = pl.nseg, units = pl.units, G = pl.ctas;
     ArgsDyn a;
     a.ticket = nullptr;
     a.carry = nullptr;
