@@ -1190,7 +1190,7 @@ ssd_tc_dyn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             if (lane == 0) red_release_add(a.done + j, 1u);
         };
         // The state after the c-th chunk: H <- exp(cum_end) H + G (row n =
-        // row, this warp's 32 columns); it leaves if the chunk ends a piece,
+        // row, this warp's 32 columns); it leaves if the chunk ends a unit,
         // and the next chunk's entering state, if that starts one, replaces
         // it; then its hi + lo copy for the next chunk's C H (the previous
         // copy was read by this chunk's Yx, which completed).
